@@ -1,0 +1,164 @@
+/*
+ * lmhead.h - batch-invariant LM-head token log-probabilities for one GB300
+ * GPU (sm_103a). C ABI of liblmhead.so.
+ *
+ * What is computed (the "sampler formula"): for each token row t,
+ *   z[t, v]     = s * logits[t, v]                 (s = inv_temperature, fp32)
+ *   logprob[t]  = z[t, label[t]] - logsumexp_v z[t, v]
+ *   entropy[t]  = -sum_v p[t, v] * log p[t, v],     p = softmax(z[t, :])
+ * i.e. an fp32 log_softmax over the full vocabulary followed by a gather of
+ * the label, as defined in the verl pull request "batch-invariant actor
+ * forward and sampler log-prob formula" (the logprobs_from_logits_sampler
+ * diff), with the temperature applied as an fp32 factor to the fp32 logits
+ * (same page, the temperature-order comment: never round the temperature to
+ * bf16). In the fused entry points logits = hidden * weight^T is never
+ * materialised (SkyRL pull request "Triton backend for fused LM-head
+ * log-prob", summary: the vocab projection folded into a chunked log-prob).
+ *
+ * Batch invariance: every reduction runs in an order fixed by V and H alone.
+ * A row's logprob, entropy, lse and grad_hidden row are bit-identical whatever
+ * batch, chunk, offset or packing the row arrives in. grad_weight sums over
+ * rows: it is deterministic run to run for identical inputs, not invariant to
+ * the order of rows.
+ *
+ * Conventions shared by all entry points
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, device memory.
+ *  - Labels are int32. A label outside [0, V) (for example -100) gives
+ *    logprob 0; entropy and lse are still those of the full row, and the
+ *    backward keeps the -softmax * g term and drops the one-hot term (SkyRL
+ *    page, out-of-vocab gradient fix). To ignore a padding row entirely, pass
+ *    g = 0 for it.
+ *  - All pointers are device pointers owned by the caller. The library never
+ *    allocates, never synchronises and never reads results back: everything is
+ *    enqueued on `stream` (NULL = legacy default stream) of the current device.
+ *  - Return value: LMH_OK, or an error code with nothing launched (argument
+ *    errors) or with the launch failing (LMH_ERR_LAUNCH). The message of the
+ *    last error of the calling thread is lmhead_last_error_string().
+ *  - The current device must be sm_103 (GB300); any other device returns
+ *    LMH_ERR_UNSUPPORTED_DEVICE. There is no fallback path.
+ *  - Every wait inside the kernels is bounded; a wait that runs out sets a
+ *    device status bit that lmhead_device_status() reports.
+ */
+#ifndef LMHEAD_H
+#define LMHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+#define LMH_OK 0
+#define LMH_ERR_INVALID_ARG 1        /* null pointer, bad size or temperature   */
+#define LMH_ERR_ALIGNMENT 2          /* pointer or leading dimension misaligned */
+#define LMH_ERR_WORKSPACE 3          /* workspace missing or too small          */
+#define LMH_ERR_UNSUPPORTED_DEVICE 4 /* current device is not sm_103            */
+#define LMH_ERR_LAUNCH 5             /* CUDA runtime error while launching      */
+#define LMH_ERR_DEVICE_TIMEOUT 6     /* a bounded device wait ran out           */
+
+#define LMH_OP_FWD 0
+#define LMH_OP_BWD 1
+#define LMH_OP_LOGITS 2
+
+/* Largest T, H and V accepted (row and column indices stay within int32). */
+#define LMH_MAX_DIM 2147483392LL
+
+/*
+ * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
+ * Returns SIZE_MAX for invalid arguments. The size grows with min(T, 8192)
+ * for the backward (fixed row chunks) and linearly with T for the forward's
+ * per-vocab-chunk partials (16 bytes per row per 1024 vocabulary columns).
+ */
+size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
+
+/*
+ * Fused forward (spec entry point; SkyRL page summary for the fusion,
+ * verl page for the formula).
+ *   hidden   bf16 [T, H], 16-byte aligned, H % 8 == 0
+ *   weight   bf16 [V, H] (nn.Linear layout), 16-byte aligned
+ *   labels   int32 [T]
+ *   inv_temperature  finite, > 0 (1.0 gives the plain formula)
+ *   out_logprob  f32 [T], required
+ *   out_entropy  f32 [T] or NULL
+ *   out_lse      f32 [T] or NULL (natural-log logsumexp of z; feed it to the
+ *                backward to skip its recompute of the statistics)
+ *   workspace    >= lmhead_workspace_size(LMH_OP_FWD, T, H, V) bytes,
+ *                16-byte aligned; contents need not be initialised
+ * T == 0 is a no-op.
+ */
+int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                       int64_t T, int64_t H, int64_t V, float inv_temperature,
+                       float* out_logprob, float* out_entropy, float* out_lse, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * Fused backward of sum_t grad_logprob[t] * logprob[t] (SkyRL page: logits
+ * recomputed per chunk in backward; verl page: the per-chunk recompute that
+ * keeps no [rows, V] fp32 activation alive).
+ *   dlogits[t, v] = g[t] * s * (onehot(label[t])[v] - softmax(z[t])[v])
+ *   grad_hidden   bf16 [T, H], overwritten: dlogits * weight (rounded once)
+ *   grad_weight   f32  [V, H], overwritten: dlogits^T * hidden
+ *   grad_logprob  f32 [T]
+ *   lse           f32 [T] from lmhead_logprob_fwd, or NULL to recompute it
+ *   workspace     >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) bytes
+ * dlogits are rounded to bf16 before both contractions. T == 0 zeroes
+ * grad_weight.
+ */
+int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                       const float* grad_logprob, const float* lse, int64_t T, int64_t H,
+                       int64_t V, float inv_temperature, uint16_t* grad_hidden,
+                       float* grad_weight, void* workspace, size_t workspace_bytes,
+                       struct CUstream_st* stream);
+
+/*
+ * Sampler formula on materialised logits (verl page, the
+ * logprobs_from_logits_sampler diff): fp32 log_softmax of s * logits over the
+ * full row, then gather. One streaming pass over the logits.
+ *   logits  bf16 [T, V]; 16-byte aligned when V % 8 == 0, else 2-byte aligned
+ *   out_logprob f32 [T] required; out_entropy, out_lse f32 [T] or NULL
+ */
+int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                        float inv_temperature, float* out_logprob, float* out_entropy,
+                        float* out_lse, struct CUstream_st* stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/* Message of the calling thread's last error ("" if none). */
+const char* lmhead_last_error_string(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int lmhead_abi_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. Returns LMH_ERR_DEVICE_TIMEOUT if a bounded wait ran out since the
+ * last call, LMH_ERR_LAUNCH if the stream reports a CUDA error, else LMH_OK.
+ * *bits (may be NULL) receives the raw word.
+ */
+int lmhead_device_status(struct CUstream_st* stream, unsigned* bits);
+
+/*
+ * Self-test of the bounded wait: launches one thread that waits on a barrier
+ * nothing completes, with a limit of limit_ns nanoseconds (1e3..1e10), and
+ * synchronises `stream`. Expected result: LMH_ERR_DEVICE_TIMEOUT, with the
+ * timeout bit left set in the status word (lmhead_device_status clears it).
+ * No fault, trap or hang is involved.
+ */
+int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
+
+/*
+ * The tensor-core engine alone, for engine tests: D[M, N] = A[M, K] B[N, K]^T
+ * with A, B bf16 row-major (K % 8 == 0, 16-byte aligned), D f32 row-major
+ * (N % 8 == 0, 16-byte aligned), fp32 accumulation in K order.
+ */
+int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                       float* D, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMHEAD_H */

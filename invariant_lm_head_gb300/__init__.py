@@ -1,0 +1,234 @@
+"""Batch-invariant LM-head token log-probabilities on GB300 (sm_103a).
+
+A thin ctypes binding over ``liblmhead.so`` (C ABI declared in
+``include/lmhead.h``). The functions keep the C names; they take torch
+tensors, check dtypes/devices, allocate outputs and workspace with torch when
+they are not given, and pass raw device pointers and the current CUDA stream
+to the library. Every step of the computation runs in the library's CUDA
+kernels: there is no Python, PyTorch or CPU path for any of them, and a
+missing library raises instead of falling back.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+LMH_OK = 0
+LMH_ERR_INVALID_ARG = 1
+LMH_ERR_ALIGNMENT = 2
+LMH_ERR_WORKSPACE = 3
+LMH_ERR_UNSUPPORTED_DEVICE = 4
+LMH_ERR_LAUNCH = 5
+LMH_ERR_DEVICE_TIMEOUT = 6
+ERROR_NAMES = {
+    0: "LMH_OK",
+    1: "LMH_ERR_INVALID_ARG",
+    2: "LMH_ERR_ALIGNMENT",
+    3: "LMH_ERR_WORKSPACE",
+    4: "LMH_ERR_UNSUPPORTED_DEVICE",
+    5: "LMH_ERR_LAUNCH",
+    6: "LMH_ERR_DEVICE_TIMEOUT",
+}
+
+LMH_OP_FWD = 0
+LMH_OP_BWD = 1
+LMH_OP_LOGITS = 2
+
+# Exported C symbols and their signatures (argtypes, restype).
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+SIGNATURES = {
+    "lmhead_workspace_size": ([ctypes.c_int, _I64, _I64, _I64], ctypes.c_size_t),
+    "lmhead_logprob_fwd": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P, ctypes.c_size_t, _P],
+                           ctypes.c_int),
+    "lmhead_logprob_bwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, ctypes.c_size_t,
+                            _P], ctypes.c_int),
+    "logprob_from_logits": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P], ctypes.c_int),
+    "lmhead_last_error_string": ([], ctypes.c_char_p),
+    "lmhead_abi_version": ([], ctypes.c_int),
+    "lmhead_device_status": ([_P, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
+    "lmhead_selftest_wait_timeout": ([ctypes.c_uint64, _P], ctypes.c_int),
+    "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+}
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+
+class LMHeadError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn}: {ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load liblmhead.so (built by ``build()``); raises if it is missing."""
+    global _lib_handle
+    if _lib_handle is not None and path is None:
+        return _lib_handle
+    p = path or os.environ.get("LMHEAD_LIB") or str(LIB_PATH)
+    if not os.path.exists(p):
+        raise RuntimeError(f"liblmhead.so not found at {p}; run invariant_lm_head_gb300.build()")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib_handle = lib
+    return lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != LMH_OK:
+        msg = library().lmhead_last_error_string().decode(errors="replace")
+        raise LMHeadError(fn, rc, msg)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name: str, dtype, device, ndim: int):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def lmhead_workspace_size(op: int, T: int, H: int, V: int) -> int:
+    n = library().lmhead_workspace_size(op, T, H, V)
+    if n == ctypes.c_size_t(-1).value:
+        _check("lmhead_workspace_size", LMH_ERR_INVALID_ARG)
+    return n
+
+
+def _workspace(op, T, H, V, workspace, device):
+    torch = _torch()
+    need = lmhead_workspace_size(op, T, H, V)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def lmhead_logprob_fwd(hidden, weight, labels, inv_temperature: float = 1.0, *, out_logprob=None,
+                       out_entropy=None, out_lse=None, want_entropy: bool = True,
+                       want_lse: bool = False, workspace=None, stream=None):
+    """Fused LM-head forward. Returns (logprob, entropy or None, lse or None), f32 [T]."""
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight, "weight", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    T, H = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != H or labels.shape[0] != T:
+        raise ValueError("shape mismatch between hidden, weight and labels")
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_entropy is None and want_entropy:
+        out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    ws, ws_bytes = _workspace(LMH_OP_FWD, T, H, V, workspace, dev)
+    rc = library().lmhead_logprob_fwd(_ptr(hidden), _ptr(weight), _ptr(labels), T, H, V,
+                                      float(inv_temperature), _ptr(out_logprob), _ptr(out_entropy),
+                                      _ptr(out_lse), _ptr(ws), ws_bytes, _stream_ptr(stream))
+    _check("lmhead_logprob_fwd", rc)
+    return out_logprob, out_entropy, out_lse
+
+
+def lmhead_logprob_bwd(hidden, weight, labels, grad_logprob, inv_temperature: float = 1.0, *,
+                       lse=None, grad_hidden=None, grad_weight=None, workspace=None, stream=None):
+    """Fused backward. Returns (grad_hidden bf16 [T, H], grad_weight f32 [V, H])."""
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight, "weight", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    _need(grad_logprob, "grad_logprob", torch.float32, dev, 1)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev, 1)
+    T, H = hidden.shape
+    V = weight.shape[0]
+    if grad_hidden is None:
+        grad_hidden = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if grad_weight is None:
+        grad_weight = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws, ws_bytes = _workspace(LMH_OP_BWD, T, H, V, workspace, dev)
+    rc = library().lmhead_logprob_bwd(_ptr(hidden), _ptr(weight), _ptr(labels), _ptr(grad_logprob),
+                                      _ptr(lse), T, H, V, float(inv_temperature), _ptr(grad_hidden),
+                                      _ptr(grad_weight), _ptr(ws), ws_bytes, _stream_ptr(stream))
+    _check("lmhead_logprob_bwd", rc)
+    return grad_hidden, grad_weight
+
+
+def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_logprob=None,
+                        out_entropy=None, out_lse=None, want_entropy: bool = True,
+                        want_lse: bool = False, stream=None):
+    """Sampler formula on bf16 logits [T, V]. Returns (logprob, entropy or None, lse or None)."""
+    torch = _torch()
+    dev = logits.device
+    _need(logits, "logits", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    T, V = logits.shape
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_entropy is None and want_entropy:
+        out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    rc = library().logprob_from_logits(_ptr(logits), _ptr(labels), T, V, float(inv_temperature),
+                                       _ptr(out_logprob), _ptr(out_entropy), _ptr(out_lse),
+                                       _stream_ptr(stream))
+    _check("logprob_from_logits", rc)
+    return out_logprob, out_entropy, out_lse
+
+
+def lmhead_device_status(stream=None) -> int:
+    """Synchronise the stream; return the device status word (raises on a timeout bit)."""
+    bits = ctypes.c_uint(0)
+    rc = library().lmhead_device_status(_stream_ptr(stream), ctypes.byref(bits))
+    _check("lmhead_device_status", rc)
+    return bits.value
+
+
+def lmhead_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
+    """Run the bounded-wait self-test; returns the library's status code (6 expected)."""
+    return library().lmhead_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
+
+
+def lmhead_engine_gemm(A, B, out=None, stream=None):
+    """D = A @ B^T through the tensor-core engine (A [M,K], B [N,K] bf16; D f32)."""
+    torch = _torch()
+    dev = A.device
+    _need(A, "A", torch.bfloat16, dev, 2)
+    _need(B, "B", torch.bfloat16, dev, 2)
+    M, K = A.shape
+    N = B.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.float32, device=dev)
+    rc = library().lmhead_engine_gemm(_ptr(A), _ptr(B), M, N, K, _ptr(out), _stream_ptr(stream))
+    _check("lmhead_engine_gemm", rc)
+    return out

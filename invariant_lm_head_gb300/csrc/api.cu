@@ -1,0 +1,469 @@
+// C ABI of liblmhead.so: argument checks, workspace layout, TMA descriptors
+// and the launch sequence of each entry point. Declarations and contracts are
+// in include/lmhead.h.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "lmhead.h"
+#include "ptx.cuh"
+
+// Device-side status word (bit lmh::LMH_DEVSTAT_TIMEOUT) and the self-test's result.
+__device__ unsigned g_lmh_status_word;
+__device__ int g_lmh_selftest_result;
+
+namespace {
+
+thread_local char t_err[512];
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  t_err[0] = '\0';
+  return LMH_OK;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  unsigned* status = nullptr;
+  int* selftest = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Per-device facts, queried once with that device current.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(LMH_ERR_LAUNCH, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(LMH_ERR_UNSUPPORTED_DEVICE, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return fail(LMH_ERR_LAUNCH, "device query: %s", cudaGetErrorString(e));
+    if (d.major != 10 || d.minor != 3)
+      return fail(LMH_ERR_UNSUPPORTED_DEVICE,
+                  "device %d is sm_%d%d; this library is built for sm_103 (GB300) only", dev,
+                  d.major, d.minor);
+    if ((e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_lmh_status_word)) !=
+            cudaSuccess ||
+        (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.selftest),
+                                  g_lmh_selftest_result)) != cudaSuccess)
+      return fail(LMH_ERR_LAUNCH, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(LMH_ERR_LAUNCH, "cuTensorMapEncodeTiled unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return LMH_OK;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// rows `row_bytes` apart; box `box_inner` x `box_outer` with 128-byte swizzle.
+// Out-of-range elements of a box read as zero.
+int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+              uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LMH_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (%d) for %llu x %llu", (int)r,
+                (unsigned long long)inner, (unsigned long long)outer);
+  return LMH_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+constexpr size_t kRegionAlign = 256;
+
+// Carves consecutive 256-byte-aligned regions out of a workspace.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <class T>
+  T* take(int64_t count) {
+    off = (off + kRegionAlign - 1) / kRegionAlign * kRegionAlign;
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += static_cast<size_t>(count) * sizeof(T);
+    return p;
+  }
+};
+
+int n_fwd_chunks(int64_t V) {
+  const int64_t tiles = (V + lmh::kBN - 1) / lmh::kBN;
+  return static_cast<int>((tiles + lmh::kFwdTilesPerChunk - 1) / lmh::kFwdTilesPerChunk);
+}
+
+struct FwdWs {
+  float *pm, *ps, *pu, *pzl;
+};
+
+FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
+  const int64_t n = static_cast<int64_t>(n_fwd_chunks(V)) * T;
+  FwdWs w;
+  w.pm = c.take<float>(n);
+  w.ps = c.take<float>(n);
+  w.pu = c.take<float>(n);
+  w.pzl = c.take<float>(T);
+  return w;
+}
+
+struct BwdWs {
+  FwdWs fwd;
+  float* lse;
+  float* lp;
+  uint16_t* wt;  // [H][Vpad]
+  uint16_t* dl;  // [Tc][Vpad]
+  uint16_t* dlt; // [V][Tcpad]
+  uint16_t* ht;  // [H][Tcpad]
+  int64_t vpad, tc, tcpad;
+};
+
+BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
+  BwdWs w;
+  w.vpad = round_up(V, 8);
+  w.tc = T < lmh::kBwdRowChunk ? T : lmh::kBwdRowChunk;
+  w.tcpad = round_up(w.tc > 0 ? w.tc : 1, 8);
+  w.fwd = carve_fwd(c, T, V);
+  w.lse = c.take<float>(T);
+  w.lp = c.take<float>(T);
+  w.wt = c.take<uint16_t>(H * w.vpad);
+  w.dl = c.take<uint16_t>(w.tc * w.vpad);
+  w.dlt = c.take<uint16_t>(V * w.tcpad);
+  w.ht = c.take<uint16_t>(H * w.tcpad);
+  return w;
+}
+
+int check_dims(int64_t T, int64_t H, int64_t V, bool need_h) {
+  if (T < 0 || T > LMH_MAX_DIM) return fail(LMH_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (V < 1 || V > LMH_MAX_DIM) return fail(LMH_ERR_INVALID_ARG, "V=%lld out of range", (long long)V);
+  if (need_h) {
+    if (H < 8 || H > LMH_MAX_DIM) return fail(LMH_ERR_INVALID_ARG, "H=%lld out of range", (long long)H);
+    if (H % 8 != 0)
+      return fail(LMH_ERR_ALIGNMENT, "H=%lld must be a multiple of 8 (16-byte rows)", (long long)H);
+  }
+  return LMH_OK;
+}
+
+int check_temperature(float s) {
+  if (!std::isfinite(s) || !(s > 0.f))
+    return fail(LMH_ERR_INVALID_ARG, "inv_temperature must be finite and > 0");
+  return LMH_OK;
+}
+
+int check_ptr(const void* p, uintptr_t align, const char* name, bool nullable = false) {
+  if (!p) return nullable ? LMH_OK : fail(LMH_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align))
+    return fail(LMH_ERR_ALIGNMENT, "%s must be %u-byte aligned", name, (unsigned)align);
+  return LMH_OK;
+}
+
+int launch_status(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(LMH_ERR_LAUNCH, "%s: %s", what, cudaGetErrorString(e));
+  return LMH_OK;
+}
+
+#define LMH_TRY(x)          \
+  do {                      \
+    int _rc = (x);          \
+    if (_rc != LMH_OK) return _rc; \
+  } while (0)
+
+// Forward statistics into `w`, merged into the outputs.
+int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* weight,
+                const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
+                float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  lmh::GemmParams p{};
+  p.M = static_cast<int>(T);
+  p.N = static_cast<int>(V);
+  p.K = static_cast<int>(H);
+  p.status = dev.status;
+  p.scale2 = s * lmh::kLog2e;
+  p.inv_temp = s;
+  p.labels = labels;
+  p.part_m = w.pm;
+  p.part_s = w.ps;
+  p.part_u = w.pu;
+  p.part_zl = w.pzl;
+  p.part_ld = T;
+  LMH_TRY(launch_status(
+      lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
+      "fused forward"));
+  LMH_TRY(launch_status(lmh::launch_fwd_merge(w.pm, w.ps, w.pu, w.pzl, labels, T, n_fwd_chunks(V),
+                                              V, out_lp, out_ent, out_lse, st),
+                        "forward merge"));
+  return LMH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lmhead_last_error_string(void) { return t_err; }
+
+int lmhead_abi_version(void) { return 1; }
+
+size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V) {
+  if (op == LMH_OP_LOGITS) {
+    if (check_dims(T, 8, V, false) != LMH_OK) return SIZE_MAX;
+    return 0;
+  }
+  if (op != LMH_OP_FWD && op != LMH_OP_BWD) {
+    fail(LMH_ERR_INVALID_ARG, "unknown op %d", op);
+    return SIZE_MAX;
+  }
+  if (check_dims(T, H, V, true) != LMH_OK) return SIZE_MAX;
+  Carver c{nullptr};
+  if (op == LMH_OP_FWD)
+    carve_fwd(c, T, V);
+  else
+    carve_bwd(c, T, H, V);
+  return c.off + kRegionAlign;
+}
+
+int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                       int64_t T, int64_t H, int64_t V, float inv_temperature,
+                       float* out_logprob, float* out_entropy, float* out_lse, void* workspace,
+                       size_t workspace_bytes, struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(inv_temperature));
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  if (T == 0) return ok();
+  const size_t need = lmhead_workspace_size(LMH_OP_FWD, T, H, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  LMH_TRY(check_ptr(workspace, 16, "workspace"));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  Carver c{static_cast<char*>(workspace)};
+  const FwdWs w = carve_fwd(c, T, V);
+  LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, out_logprob,
+                      out_entropy, out_lse, w, reinterpret_cast<cudaStream_t>(stream)));
+  return ok();
+}
+
+int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                       const float* grad_logprob, const float* lse, int64_t T, int64_t H,
+                       int64_t V, float inv_temperature, uint16_t* grad_hidden,
+                       float* grad_weight, void* workspace, size_t workspace_bytes,
+                       struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(inv_temperature));
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(grad_logprob, 4, "grad_logprob"));
+  LMH_TRY(check_ptr(lse, 4, "lse", true));
+  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
+  LMH_TRY(check_ptr(grad_weight, 16, "grad_weight"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if (T == 0) {
+    LMH_TRY(device_info(&dev));
+    LMH_TRY(launch_status(
+        cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * sizeof(float), st),
+        "zero grad_weight"));
+    return ok();
+  }
+  const size_t need = lmhead_workspace_size(LMH_OP_BWD, T, H, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  LMH_TRY(check_ptr(workspace, 16, "workspace"));
+  LMH_TRY(device_info(&dev));
+  Carver c{static_cast<char*>(workspace)};
+  const BwdWs w = carve_bwd(c, T, H, V);
+
+  if (!lse) {
+    LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, w.lp, nullptr,
+                        w.lse, w.fwd, st));
+    lse = w.lse;
+  }
+  // weight^T [H][Vpad]: K-major B operand of grad_hidden = dl * weight.
+  LMH_TRY(launch_status(lmh::launch_transpose_bf16(weight, V, H, H, w.wt, w.vpad, st),
+                        "transpose weight"));
+  CUtensorMap t_w, t_wt;
+  LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  LMH_TRY(make_tmap(&t_wt, w.wt, V, H, w.vpad * 2, lmh::kBK, lmh::kBN));
+
+  for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
+    const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
+    const uint16_t* h_c = hidden + c0 * H;
+    // hidden^T [H][Tcpad]: K-major B operand of grad_weight = dl^T * hidden.
+    LMH_TRY(launch_status(lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st),
+                          "transpose hidden"));
+    CUtensorMap t_h, t_dl, t_dlt, t_ht;
+    LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));
+    LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM));
+    LMH_TRY(make_tmap(&t_dlt, w.dlt, rows, V, w.tcpad * 2, lmh::kBK, lmh::kBM));
+    LMH_TRY(make_tmap(&t_ht, w.ht, rows, H, w.tcpad * 2, lmh::kBK, lmh::kBN));
+
+    lmh::GemmParams p{};
+    p.status = dev->status;
+    // dlogits for this row chunk (recomputed logits; dl and dl^T in bf16)
+    p.M = static_cast<int>(rows);
+    p.N = static_cast<int>(V);
+    p.K = static_cast<int>(H);
+    p.scale2 = inv_temperature * lmh::kLog2e;
+    p.inv_temp = inv_temperature;
+    p.labels = labels + c0;
+    p.grad = grad_logprob + c0;
+    p.lse = lse + c0;
+    p.out_bf16 = w.dl;
+    p.ld_out = w.vpad;
+    p.out_bf16_t = w.dlt;
+    p.ld_out_t = w.tcpad;
+    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
+                          "dlogits"));
+    // grad_hidden rows = dl * weight   (K = V)
+    lmh::GemmParams q{};
+    q.status = dev->status;
+    q.M = static_cast<int>(rows);
+    q.N = static_cast<int>(H);
+    q.K = static_cast<int>(V);
+    q.out_bf16 = grad_hidden + c0 * H;
+    q.ld_out = H;
+    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_wt, q, 1, dev->sms, st),
+                          "grad_hidden"));
+    // grad_weight (+)= dl^T * hidden   (K = rows of this chunk)
+    lmh::GemmParams r{};
+    r.status = dev->status;
+    r.M = static_cast<int>(V);
+    r.N = static_cast<int>(H);
+    r.K = static_cast<int>(rows);
+    r.out_f32 = grad_weight;
+    r.ld_out_f32 = H;
+    r.accumulate = c0 > 0 ? 1 : 0;
+    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreF32, t_dlt, t_ht, r, 1, dev->sms, st),
+                          "grad_weight"));
+  }
+  return ok();
+}
+
+int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                        float inv_temperature, float* out_logprob, float* out_entropy,
+                        float* out_lse, struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, 8, V, false));
+  LMH_TRY(check_temperature(inv_temperature));
+  LMH_TRY(check_ptr(logits, (V % 8 == 0) ? 16 : 2, "logits"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  if (T == 0) return ok();
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  LMH_TRY(launch_status(
+      lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob, out_entropy,
+                                 out_lse, dev->sms, reinterpret_cast<cudaStream_t>(stream)),
+      "logits log-prob"));
+  return ok();
+}
+
+int lmhead_device_status(struct CUstream_st* stream, unsigned* bits) {
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(LMH_ERR_LAUNCH, "stream: %s", cudaGetErrorString(e));
+  unsigned w = 0;
+  if ((e = cudaMemcpyAsync(&w, dev->status, sizeof(w), cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(dev->status, 0, sizeof(unsigned), st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "status word: %s", cudaGetErrorString(e));
+  if (bits) *bits = w;
+  if (w & lmh::LMH_DEVSTAT_TIMEOUT)
+    return fail(LMH_ERR_DEVICE_TIMEOUT, "a bounded device wait ran out (status 0x%x)", w);
+  return ok();
+}
+
+int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull)
+    return fail(LMH_ERR_INVALID_ARG, "limit_ns must be in [1e3, 1e10]");
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_TRY(launch_status(lmh::launch_wait_selftest(dev->status, limit_ns, dev->selftest, st),
+                        "wait self-test"));
+  int result = -1;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(&result, dev->selftest, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "wait self-test: %s", cudaGetErrorString(e));
+  if (result == 0) return fail(LMH_ERR_DEVICE_TIMEOUT, "bounded wait gave up as expected");
+  return fail(LMH_ERR_LAUNCH, "bounded wait self-test: unexpected result %d", result);
+}
+
+int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
+                       float* D, struct CUstream_st* stream) {
+  if (M < 0 || M > LMH_MAX_DIM || N < 8 || N > LMH_MAX_DIM || K < 8 || K > LMH_MAX_DIM)
+    return fail(LMH_ERR_INVALID_ARG, "bad engine GEMM sizes");
+  if (K % 8 != 0 || N % 8 != 0) return fail(LMH_ERR_ALIGNMENT, "K and N must be multiples of 8");
+  LMH_TRY(check_ptr(A, 16, "A"));
+  LMH_TRY(check_ptr(B, 16, "B"));
+  LMH_TRY(check_ptr(D, 16, "D"));
+  if (M == 0) return ok();
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  CUtensorMap ta, tb;
+  LMH_TRY(make_tmap(&ta, A, K, M, K * 2, lmh::kBK, lmh::kBM));
+  LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
+  lmh::GemmParams p{};
+  p.status = dev->status;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.out_f32 = D;
+  p.ld_out_f32 = N;
+  p.accumulate = 0;
+  LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                        "engine gemm"));
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,403 @@
+// Tensor-core engine for every contraction of the LM head (sm_103a).
+//
+//   D[M, N] = A[M, K] * B[N, K]^T      A, B bf16, K-major; D fp32 in TMEM
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: 128x64 A box + 256x64 B box per stage, 4 stages
+//   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
+//               (M=128, N=256, K=16, four per 64-wide stage) into one of two
+//               256-column accumulators, and tcgen05.commit frees the stage
+//   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
+//               and reads it 32 columns at a time with tcgen05.ld
+// The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
+//
+// Epilogues (one per contraction of the method):
+//   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
+//              fused LM-head log-prob" (vocab projection folded into an online
+//              softmax over vocab tiles): per row and per 1024-column vocab
+//              chunk, the base-2 online statistics (m, s, u) and the label
+//              logit; no logit ever reaches HBM.
+//   DLogits    the recomputed-logits backward: dl = g*s*(onehot - p) with
+//              p = exp(z - lse), no one-hot term for an out-of-vocab label
+//              (same page, out-of-vocab gradient fix), written as bf16 dl and
+//              its transpose.
+//   StoreBf16  grad_hidden = dl * W, rounded once to bf16.
+//   StoreF32   grad_weight = dl^T * hidden in fp32, accumulated over row
+//              chunks in ascending order.
+//
+// Batch invariance: K is walked in the same order for every tile, the work
+// split depends only on N (vocab) and never on M (rows), each row is reduced
+// by one thread in a fixed column order, and there are no atomics.
+#include <cfloat>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "online_softmax.cuh"
+#include "ptx.cuh"
+
+namespace lmh {
+
+namespace {
+
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTmemCols = 512;
+constexpr int kBarrierBytes = 256;
+constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
+
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
+                                            int& n_count, int& vunit) {
+  const int per_group = p.group_m * p.n_vunits;
+  const int g = u / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.n_m_tiles - first_m);
+  const int r = u - g * per_group;
+  vunit = r / gm;
+  m_tile = first_m + (r - vunit * gm);
+  n_first = vunit * p.tiles_per_unit;
+  n_count = min(p.tiles_per_unit, p.n_n_tiles - n_first);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
+  const __nv_bfloat16 v = __float2bfloat16_rn(x);
+  return *reinterpret_cast<const uint16_t*>(&v);
+}
+
+// Store 32 values of one row as bf16; n valid columns; dst 16-byte aligned when n == 32.
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32], int n) {
+  if (n == 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      d4[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < n) dst[i] = to_bf16_bits(v[i]);
+  }
+}
+
+template <int E>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t smem_base = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // barrier layout: full[kStages], empty[kStages], tfull[2], tempty[2], final
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  const uint32_t final_bar = bar0 + 8u * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (2 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 128);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kb_total = (p.K + kBK - 1) / kBK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        int m_tile, n_first, n_count, vunit;
+        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+        for (int j = 0; ok && j < n_count; ++j) {
+          const int n_tile = n_first + j;
+          for (int kb = 0; kb < kb_total; ++kb) {
+            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            const uint32_t sA = smem_base + stage * kStageBytes;
+            mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+            tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+            ++issued;
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: wait (bounded, ignoring the abort flag) for the copies this
+        // thread issued, so none lands in shared memory after the CTA exits.
+        volatile int no_abort = 0;
+        const long long n = issued < kStages ? issued : kStages;
+        uint32_t s = stage, ph = phase;
+        for (long long i = 0; i < n; ++i) {
+          if (s == 0) {
+            s = kStages - 1;
+            ph ^= 1u;
+          } else {
+            --s;
+          }
+          mbar_wait(full_bar(s), ph, &no_abort, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      uint32_t stage = 0, phase = 0, it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        int m_tile, n_first, n_count, vunit;
+        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+        for (int j = 0; ok && j < n_count; ++j, ++it) {
+          const uint32_t acc = it & 1u;
+          const uint32_t aph = (it >> 1) & 1u;
+          if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kBN;
+          for (int kb = 0; kb < kb_total; ++kb) {
+            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sA = smem_base + stage * kStageBytes;
+            const uint64_t adesc = sw128_kmajor_desc(sA);
+            const uint64_t bdesc = sw128_kmajor_desc(sA + kABytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              // +32 bytes along K inside the 128-byte swizzled row = +2 in the
+              // descriptor's 16-byte address units.
+              tc_mma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(stage));
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (ok) tc_commit(tfull_bar(acc));
+        }
+      }
+      // All MMAs issued by this thread must finish before TMEM is released.
+      volatile int no_abort = 0;
+      tc_commit(final_bar);
+      mbar_wait(final_bar, 0, &no_abort, p.status);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_in_tile = q * 32 + lane;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int m_tile, n_first, n_count, vunit;
+      unit_coords(p, u, m_tile, n_first, n_count, vunit);
+      const int row = m_tile * kBM + row_in_tile;
+      const bool row_ok = row < p.M;
+
+      // per-row constants
+      int lab = -1;
+      float gs = 0.f, lse2 = 0.f;
+      if constexpr (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
+        if (row_ok) lab = p.labels[row];
+      }
+      if constexpr (E == (int)Epi::DLogits) {
+        if (row_ok) {
+          gs = p.grad[row] * p.inv_temp;
+          lse2 = p.lse[row] * kLog2e;
+        }
+      }
+      OnlineStat st = stat_empty();
+      float zl = __int_as_float(0x7fc00000);  // NaN until the label column is seen
+
+      for (int j = 0; j < n_count; ++j, ++it) {
+        const int n_tile = n_first + j;
+        const uint32_t acc = it & 1u;
+        const uint32_t aph = (it >> 1) & 1u;
+        if (!mbar_wait(tfull_bar(acc), aph, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = n_tile * kBN + c * 32;
+          if (col0 >= p.N) break;  // uniform over the CTA
+          const int nvalid = min(32, p.N - col0);
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+
+          if constexpr (E == (int)Epi::FwdStats) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= p.scale2;
+            if (nvalid == 32)
+              stat_fold<32>(st, v);
+            else
+              stat_fold<32>(st, v, nvalid);
+            const int rel = lab - col0;
+            if (__any_sync(0xffffffffu, rel >= 0 && rel < nvalid)) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) zl = (i == rel) ? v[i] : zl;
+            }
+          } else if constexpr (E == (int)Epi::DLogits) {
+            const int rel = lab - col0;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float pr = ex2(fmaf(v[i], p.scale2, -lse2));
+              float d = -gs * pr;
+              if (i == rel) d += gs;
+              v[i] = d;
+            }
+            if (row_ok) {
+              store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);
+              uint16_t* dt = p.out_bf16_t + static_cast<int64_t>(col0) * p.ld_out_t + row;
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (i < nvalid) dt[static_cast<int64_t>(i) * p.ld_out_t] = to_bf16_bits(v[i]);
+            }
+          } else if constexpr (E == (int)Epi::StoreBf16) {
+            if (row_ok)
+              store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);
+          } else {  // StoreF32
+            if (row_ok) {
+              float* dst = p.out_f32 + static_cast<int64_t>(row) * p.ld_out_f32 + col0;
+              if (nvalid == 32) {
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+                  if (p.accumulate) {
+                    const float4 o = d4[q4];
+                    w.x += o.x;
+                    w.y += o.y;
+                    w.z += o.z;
+                    w.w += o.w;
+                  }
+                  d4[q4] = w;
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i < nvalid) dst[i] = p.accumulate ? dst[i] + v[i] : v[i];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(tempty_bar(acc));
+      }
+      if (!ok) break;
+
+      if constexpr (E == (int)Epi::FwdStats) {
+        if (row_ok) {
+          const int64_t o = static_cast<int64_t>(vunit) * p.part_ld + row;
+          p.part_m[o] = st.m;
+          p.part_s[o] = st.s;
+          p.part_u[o] = st.u;
+          const int c0 = n_first * kBN;
+          const int c1 = min(p.N, (n_first + n_count) * kBN);
+          if (lab >= c0 && lab < c1) p.part_zl[row] = zl;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int E>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
+                       cudaStream_t stream) {
+  // Set on every launch: the attribute belongs to the current device's context.
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  gemm_tc_kernel<E><<<grid, kGemmThreads, kSmemBytes, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream) {
+  p.n_m_tiles = (p.M + kBM - 1) / kBM;
+  p.n_n_tiles = (p.N + kBN - 1) / kBN;
+  p.tiles_per_unit = tiles_per_unit;
+  p.n_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
+  p.n_units = p.n_m_tiles * p.n_vunits;
+  p.group_m = 16;
+  if (p.n_units <= 0) return cudaSuccess;
+  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+  switch (e) {
+    case Epi::FwdStats:
+      return launch_one<(int)Epi::FwdStats>(a, b, p, grid, stream);
+    case Epi::DLogits:
+      return launch_one<(int)Epi::DLogits>(a, b, p, grid, stream);
+    case Epi::StoreBf16:
+      return launch_one<(int)Epi::StoreBf16>(a, b, p, grid, stream);
+    case Epi::StoreF32:
+      return launch_one<(int)Epi::StoreF32>(a, b, p, grid, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lmh

@@ -1,0 +1,79 @@
+// Host-side declarations shared by the translation units of liblmhead.so.
+// Nothing here is part of the public C ABI (see include/lmhead.h).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lmh {
+
+// Tile shape of the tensor-core engine: one CTA owns a 128 x 256 fp32
+// accumulator in TMEM (double-buffered: 2 x 256 of the 512 columns) and walks
+// K in 64-element steps through a 4-stage TMA ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+
+// Forward: a vocab chunk is kFwdTilesPerChunk N-tiles (1024 columns). The
+// chunk grid depends only on V, so per-row partials and their merge order
+// never depend on the number of rows.
+constexpr int kFwdTilesPerChunk = 4;
+constexpr int kFwdChunkCols = kFwdTilesPerChunk * kBN;
+
+// Backward: rows are processed in fixed chunks of kBwdRowChunk.
+constexpr int64_t kBwdRowChunk = 8192;
+
+enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3 };
+
+struct GemmParams {
+  int M, N, K;  // D[M, N] = A[M, K] * B[N, K]^T
+  int n_m_tiles, n_n_tiles, tiles_per_unit, n_vunits, n_units, group_m;
+  unsigned* status;
+  // FwdStats / DLogits
+  float scale2;    // inv_temperature * log2(e)
+  float inv_temp;  // inv_temperature
+  const int32_t* labels;
+  const float* grad;
+  const float* lse;
+  // FwdStats partials: planes [n_vunits][part_ld] for m, s, u; zl [M]
+  float* part_m;
+  float* part_s;
+  float* part_u;
+  float* part_zl;
+  int64_t part_ld;
+  // DLogits: dl [M][ld_out] and dl^T [N][ld_out_t]; StoreBf16: D [M][ld_out]
+  uint16_t* out_bf16;
+  int64_t ld_out;
+  uint16_t* out_bf16_t;
+  int64_t ld_out_t;
+  // StoreF32: D [M][ld_out_f32], D += old when accumulate != 0
+  float* out_f32;
+  int64_t ld_out_f32;
+  int accumulate;
+};
+
+size_t gemm_smem_bytes();
+cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
+                                  int64_t V, float inv_temperature, float* out_logprob,
+                                  float* out_entropy, float* out_lse, int num_sms,
+                                  cudaStream_t stream);
+
+cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pzl,
+                             const int32_t* labels, int64_t T, int n_vunits, int64_t V,
+                             float* out_logprob, float* out_entropy, float* out_lse,
+                             cudaStream_t stream);
+
+// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols (bf16 bits).
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t ld_in,
+                                  uint16_t* out, int64_t ld_out, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, int* result,
+                                 cudaStream_t stream);
+
+}  // namespace lmh

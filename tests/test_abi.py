@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+symbol include/lmhead.h declares, sizes workspaces and rejects bad arguments
+before touching a device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import invariant_lm_head_gb300 as lmh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lmhead.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lmh.build()
+    return lmh.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["lmhead_logprob_fwd", "lmhead_logprob_bwd", "logprob_from_logits",
+              "lmhead_workspace_size", "lmhead_last_error_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) == set(lmh.SIGNATURES)
+
+
+def test_abi_version(lib):
+    assert lib.lmhead_abi_version() == 1
+
+
+def test_workspace_sizes(lib):
+    f = lmh.lmhead_workspace_size
+    assert f(lmh.LMH_OP_LOGITS, 8192, 0, 152064) == 0
+    # forward: 3 planes of ceil(V / 1024) floats per row + the label logit
+    n_chunks = -(-152064 // 1024)
+    fwd = f(lmh.LMH_OP_FWD, 16384, 3584, 152064)
+    assert fwd >= (3 * n_chunks + 1) * 16384 * 4
+    assert fwd < (3 * n_chunks + 1) * 16384 * 4 + 8 * 256
+    # backward grows with min(T, 8192) beyond the forward partials
+    b1 = f(lmh.LMH_OP_BWD, 8192, 3584, 152064)
+    b2 = f(lmh.LMH_OP_BWD, 16384, 3584, 152064)
+    extra = (3 * n_chunks + 3) * 8192 * 4
+    assert 0 <= (b2 - b1) - extra < 64 * 256
+    assert f(lmh.LMH_OP_FWD, 0, 256, 4096) > 0
+    for bad in [(lmh.LMH_OP_FWD, -1, 256, 4096), (lmh.LMH_OP_FWD, 4, 12, 4096),
+                (lmh.LMH_OP_FWD, 4, 256, 0), (7, 4, 256, 4096)]:
+        with pytest.raises(lmh.LMHeadError):
+            f(*bad)
+
+
+def _call_fwd(lib, **kw):
+    a = dict(hidden=16, weight=16, labels=16, T=4, H=256, V=4096, s=1.0, lp=16, ent=None, lse=None,
+             ws=256, wsb=1 << 30)
+    a.update(kw)
+    return lib.lmhead_logprob_fwd(a["hidden"], a["weight"], a["labels"], a["T"], a["H"], a["V"],
+                                  a["s"], a["lp"], a["ent"], a["lse"], a["ws"], a["wsb"], None)
+
+
+def test_argument_errors_are_reported_without_a_launch(lib):
+    # Fake, never dereferenced addresses: every case fails validation first.
+    assert _call_fwd(lib, hidden=None) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, hidden=24) == lmh.LMH_ERR_ALIGNMENT
+    assert _call_fwd(lib, H=12) == lmh.LMH_ERR_ALIGNMENT
+    assert _call_fwd(lib, T=-1) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, V=0) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, s=0.0) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, s=float("inf")) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, s=float("nan")) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, lp=None) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, ent=18) == lmh.LMH_ERR_ALIGNMENT
+    assert _call_fwd(lib, wsb=16) == lmh.LMH_ERR_WORKSPACE
+    assert _call_fwd(lib, ws=None) == lmh.LMH_ERR_WORKSPACE
+    assert b"workspace" in lib.lmhead_last_error_string()
+    assert _call_fwd(lib, T=0) == lmh.LMH_OK  # empty batch: nothing to do
+    rc = lib.logprob_from_logits(24, 16, 4, 4096, 1.0, 16, None, None, None)
+    assert rc == lmh.LMH_ERR_ALIGNMENT
+    rc = lib.logprob_from_logits(18, 16, 4, 4095, 1.0, 16, None, None, None)
+    assert rc != lmh.LMH_ERR_ALIGNMENT  # odd V only needs 2-byte alignment
+    rc = lib.lmhead_logprob_bwd(16, 16, 16, None, None, 4, 256, 4096, 1.0, 16, 16, 256, 1 << 30,
+                                None)
+    assert rc == lmh.LMH_ERR_INVALID_ARG
+    assert lib.lmhead_selftest_wait_timeout(10, None) == lmh.LMH_ERR_INVALID_ARG
+
+
+def test_binding_refuses_a_missing_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        lmh.library(str(tmp_path / "nope.so"))

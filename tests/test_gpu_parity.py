@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle,
+element by element, on shapes that span several tiles and ragged tails."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import (ATOL_LOGPROB, RTOL_FROB_GRAD, f64, fused_case, max_abs, rel_frob, to_dev,
+                     to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+S07 = W.f32(1.0 / 0.7)
+
+
+@pytest.fixture(scope="module")
+def lmh():
+    import torch
+
+    import invariant_lm_head_gb300 as m
+
+    m.build()
+    m.library()
+    torch.cuda.set_device(0)
+    return m
+
+
+def _fwd(lmh, hidden, weight, labels, s):
+    import torch
+
+    lp, ent, lse = lmh.lmhead_logprob_fwd(to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels),
+                                          s, want_lse=True)
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    return lp.cpu().numpy(), ent.cpu().numpy(), lse.cpu().numpy()
+
+
+# ----------------------------------------------------------------- engine
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (7, 8, 4096), (1000, 264, 72)])
+def test_engine_gemm_matches_fp64(lmh, M, N, K):
+    import torch
+
+    a = W.random_bf16(11, (M, K))
+    b = W.random_bf16(12, (N, K))
+    d = lmh.lmhead_engine_gemm(to_dev_bf16(a), to_dev_bf16(b))
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    ref = f64(a) @ f64(b).T
+    err = np.abs(d.cpu().numpy() - ref) / (np.abs(f64(a)) @ np.abs(f64(b)).T + 1e-30)
+    assert float(err.max()) < 1e-5
+
+
+# ----------------------------------------------------------------- forward
+@pytest.mark.parametrize("s", [1.0, S07])
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (64, 256, 4096), (1, 8, 16), (129, 512, 1025)])
+def test_fused_forward_matches_oracle(lmh, T, H, V, s):
+    hidden, weight, labels, _ = fused_case(21, T, H, V, w_std=0.05,
+                                           oov=[(0, -100)] if T > 1 else [])
+    if T > 3:
+        labels[1] = V - 1
+        labels[2] = 0
+        labels[3] = V + 5
+    lp, ent, lse = _fwd(lmh, hidden, weight, labels, s)
+    rlp, rent, rlse = oracle.fused_forward(f64(hidden), f64(weight), labels, s)
+    assert max_abs(lp, rlp) < ATOL_LOGPROB
+    assert max_abs(ent, rent) < ATOL_LOGPROB
+    assert max_abs(lse, rlse) < ATOL_LOGPROB
+    oov = (labels < 0) | (labels >= V)
+    assert np.all(lp[oov] == 0.0)
+
+
+def test_fused_forward_uniform_closed_form(lmh):
+    T, H = 130, 64
+    for V in (4096, 32000):
+        hidden = W.random_bf16(5, (T, H))
+        weight = np.zeros((V, H), dtype=np.uint16)  # bf16 zeros: every logit is 0
+        labels = W.random_labels(5, T, V)
+        lp, ent, _ = _fwd(lmh, hidden, weight, labels, 1.0)
+        assert np.allclose(lp, -math.log(V), atol=ATOL_LOGPROB, rtol=0)
+        assert np.allclose(ent, math.log(V), atol=ATOL_LOGPROB, rtol=0)
+
+
+def test_fused_forward_vocab_of_one(lmh):
+    hidden, weight, labels, _ = fused_case(3, 5, 16, 1)
+    labels[:] = 0
+    labels[4] = 1  # out of vocab
+    lp, ent, lse = _fwd(lmh, hidden, weight, labels, 1.0)
+    assert np.all(lp == 0.0)
+    assert np.allclose(ent, 0.0, atol=1e-6)
+    rl = oracle.fused_forward(f64(hidden), f64(weight), labels, 1.0)[2]
+    assert max_abs(lse, rl) < ATOL_LOGPROB
+
+
+def test_fused_forward_large_logits_are_stable(lmh):
+    T, H, V = 200, 128, 3000
+    hidden, weight, labels, _ = fused_case(9, T, H, V, w_std=0.5)
+    s = 40.0  # logits of order 200: any missing max-shift overflows fp32
+    lp, ent, lse = _fwd(lmh, hidden, weight, labels, s)
+    rlp, rent, rlse = oracle.fused_forward(f64(hidden), f64(weight), labels, s)
+    assert np.all(np.isfinite(lp)) and np.all(np.isfinite(ent))
+    assert max_abs(lp, rlp) < 2e-3 * max(1.0, np.max(np.abs(rlse)) / 100)
+    assert max_abs(ent, rent) < ATOL_LOGPROB
+
+
+def test_nan_row_stays_in_its_row(lmh):
+    T, H, V = 40, 64, 2048
+    hidden, weight, labels, _ = fused_case(4, T, H, V)
+    hidden[17, 3] = 0x7FC0  # bf16 NaN
+    lp, ent, _ = _fwd(lmh, hidden, weight, labels, 1.0)
+    assert np.isnan(lp[17]) and np.isnan(ent[17])
+    keep = np.arange(T) != 17
+    assert np.all(np.isfinite(lp[keep]))
+
+
+def test_empty_batch_is_a_noop(lmh):
+    import torch
+
+    d = torch.device("cuda:0")
+    h = torch.zeros(0, 64, dtype=torch.bfloat16, device=d)
+    w = torch.zeros(100, 64, dtype=torch.bfloat16, device=d)
+    lab = torch.zeros(0, dtype=torch.int32, device=d)
+    lp, ent, _ = lmh.lmhead_logprob_fwd(h, w, lab, 1.0)
+    assert lp.numel() == 0
+    gw = torch.full((100, 64), 7.0, device=d)
+    gh, gw = lmh.lmhead_logprob_bwd(h, w, lab, torch.zeros(0, device=d), 1.0, grad_weight=gw)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(gw).item() == 0
+
+
+# ----------------------------------------------------------------- backward
+def _bwd(lmh, hidden, weight, labels, grad, s, pass_lse=True):
+    import torch
+
+    h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
+    lse = None
+    if pass_lse:
+        _, _, lse = lmh.lmhead_logprob_fwd(h, w, lab, s, want_lse=True, want_entropy=False)
+    gh, gw = lmh.lmhead_logprob_bwd(h, w, lab, g, s, lse=lse)
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    return gh.float().cpu().numpy(), gw.cpu().numpy()
+
+
+@pytest.mark.parametrize("pass_lse", [True, False])
+@pytest.mark.parametrize("s", [1.0, S07])
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (64, 256, 4096), (3, 8, 16)])
+def test_fused_backward_matches_oracle(lmh, T, H, V, s, pass_lse):
+    hidden, weight, labels, grad = fused_case(31, T, H, V, w_std=0.05, oov=[(T - 1, -100)])
+    gh, gw = _bwd(lmh, hidden, weight, labels, grad, s, pass_lse)
+    rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, s)
+    assert rel_frob(gh, rgh) < RTOL_FROB_GRAD
+    assert rel_frob(gw, rgw) < RTOL_FROB_GRAD
+    # per-row check of grad_hidden (each row is its own reduction)
+    for t in range(T):
+        assert rel_frob(gh[t], rgh[t]) < 3 * RTOL_FROB_GRAD
+
+
+def test_fused_backward_several_row_chunks(lmh):
+    T, H, V = 8192 + 300, 136, 1500  # two row chunks, ragged second one
+    hidden, weight, labels, grad = fused_case(41, T, H, V, w_std=0.1, oov=[(8191, 5000)])
+    gh, gw = _bwd(lmh, hidden, weight, labels, grad, S07)
+    rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, S07)
+    assert rel_frob(gh, rgh) < RTOL_FROB_GRAD
+    assert rel_frob(gw, rgw) < RTOL_FROB_GRAD
+
+
+def test_fused_backward_all_out_of_vocab(lmh):
+    T, H, V = 50, 64, 700
+    hidden, weight, labels, grad = fused_case(43, T, H, V)
+    labels[:] = -100
+    gh, gw = _bwd(lmh, hidden, weight, labels, grad, 1.0)
+    rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, 1.0)
+    assert rel_frob(gh, rgh) < RTOL_FROB_GRAD
+    assert rel_frob(gw, rgw) < RTOL_FROB_GRAD
+
+
+def test_backward_deterministic_run_to_run(lmh):
+    import torch
+
+    T, H, V = 400, 128, 3000
+    hidden, weight, labels, grad = fused_case(51, T, H, V)
+    h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
+    a = lmh.lmhead_logprob_bwd(h, w, lab, g, S07)
+    b = lmh.lmhead_logprob_bwd(h, w, lab, g, S07)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ----------------------------------------------------------------- logits path
+@pytest.mark.parametrize("s", [1.0, S07])
+@pytest.mark.parametrize("T,V", [(300, 5000), (64, 152064), (5, 4999), (3, 1), (130, 8)])
+def test_logits_path_matches_oracle(lmh, T, V, s):
+    import torch
+
+    wl = W.LOGITS
+    inp = W.logits_inputs(wl, T=T, V=V)
+    logits, labels = inp["logits"], inp["labels"]
+    if T > 2:
+        labels[0] = -100
+        labels[1] = V - 1
+    lp, ent, lse = lmh.logprob_from_logits(to_dev_bf16(logits), to_dev(labels), s, want_lse=True)
+    torch.cuda.synchronize()
+    rlp, rent, rlse = oracle.logprob_from_logits(f64(logits), labels, s)
+    assert max_abs(lp.cpu().numpy(), rlp) < ATOL_LOGPROB
+    assert max_abs(ent.cpu().numpy(), rent) < ATOL_LOGPROB
+    assert max_abs(lse.cpu().numpy(), rlse) < ATOL_LOGPROB
+
+
+def test_logits_path_equals_fused_path_on_same_logits(lmh):
+    """Fused path with weight = identity sees the same logits as the logits path."""
+    import torch
+
+    T, V = 40, 512
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    eye = W.f32_to_bf16_bits(np.eye(V, dtype=np.float32))
+    lp1, ent1, _ = lmh.logprob_from_logits(to_dev_bf16(inp["logits"]), to_dev(inp["labels"]), S07)
+    lp2, ent2, _ = lmh.lmhead_logprob_fwd(to_dev_bf16(inp["logits"]), to_dev_bf16(eye),
+                                          to_dev(inp["labels"]), S07)
+    torch.cuda.synchronize()
+    assert max_abs(lp1.cpu().numpy(), lp2.cpu().numpy()) < 1e-4
+    assert max_abs(ent1.cpu().numpy(), ent2.cpu().numpy()) < 1e-4
+
+
+# ----------------------------------------------------------------- status
+def test_bounded_wait_selftest_reports_timeout(lmh):
+    assert lmh.lmhead_selftest_wait_timeout(2_000_000) == lmh.LMH_ERR_DEVICE_TIMEOUT
+    with pytest.raises(lmh.LMHeadError) as e:
+        lmh.lmhead_device_status()
+    assert e.value.code == lmh.LMH_ERR_DEVICE_TIMEOUT
+    assert lmh.lmhead_device_status() == 0  # cleared by the read
+    # the context is still usable
+    test_engine_gemm_matches_fp64(lmh, 128, 256, 64)
