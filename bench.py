@@ -1,0 +1,572 @@
+#!/usr/bin/env python
+"""Benchmark of the batch-invariant LM-head log-prob library on GB300.
+
+One step = one pass of the fused hot path over one batch: the fused forward
+(vocab projection + online log-softmax + label gather + entropy, lse kept)
+followed by the fused backward (recomputed logits -> dlogits -> grad_hidden,
+grad_weight). Workload: T=16384 tokens, H=3584, V=152064, inv_temperature =
+1/0.7 (fp32), bf16 hidden ~ N(0,1), weight ~ N(0, 0.02^2), labels uniform,
+upstream grad ~ N(0,1). Inputs (weight 1.09 GB) are larger than L2, so no L2
+flush is needed between steps.
+
+Prints ONE JSON line (rank 0). Besides the contract keys it carries:
+  roofline       the dominant kernel of the step against the measured peak
+  kernels        per-kernel average durations measured with CUDA events
+  fwd_only       forward-only tokens/s of the same workload and of
+                 T=4096 H=4096 V=32000
+  logits_path    the sampler formula on bf16 logits [8192, 152064] vs HBM
+  cpu_baseline   the fp64 CPU oracle timed on a bounded sample on host cores
+  e2e            the same step through the binding with pinned host inputs
+                 copied in and log-probs/entropy copied out every step
+
+Multi-GPU (torchrun): every rank runs its own replica of the workload on its
+own GPU (weak scaling, no data-path collective); the step time is the max over
+ranks and `value` sums the tokens of all ranks.
+
+--impl reference times the fp64 CPU oracle (the reference arm of this build)
+on host cores, on a bounded row sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s fused LM-head logprob fwd & fwd+bwd; % bf16 tensor peak / % HBM"
+WORKLOAD = "fused forward+backward T=16384 H=3584 V=152064 inv_T=1/0.7 (bf16 in, fp32 accumulate)"
+T_, H_, V_ = 16384, 3584, 152064
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_KINDS = ("fused_fwd_gemm", "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm")
+
+
+def inv_temperature() -> float:
+    import numpy as np
+
+    return float(np.float32(1.0 / 0.7))
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "of measured"
+    return dict(FALLBACK_PEAKS), "of fallback"
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source has changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    src = os.path.join(ROOT, d.get("source_file", ""))
+    if not os.path.exists(src) or file_sha(src) != d.get("source_sha"):
+        return None
+    k = d.get("kernels", {}).get(kernel)
+    return None if k is None else k.get("dram_bytes_per_full_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="lmh_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                if self.uuid and parts[1] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        mhz = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def aggregate_tokens_per_s(tokens_per_rank: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (max_ms / 1e3)
+
+
+# ----------------------------------------------------------------------------- oracle legs
+_SAMPLE_CACHE = {}
+
+
+def oracle_sample(n_rows: int):
+    """The first n_rows rows of the workload's seeded CPU inputs (full H and V)."""
+    import workloads as W
+
+    wl = W.QWEN
+    if "full" not in _SAMPLE_CACHE or _SAMPLE_CACHE["full"][0].shape[0] < n_rows:
+        inp = W.fused_inputs(wl, T=max(n_rows, 256))
+        _SAMPLE_CACHE["full"] = (W.bf16_bits_to_f32(inp["hidden"]), W.bf16_bits_to_f32(inp["weight"]),
+                                 inp["labels"], inp["grad"])
+    h, w, lab, g = _SAMPLE_CACHE["full"]
+    return h[:n_rows], w, lab[:n_rows], g[:n_rows], wl.inv_temperature
+
+
+def oracle_step(sample):
+    import oracle
+
+    h, w, lab, g, s = sample
+    oracle.fused_forward(h, w, lab, s)
+    oracle.fused_backward(h, w, lab, g, s)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(target_s: float = 15.0):
+    """fp64 oracle fwd+bwd on a row sample of the workload (full H and V)."""
+    probe_rows = 8
+    sample = oracle_sample(probe_rows)
+    t0 = time.perf_counter()
+    oracle_step(sample)
+    t_probe = time.perf_counter() - t0
+    rows = int(max(probe_rows, min(256, probe_rows * target_s / max(t_probe, 1e-3))))
+    sample = oracle_sample(rows)
+    t0 = time.perf_counter()
+    oracle_step(sample)
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{rows} rows of the workload (full H={H_}, V={V_}), fp64 forward+backward "
+                      f"incl. grad_weight over the sampled rows, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    probe = oracle_sample(4)
+    t0 = time.perf_counter()
+    oracle_step(probe)
+    per_step_4 = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(64, 4 * budget / max(per_step_4, 1e-3))))
+    sample = oracle_sample(rows)
+    for _ in range(args.warmup):
+        oracle_step(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(sample)
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_, "H": H_, "V": V_,
+                   "inv_temperature": inv_temperature(),
+                   "sample_rows_per_step": rows, "l2": "host run; not applicable"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows} rows per step of the workload (full H, V), fp64 "
+                                   f"forward+backward"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def make_inputs(T, H, V, seed, dev):
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    hidden = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
+    weight = (torch.randn(V, H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    labels = torch.randint(0, V, (T,), generator=g, device=dev, dtype=torch.int32)
+    grad = torch.randn(T, generator=g, device=dev)
+    return hidden, weight, labels, grad
+
+
+def timed(fn, steps, warmup):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_gpu(args):
+    import torch
+
+    import invariant_lm_head_gb300 as lmh
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lmh.build()
+    lmh.library()
+    peaks, peak_src = load_peaks()
+    s = inv_temperature()
+
+    T, H, V = T_, H_, V_
+    hidden, weight, labels, grad = make_inputs(T, H, V, 1234 + rank, dev)
+    lp = torch.empty(T, device=dev)
+    ent = torch.empty(T, device=dev)
+    lse = torch.empty(T, device=dev)
+    gh = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    gw = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws_f = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, T, H, V), dtype=torch.uint8,
+                       device=dev)
+    ws_b = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_BWD, T, H, V), dtype=torch.uint8,
+                       device=dev)
+
+    def fwd():
+        lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp, out_entropy=ent,
+                               out_lse=lse, workspace=ws_f)
+
+    def bwd():
+        lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse, grad_hidden=gh,
+                               grad_weight=gw, workspace=ws_b)
+
+    for _ in range(args.warmup):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = lmh.lmhead_kernel_launches()
+    lmh.lmhead_timing_enable(True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    ev_start.record()
+    for _ in range(args.steps):
+        fwd()
+        bwd()
+    ev_end.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = ev_start.elapsed_time(ev_end)
+    launches = lmh.lmhead_kernel_launches() - launches0
+    recs = lmh.lmhead_timing_read()
+    lmh.lmhead_timing_enable(False)
+    clk = clocks.stop()
+    lmh.lmhead_device_status()
+    max_ms = reduce_max(total_ms, ws, dev)
+    ms_per_step = max_ms / args.steps
+    value = aggregate_tokens_per_s(T, ws, args.steps, max_ms)
+
+    # per-kernel durations (CUDA events on the launching stream, timed region)
+    per = {}
+    for name, ms in recs:
+        per.setdefault(name, []).append(ms)
+    kernels = {k: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
+               for k, v in per.items()}
+    rows_per_chunk = 8192
+    flops_per_launch = {
+        "fused_fwd_gemm": 2.0 * T * H * V,
+        "dlogits_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
+        "grad_hidden_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
+        "grad_weight_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
+    }
+    for k, info in kernels.items():
+        if k in flops_per_launch:
+            info["tflops"] = flops_per_launch[k] / (info["avg_ms"] * 1e-3) / 1e12
+    dominant = max(kernels, key=lambda k: kernels[k]["total_ms"]) if kernels else None
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    roofline = None
+    if dominant in flops_per_launch:
+        ach = kernels[dominant]["tflops"]
+        roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                    "peak_source": f"bf16_tflops_sustained {peak_src} (kernel timed inside a "
+                                   f"multi-kernel step)",
+                    "traffic": traffic_for(dominant),
+                    "algorithmic_flops_per_launch": flops_per_launch[dominant]}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T, "H": H, "V": V, "inv_temperature": s,
+                   "parallelism": f"replicas x{ws} (rows per GPU fixed)",
+                   "l2": "inputs larger than L2 (weight 1.09 GB); no flush"},
+        "gpu_launches": launches, "roofline": roofline, "kernels": kernels, "clocks": clk,
+        "model_tflops_per_gpu": 6.0 * T * H * V / (ms_per_step * 1e-3) / 1e12,
+    }
+
+    # ------------------------------------------------------------- e2e (host buffers)
+    h_host = hidden.cpu().pin_memory()
+    w_host = weight.cpu().pin_memory()
+    l_host = labels.cpu().pin_memory()
+    g_host = grad.cpu().pin_memory()
+    lp_host = torch.empty(T, dtype=torch.float32).pin_memory()
+    ent_host = torch.empty(T, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        hidden.copy_(h_host, non_blocking=True)
+        weight.copy_(w_host, non_blocking=True)
+        labels.copy_(l_host, non_blocking=True)
+        grad.copy_(g_host, non_blocking=True)
+        fwd()
+        bwd()
+        lp_host.copy_(lp, non_blocking=True)
+        ent_host.copy_(ent, non_blocking=True)
+
+    barrier(ws)
+    e2e_ms = reduce_max(timed(e2e_step, args.steps, 2) * args.steps, ws, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_host, w_host, l_host, g_host))
+    line["e2e"] = {"value": aggregate_tokens_per_s(T, ws, args.steps, e2e_ms), "unit": "tokens/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 2 * T * 4}
+    del h_host, w_host
+
+    if ws == 1 and not args.no_extras:
+        # forward only, same workload
+        f_ms = timed(fwd, args.steps, 2)
+        extras = {"fwd_only": {"T=16384 H=3584 V=152064": {
+            "tokens_per_s": T / (f_ms * 1e-3), "ms": f_ms,
+            "tflops": 2.0 * T * H * V / (f_ms * 1e-3) / 1e12}}}
+        gh = gw = ws_b = hidden = weight = None  # free before the next legs
+        torch.cuda.empty_cache()
+        # forward only, Llama-like shape
+        T2, H2, V2 = 4096, 4096, 32000
+        h2, w2, l2, _ = make_inputs(T2, H2, V2, 99, dev)
+        ws2 = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, T2, H2, V2), dtype=torch.uint8,
+                          device=dev)
+        lp2 = torch.empty(T2, device=dev)
+        ent2 = torch.empty(T2, device=dev)
+        f2 = timed(lambda: lmh.lmhead_logprob_fwd(h2, w2, l2, 1.0, out_logprob=lp2,
+                                                   out_entropy=ent2, workspace=ws2),
+                   args.steps, 3)
+        extras["fwd_only"]["T=4096 H=4096 V=32000"] = {
+            "tokens_per_s": T2 / (f2 * 1e-3), "ms": f2,
+            "tflops": 2.0 * T2 * H2 * V2 / (f2 * 1e-3) / 1e12,
+            "frac_of_burst_peak": 2.0 * T2 * H2 * V2 / (f2 * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+        del h2, w2
+        # logits path: bf16 logits [8192, 152064] (2.49 GB > L2)
+        T3, V3 = 8192, 152064
+        g3 = torch.Generator(device=dev)
+        g3.manual_seed(7)
+        x = (torch.randn(T3, V3, generator=g3, device=dev) * 2.0
+             + torch.randn(T3, 1, generator=g3, device=dev)).to(torch.bfloat16)
+        l3 = torch.randint(0, V3, (T3,), generator=g3, device=dev, dtype=torch.int32)
+        lp3 = torch.empty(T3, device=dev)
+        ent3 = torch.empty(T3, device=dev)
+        lmh.lmhead_timing_enable(True)
+        l_ms = timed(lambda: lmh.logprob_from_logits(x, l3, 1.0, out_logprob=lp3,
+                                                     out_entropy=ent3), args.steps, 3)
+        krec = [ms for name, ms in lmh.lmhead_timing_read() if name == "logits_rowwise"]
+        lmh.lmhead_timing_enable(False)
+        k_ms = sum(krec) / len(krec)
+        gbs = T3 * V3 * 2 / (k_ms * 1e-3) / 1e9
+        extras["logits_path"] = {
+            "workload": "sampler formula on bf16 logits T=8192 V=152064",
+            "tokens_per_s": T3 / (l_ms * 1e-3), "ms": l_ms,
+            "roofline": {"kernel": "logits_rowwise", "bound": "hbm", "achieved": round(gbs, 1),
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": round(gbs / peaks["hbm_gbs"], 4),
+                         "peak_source": f"hbm_gbs {peak_src}",
+                         "traffic": traffic_for("logits_rowwise"),
+                         "algorithmic_bytes_per_launch": T3 * V3 * 2}}
+        del x
+        torch.cuda.empty_cache()
+        line.update(extras)
+
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def run_case(args):
+    """One kernel family on one shape, for profiling: --case fwd|bwd|logits --shape ..."""
+    import torch
+
+    import invariant_lm_head_gb300 as lmh
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lmh.build()
+    dims = [int(x) for x in args.shape.split(",")]
+    s = inv_temperature()
+    if args.case == "logits":
+        T, V = dims
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        x = (torch.randn(T, V, generator=g, device=dev) * 2.0
+             + torch.randn(T, 1, generator=g, device=dev)).to(torch.bfloat16)
+        lab = torch.randint(0, V, (T,), generator=g, device=dev, dtype=torch.int32)
+        lp = torch.empty(T, device=dev)
+        ent = torch.empty(T, device=dev)
+        fn = lambda: lmh.logprob_from_logits(x, lab, s, out_logprob=lp, out_entropy=ent)  # noqa: E731
+        work = {"bytes": T * V * 2}
+    else:
+        T, H, V = dims
+        hidden, weight, labels, grad = make_inputs(T, H, V, 1234, dev)
+        lp = torch.empty(T, device=dev)
+        ent = torch.empty(T, device=dev)
+        lse = torch.empty(T, device=dev)
+        ws_f = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, T, H, V), dtype=torch.uint8,
+                           device=dev)
+        lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp, out_entropy=ent,
+                               out_lse=lse, workspace=ws_f)
+        if args.case == "fwd":
+            fn = lambda: lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp,  # noqa: E731
+                                                out_entropy=ent, out_lse=lse, workspace=ws_f)
+            work = {"flops": 2.0 * T * H * V}
+        else:
+            gh = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            gw = torch.empty(V, H, device=dev)
+            ws_b = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_BWD, T, H, V),
+                               dtype=torch.uint8, device=dev)
+            fn = lambda: lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse,  # noqa: E731
+                                                grad_hidden=gh, grad_weight=gw, workspace=ws_b)
+            work = {"flops": 6.0 * T * H * V}
+    lmh.lmhead_timing_enable(True)
+    ms = timed(fn, args.steps, args.warmup)
+    recs = lmh.lmhead_timing_read()
+    lmh.lmhead_timing_enable(False)
+    lmh.lmhead_device_status()
+    per = {}
+    for name, t in recs:
+        per.setdefault(name, []).append(t)
+    out = {"case": args.case, "shape": dims, "ms": ms,
+           "kernels_avg_ms": {k: sum(v) / len(v) for k, v in per.items()}}
+    if "flops" in work:
+        out["tflops"] = work["flops"] / (ms * 1e-3) / 1e12
+    else:
+        out["gbs"] = work["bytes"] / (ms * 1e-3) / 1e9
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip fwd-only and logits-path legs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits"], default=None,
+                    help="time one entry point on --shape only (profiling aid; no contract line)")
+    ap.add_argument("--shape", default="4096,4096,32000", help="T,H,V (fwd/bwd) or T,V (logits)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.case:
+        return run_case(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -87,7 +87,7 @@ size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
  *                backward to skip its recompute of the statistics)
  *   workspace    >= lmhead_workspace_size(LMH_OP_FWD, T, H, V) bytes,
  *                16-byte aligned; contents need not be initialised
- * T == 0 is a no-op.
+ * T == 0 is a no-op (then every pointer may be NULL).
  */
 int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                        int64_t T, int64_t H, int64_t V, float inv_temperature,
@@ -105,7 +105,7 @@ int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int
  *   lse           f32 [T] from lmhead_logprob_fwd, or NULL to recompute it
  *   workspace     >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) bytes
  * dlogits are rounded to bf16 before both contractions. T == 0 zeroes
- * grad_weight.
+ * grad_weight (then only grad_weight has to be a valid pointer).
  */
 int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                        const float* grad_logprob, const float* lse, int64_t T, int64_t H,
@@ -131,6 +131,22 @@ const char* lmhead_last_error_string(void);
 
 /* ABI version of this header (incremented on incompatible changes). */
 int lmhead_abi_version(void);
+
+/* Number of CUDA kernels this library has launched in this process so far. */
+unsigned long long lmhead_kernel_launches(void);
+
+/*
+ * Per-launch timing (diagnostics, off by default). While enabled, every kernel
+ * launch of the library is bracketed by two CUDA events recorded on the
+ * launching stream. lmhead_timing_enable(1) starts recording and discards old
+ * records; lmhead_timing_enable(0) stops. lmhead_timing_read() waits for the
+ * recorded events, writes up to `capacity` (kind, milliseconds) pairs, sets
+ * *count and discards the records. lmhead_timing_kind_name() names a kind
+ * (for example "fused_fwd_gemm"), "" for an unknown one.
+ */
+int lmhead_timing_enable(int on);
+int lmhead_timing_read(int* kinds, float* ms, int capacity, int* count);
+const char* lmhead_timing_kind_name(int kind);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's status

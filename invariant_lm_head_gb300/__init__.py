@@ -51,6 +51,11 @@ SIGNATURES = {
     "logprob_from_logits": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P], ctypes.c_int),
     "lmhead_last_error_string": ([], ctypes.c_char_p),
     "lmhead_abi_version": ([], ctypes.c_int),
+    "lmhead_kernel_launches": ([], ctypes.c_ulonglong),
+    "lmhead_timing_enable": ([ctypes.c_int], ctypes.c_int),
+    "lmhead_timing_read": ([ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_float), ctypes.c_int,
+                            ctypes.POINTER(ctypes.c_int)], ctypes.c_int),
+    "lmhead_timing_kind_name": ([ctypes.c_int], ctypes.c_char_p),
     "lmhead_device_status": ([_P, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
     "lmhead_selftest_wait_timeout": ([ctypes.c_uint64, _P], ctypes.c_int),
     "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
@@ -204,6 +209,26 @@ def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_log
                                        _stream_ptr(stream))
     _check("logprob_from_logits", rc)
     return out_logprob, out_entropy, out_lse
+
+
+def lmhead_kernel_launches() -> int:
+    """Kernels launched by the library in this process so far."""
+    return int(library().lmhead_kernel_launches())
+
+
+def lmhead_timing_enable(on: bool = True) -> None:
+    """Start (and clear) or stop per-launch event timing inside the library."""
+    _check("lmhead_timing_enable", library().lmhead_timing_enable(1 if on else 0))
+
+
+def lmhead_timing_read(capacity: int = 1 << 16):
+    """[(kernel kind name, milliseconds)] for the launches recorded since enabling."""
+    kinds = (ctypes.c_int * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = ctypes.c_int(0)
+    lib = library()
+    _check("lmhead_timing_read", lib.lmhead_timing_read(kinds, ms, capacity, ctypes.byref(n)))
+    return [(lib.lmhead_timing_kind_name(kinds[i]).decode(), float(ms[i])) for i in range(n.value)]
 
 
 def lmhead_device_status(stream=None) -> int:

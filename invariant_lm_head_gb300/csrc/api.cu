@@ -6,7 +6,9 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -48,6 +50,7 @@ struct DeviceInfo {
 };
 
 std::mutex g_mu;
+std::atomic<unsigned long long> g_launches{0};
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -205,6 +208,74 @@ int launch_status(cudaError_t e, const char* what) {
     if (_rc != LMH_OK) return _rc; \
   } while (0)
 
+// ---------------------------------------------------------------- kernel timing
+// Opt-in diagnostics: with timing enabled, every launch is bracketed by two
+// CUDA events recorded on the launching stream; lmhead_timing_read() returns
+// the kind and duration of each launch. Off by default (no events recorded).
+enum Kind : int {
+  K_FWD_GEMM = 0,
+  K_FWD_MERGE,
+  K_DLOGITS_GEMM,
+  K_DHIDDEN_GEMM,
+  K_DWEIGHT_GEMM,
+  K_TRANSPOSE_W,
+  K_TRANSPOSE_H,
+  K_LOGITS_ROWWISE,
+  K_ENGINE_GEMM,
+  K_SELFTEST,
+  K_COUNT
+};
+const char* const kKindNames[K_COUNT] = {
+    "fused_fwd_gemm", "fwd_merge", "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm",
+    "transpose_weight", "transpose_hidden", "logits_rowwise", "engine_gemm", "selftest_wait"};
+
+struct TimingRec {
+  int kind;
+  cudaEvent_t b, e;
+};
+std::mutex g_tmu;
+std::atomic<bool> g_timing{false};
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct KernelTimer {
+  int kind;
+  cudaStream_t st;
+  cudaEvent_t b = nullptr;
+  KernelTimer(int k, cudaStream_t s) : kind(k), st(s) {
+    if (!g_timing.load(std::memory_order_relaxed)) return;
+    std::lock_guard<std::mutex> lk(g_tmu);
+    b = take_event();
+    if (b) cudaEventRecord(b, st);
+  }
+  ~KernelTimer() {
+    if (!b) return;
+    std::lock_guard<std::mutex> lk(g_tmu);
+    cudaEvent_t e = take_event();
+    if (!e) return;
+    cudaEventRecord(e, st);
+    g_recs.push_back(TimingRec{kind, b, e});
+  }
+};
+
+#define LMH_LAUNCH(kind, st, expr, what)                  \
+  do {                                                    \
+    KernelTimer _kt((kind), (st));                        \
+    int _rc = launch_status((expr), (what));              \
+    if (_rc != LMH_OK) return _rc;                        \
+  } while (0)
+
 // Forward statistics into `w`, merged into the outputs.
 int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* weight,
                 const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
@@ -225,18 +296,64 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_u = w.pu;
   p.part_zl = w.pzl;
   p.part_ld = T;
-  LMH_TRY(launch_status(
-      lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
-      "fused forward"));
-  LMH_TRY(launch_status(lmh::launch_fwd_merge(w.pm, w.ps, w.pu, w.pzl, labels, T, n_fwd_chunks(V),
-                                              V, out_lp, out_ent, out_lse, st),
-                        "forward merge"));
+  LMH_LAUNCH(K_FWD_GEMM, st,
+             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
+             "fused forward");
+  LMH_LAUNCH(K_FWD_MERGE, st,
+             lmh::launch_fwd_merge(w.pm, w.ps, w.pu, w.pzl, labels, T, n_fwd_chunks(V), V, out_lp,
+                                   out_ent, out_lse, st),
+             "forward merge");
   return LMH_OK;
 }
 
 }  // namespace
 
+namespace lmh {
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace lmh
+
 extern "C" {
+
+unsigned long long lmhead_kernel_launches(void) { return g_launches.load(); }
+
+int lmhead_timing_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  for (const TimingRec& r : g_recs) {
+    g_event_pool.push_back(r.b);
+    g_event_pool.push_back(r.e);
+  }
+  g_recs.clear();
+  g_timing.store(on != 0);
+  return ok();
+}
+
+int lmhead_timing_read(int* kinds, float* ms, int capacity, int* count) {
+  if (!count || capacity < 0 || (capacity > 0 && (!kinds || !ms)))
+    return fail(LMH_ERR_INVALID_ARG, "lmhead_timing_read: bad arguments");
+  std::lock_guard<std::mutex> lk(g_tmu);
+  int n = 0;
+  int rc = LMH_OK;
+  for (const TimingRec& r : g_recs) {
+    if (n < capacity) {
+      float t = 0.f;
+      cudaError_t e = cudaEventSynchronize(r.e);
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.b, r.e);
+      if (e != cudaSuccess) rc = fail(LMH_ERR_LAUNCH, "timing: %s", cudaGetErrorString(e));
+      kinds[n] = r.kind;
+      ms[n] = t;
+      ++n;
+    }
+    g_event_pool.push_back(r.b);
+    g_event_pool.push_back(r.e);
+  }
+  g_recs.clear();
+  *count = n;
+  return rc == LMH_OK ? ok() : rc;
+}
+
+const char* lmhead_timing_kind_name(int kind) {
+  return (kind >= 0 && kind < K_COUNT) ? kKindNames[kind] : "";
+}
 
 const char* lmhead_last_error_string(void) { return t_err; }
 
@@ -266,13 +383,13 @@ int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int
                        size_t workspace_bytes, struct CUstream_st* stream) {
   LMH_TRY(check_dims(T, H, V, true));
   LMH_TRY(check_temperature(inv_temperature));
+  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
   LMH_TRY(check_ptr(hidden, 16, "hidden"));
   LMH_TRY(check_ptr(weight, 16, "weight"));
   LMH_TRY(check_ptr(labels, 4, "labels"));
   LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
   LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
   LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
-  if (T == 0) return ok();
   const size_t need = lmhead_workspace_size(LMH_OP_FWD, T, H, V);
   if (!workspace || workspace_bytes < need)
     return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
@@ -293,22 +410,22 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
                        struct CUstream_st* stream) {
   LMH_TRY(check_dims(T, H, V, true));
   LMH_TRY(check_temperature(inv_temperature));
-  LMH_TRY(check_ptr(hidden, 16, "hidden"));
-  LMH_TRY(check_ptr(weight, 16, "weight"));
-  LMH_TRY(check_ptr(labels, 4, "labels"));
-  LMH_TRY(check_ptr(grad_logprob, 4, "grad_logprob"));
-  LMH_TRY(check_ptr(lse, 4, "lse", true));
-  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
   LMH_TRY(check_ptr(grad_weight, 16, "grad_weight"));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   DeviceInfo* dev = nullptr;
-  if (T == 0) {
+  if (T == 0) {  // only grad_weight is written (zeros); other pointers may be NULL
     LMH_TRY(device_info(&dev));
     LMH_TRY(launch_status(
         cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * sizeof(float), st),
         "zero grad_weight"));
     return ok();
   }
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(grad_logprob, 4, "grad_logprob"));
+  LMH_TRY(check_ptr(lse, 4, "lse", true));
+  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
   const size_t need = lmhead_workspace_size(LMH_OP_BWD, T, H, V);
   if (!workspace || workspace_bytes < need)
     return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
@@ -323,8 +440,8 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
     lse = w.lse;
   }
   // weight^T [H][Vpad]: K-major B operand of grad_hidden = dl * weight.
-  LMH_TRY(launch_status(lmh::launch_transpose_bf16(weight, V, H, H, w.wt, w.vpad, st),
-                        "transpose weight"));
+  LMH_LAUNCH(K_TRANSPOSE_W, st, lmh::launch_transpose_bf16(weight, V, H, H, w.wt, w.vpad, st),
+             "transpose weight");
   CUtensorMap t_w, t_wt;
   LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
   LMH_TRY(make_tmap(&t_wt, w.wt, V, H, w.vpad * 2, lmh::kBK, lmh::kBN));
@@ -333,8 +450,8 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
     // hidden^T [H][Tcpad]: K-major B operand of grad_weight = dl^T * hidden.
-    LMH_TRY(launch_status(lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st),
-                          "transpose hidden"));
+    LMH_LAUNCH(K_TRANSPOSE_H, st, lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st),
+               "transpose hidden");
     CUtensorMap t_h, t_dl, t_dlt, t_ht;
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM));
@@ -356,8 +473,8 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
     p.ld_out = w.vpad;
     p.out_bf16_t = w.dlt;
     p.ld_out_t = w.tcpad;
-    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
-                          "dlogits"));
+    LMH_LAUNCH(K_DLOGITS_GEMM, st, lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
+               "dlogits");
     // grad_hidden rows = dl * weight   (K = V)
     lmh::GemmParams q{};
     q.status = dev->status;
@@ -366,8 +483,9 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
     q.K = static_cast<int>(V);
     q.out_bf16 = grad_hidden + c0 * H;
     q.ld_out = H;
-    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_wt, q, 1, dev->sms, st),
-                          "grad_hidden"));
+    LMH_LAUNCH(K_DHIDDEN_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_wt, q, 1, dev->sms, st),
+               "grad_hidden");
     // grad_weight (+)= dl^T * hidden   (K = rows of this chunk)
     lmh::GemmParams r{};
     r.status = dev->status;
@@ -377,8 +495,9 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
     r.out_f32 = grad_weight;
     r.ld_out_f32 = H;
     r.accumulate = c0 > 0 ? 1 : 0;
-    LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreF32, t_dlt, t_ht, r, 1, dev->sms, st),
-                          "grad_weight"));
+    LMH_LAUNCH(K_DWEIGHT_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::StoreF32, t_dlt, t_ht, r, 1, dev->sms, st),
+               "grad_weight");
   }
   return ok();
 }
@@ -388,18 +507,19 @@ int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T
                         float* out_lse, struct CUstream_st* stream) {
   LMH_TRY(check_dims(T, 8, V, false));
   LMH_TRY(check_temperature(inv_temperature));
+  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
   LMH_TRY(check_ptr(logits, (V % 8 == 0) ? 16 : 2, "logits"));
   LMH_TRY(check_ptr(labels, 4, "labels"));
   LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
   LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
   LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
-  if (T == 0) return ok();
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
-  LMH_TRY(launch_status(
-      lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob, out_entropy,
-                                 out_lse, dev->sms, reinterpret_cast<cudaStream_t>(stream)),
-      "logits log-prob"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_LAUNCH(K_LOGITS_ROWWISE, st,
+             lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob,
+                                        out_entropy, out_lse, dev->sms, st),
+             "logits log-prob");
   return ok();
 }
 
@@ -426,8 +546,8 @@ int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) 
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_TRY(launch_status(lmh::launch_wait_selftest(dev->status, limit_ns, dev->selftest, st),
-                        "wait self-test"));
+  LMH_LAUNCH(K_SELFTEST, st, lmh::launch_wait_selftest(dev->status, limit_ns, dev->selftest, st),
+             "wait self-test");
   int result = -1;
   cudaError_t e;
   if ((e = cudaMemcpyAsync(&result, dev->selftest, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
@@ -460,9 +580,9 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   p.out_f32 = D;
   p.ld_out_f32 = N;
   p.accumulate = 0;
-  LMH_TRY(launch_status(lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms,
-                                         reinterpret_cast<cudaStream_t>(stream)),
-                        "engine gemm"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_LAUNCH(K_ENGINE_GEMM, st, lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st),
+             "engine gemm");
   return ok();
 }
 

@@ -370,7 +370,9 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmPar
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   gemm_tc_kernel<E><<<grid, kGemmThreads, kSmemBytes, stream>>>(a, b, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace

@@ -55,6 +55,9 @@ struct GemmParams {
   int accumulate;
 };
 
+// Counts every kernel this library launches (reported by lmhead_kernel_launches).
+void note_launch();
+
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
                         int tiles_per_unit, int num_sms, cudaStream_t stream);

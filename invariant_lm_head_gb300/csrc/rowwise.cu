@@ -264,7 +264,9 @@ cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels,
   else
     logits_logprob_scalar_kernel<<<grid, kRowThreads, 0, stream>>>(logits, labels, T, V, scale2,
                                                                     out_lp, out_ent, out_lse);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pzl,
@@ -275,7 +277,9 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
   const int64_t blocks = (T + threads - 1) / threads;
   fwd_merge_kernel<<<(unsigned)blocks, threads, 0, stream>>>(pm, ps, pu, pzl, labels, T, n_vunits,
                                                              V, out_lp, out_ent, out_lse);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t ld_in,
@@ -284,13 +288,17 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols
   const int64_t gy = (rows + 63) / 64;
   dim3 grid((unsigned)((cols + 63) / 64), (unsigned)(gy < 65535 ? gy : 65535));
   transpose_bf16_kernel<<<grid, 256, 0, stream>>>(in, rows, cols, ld_in, out, ld_out);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, int* result,
                                  cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns, result);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
 }
 
 }  // namespace lmh

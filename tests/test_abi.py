@@ -23,8 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
-                       text, flags=re.M)
+    names = re.findall(r"^\s*[A-Za-z_][\w \t*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
     return sorted(set(names))
 
 
@@ -89,6 +88,7 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     assert _call_fwd(lib, ws=None) == lmh.LMH_ERR_WORKSPACE
     assert b"workspace" in lib.lmhead_last_error_string()
     assert _call_fwd(lib, T=0) == lmh.LMH_OK  # empty batch: nothing to do
+    assert _call_fwd(lib, T=0, hidden=None, labels=None, lp=None, ws=None) == lmh.LMH_OK
     rc = lib.logprob_from_logits(24, 16, 4, 4096, 1.0, 16, None, None, None)
     assert rc == lmh.LMH_ERR_ALIGNMENT
     rc = lib.logprob_from_logits(18, 16, 4, 4095, 1.0, 16, None, None, None)

@@ -1,0 +1,53 @@
+"""Host logic of bench.py for N > 1 ranks, on CPU with gloo (world size 2):
+max-over-ranks timing and the whole-job throughput aggregate."""
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms = 100.0 + 50.0 * rank  # rank 1 is the slow one
+        bench.barrier(world)
+        worst = bench.reduce_max(ms, world, torch.device("cpu"))
+        out[rank] = (worst, bench.aggregate_tokens_per_s(16384, world, 10, worst))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_max_and_aggregate():
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, start_method="spawn")
+    assert out[0][0] == out[1][0] == 150.0
+    assert out[0][1] == pytest.approx(16384 * 2 * 10 / 0.150)
+
+
+def test_single_rank_aggregate_and_defaults():
+    assert bench.aggregate_tokens_per_s(100, 1, 4, 200.0) == pytest.approx(2000.0)
+    assert bench.reduce_max(3.0, 1, None) == 3.0
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
+
+
+def test_traffic_lookup_ignores_stale_counters(tmp_path, monkeypatch):
+    assert bench.traffic_for("no_such_kernel") is None
