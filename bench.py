@@ -74,17 +74,19 @@ def file_sha(path: str) -> str:
 
 def traffic_for(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source has changed since the counters were taken."""
+    kernel's source has changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    src = os.path.join(ROOT, d.get("source_file", ""))
-    if not os.path.exists(src) or file_sha(src) != d.get("source_sha"):
-        return None
     k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("dram_bytes_per_full_launch")
+    if not k:
+        return None
+    src = os.path.join(ROOT, k.get("source_file", ""))
+    if not os.path.exists(src) or file_sha(src) != k.get("source_sha"):
+        return None
+    return k.get("dram_bytes_per_full_launch")
 
 
 class ClockSampler:

@@ -182,17 +182,24 @@ def fused_grad_hidden_rows(hidden, weight, labels, grad, inv_temperature: float,
     return np.concatenate(out) if out else np.zeros((0, w.shape[1]))
 
 
-def grad_weight_from_rows(hidden, weight, labels, grad, inv_temperature: float, rows):
+def grad_weight_from_rows(hidden, weight, labels, grad, inv_temperature: float, rows,
+                          vocab_rows=None):
     """sum over the listed rows t of dlogit[t, :]^T hidden[t, :], [V, H].
 
     Equals the full grad_weight when grad[t] = 0 for every row not listed.
+    With ``vocab_rows`` only those rows of the result are formed
+    ([len(vocab_rows), H]); the softmax still runs over the full vocabulary.
     """
     w = _f64(weight)
     labels = np.asarray(labels, dtype=np.int64)
     g = _f64(grad)
-    acc = np.zeros(w.shape, dtype=np.float64)
+    out_rows = w.shape[0] if vocab_rows is None else len(vocab_rows)
+    acc = np.zeros((out_rows, w.shape[1]), dtype=np.float64)
     for r in _row_blocks(rows):
         h = _f64(hidden[r])
         z = fp32_scalar(inv_temperature) * (h @ w.T)
-        acc += dlogits(z, labels[r], g[r], inv_temperature).T @ h
+        dl = dlogits(z, labels[r], g[r], inv_temperature)
+        if vocab_rows is not None:
+            dl = dl[:, np.asarray(vocab_rows, dtype=np.int64)]
+        acc += dl.T @ h
     return acc

@@ -248,6 +248,8 @@ def test_row_independence_and_sampled_forms():
     g0[rows] = g[rows]
     _, gw0 = oracle.fused_backward(h, w, lab, g0, S07)
     assert np.max(np.abs(oracle.grad_weight_from_rows(h, w, lab, g0, S07, rows) - gw0)) < 1e-12
+    vr = np.array([3, 0, 63])
+    assert np.max(np.abs(oracle.grad_weight_from_rows(h, w, lab, g0, S07, rows, vr) - gw0[vr])) < 1e-12
 
 
 def test_logits_path_equals_fused_with_identity_weight():
