@@ -124,6 +124,32 @@ int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T
                         float inv_temperature, float* out_logprob, float* out_entropy,
                         float* out_lse, struct CUstream_st* stream);
 
+/*
+ * Forward without a workspace, for callers that cannot allocate device memory
+ * (a plugin whose host framework owns all device memory and hands out no
+ * workspace, or code that must not call cudaMalloc because it can block and
+ * synchronise the device). The pages have no counterpart: this is an addition
+ * of this library.
+ *
+ * Same arguments, results and rules as lmhead_logprob_fwd minus the
+ * workspace. The forward's partials go to a fixed scratch array compiled into
+ * the library (LMH_NOALLOC_SCRATCH_BYTES, 16 MiB, held on every GPU where the
+ * library's device code is loaded until the process exits); nothing is
+ * allocated. The partials need 12 * ceil(V / 1024) * T + 4 * T bytes (each
+ * part rounded up to 256); larger calls return LMH_ERR_WORKSPACE with nothing
+ * launched (for V = 152064 that is T up to about 9300 rows).
+ * The first call on a device looks up the scratch array's device address
+ * (cudaGetSymbolAddress); make it before any stream capture. All calls share
+ * the one array, which keeps the previous call's contents (nothing in it needs
+ * to start at zero). Calls that overlap on the GPU (other streams, or
+ * unordered host threads) race on it: serialise them.
+ */
+#define LMH_NOALLOC_SCRATCH_BYTES (16u << 20)
+int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* labels, int64_t T, int64_t H, int64_t V,
+                               float inv_temperature, float* out_logprob, float* out_entropy,
+                               float* out_lse, struct CUstream_st* stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /* Message of the calling thread's last error ("" if none). */

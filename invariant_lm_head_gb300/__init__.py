@@ -59,6 +59,8 @@ SIGNATURES = {
     "lmhead_device_status": ([_P, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
     "lmhead_selftest_wait_timeout": ([ctypes.c_uint64, _P], ctypes.c_int),
     "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+    "lmhead_logprob_fwd_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P],
+                                   ctypes.c_int),
 }
 
 _lib_handle: Optional[ctypes.CDLL] = None

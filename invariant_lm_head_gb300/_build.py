@@ -21,7 +21,7 @@ CSRC = PKG_DIR / "csrc"
 INCLUDE = ROOT / "include"
 BUILD_DIR = ROOT / "_build"
 LIB_PATH = PKG_DIR / "liblmhead.so"
-SOURCES = ["api.cu", "gemm_tc.cu", "rowwise.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "rowwise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

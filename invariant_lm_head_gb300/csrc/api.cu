@@ -310,6 +310,25 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
 
 namespace lmh {
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int api_set_error(int code, const char* msg) {
+  if (code == LMH_OK) return ok();
+  return fail(code, "%s", msg);
+}
+
+int api_device(int* sms, unsigned** status) {
+  DeviceInfo* d = nullptr;
+  const int rc = device_info(&d);
+  if (rc != LMH_OK) return rc;
+  *sms = d->sms;
+  *status = d->status;
+  return LMH_OK;
+}
+
+int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap(map, base, inner, outer, row_bytes, box_inner, box_outer);
+}
 }  // namespace lmh
 
 extern "C" {

@@ -58,6 +58,14 @@ struct GemmParams {
 // Counts every kernel this library launches (reported by lmhead_kernel_launches).
 void note_launch();
 
+// Shared host helpers of the C ABI (defined in api.cu): record the calling
+// thread's error message, query the current device (sm_103 check, SM count,
+// status word) and encode a 2-D bf16 TMA descriptor. Each returns an LMH_* code.
+int api_set_error(int code, const char* msg);
+int api_device(int* sms, unsigned** status);
+int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
 size_t gemm_smem_bytes();
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
                         int tiles_per_unit, int num_sms, cudaStream_t stream);
