@@ -68,9 +68,9 @@ struct CUstream_st; /* cudaStream_t */
 
 /*
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
- * Returns SIZE_MAX for invalid arguments. The size grows with min(T, 8192)
- * for the backward (fixed row chunks) and linearly with T for the forward's
- * per-vocab-chunk partials (16 bytes per row per 1024 vocabulary columns).
+ * Returns SIZE_MAX for invalid arguments. The forward needs 12 bytes per row
+ * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
+ * row and a bf16 dlogits buffer of min(T, 8192) x V.
  */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 
@@ -104,14 +104,35 @@ int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int
  *   grad_logprob  f32 [T]
  *   lse           f32 [T] from lmhead_logprob_fwd, or NULL to recompute it
  *   workspace     >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) bytes
- * dlogits are rounded to bf16 before both contractions. T == 0 zeroes
- * grad_weight (then only grad_weight has to be a valid pointer).
+ * Rows are processed in fixed chunks of 8192; dlogits of a chunk are rounded
+ * to bf16 before both contractions; grad_weight sums the chunks in ascending
+ * order. T == 0 zeroes grad_weight (then only grad_weight has to be a valid
+ * pointer).
  */
 int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                        const float* grad_logprob, const float* lse, int64_t T, int64_t H,
                        int64_t V, float inv_temperature, uint16_t* grad_hidden,
                        float* grad_weight, void* workspace, size_t workspace_bytes,
                        struct CUstream_st* stream);
+
+/*
+ * Fused backward with an entropy term: differentiates
+ *   sum_t grad_logprob[t] * logprob[t] + grad_entropy[t] * entropy[t].
+ * The SkyRL page leaves entropy under the fused head metric-only ("until
+ * entropy gradients are wired"); this wires it. With p = softmax(z[t]),
+ *   d entropy[t] / d z[t, v] = -p[v] * (z[t, v] - lse[t] + entropy[t]),
+ * so dlogits[t, v] = s * (g[t] * onehot[v] - p[v] * (g[t] + gH[t] *
+ * (z[t, v] - lse[t] + entropy[t]))).
+ *   grad_logprob, grad_entropy  f32 [T] or NULL (= zero); not both NULL
+ *   lse, entropy  f32 [T] from lmhead_logprob_fwd, or NULL to recompute both
+ * Everything else as lmhead_logprob_bwd (same workspace size).
+ */
+int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* labels, const float* grad_logprob,
+                               const float* grad_entropy, const float* lse, const float* entropy,
+                               int64_t T, int64_t H, int64_t V, float inv_temperature,
+                               uint16_t* grad_hidden, float* grad_weight, void* workspace,
+                               size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * Sampler formula on materialised logits (verl page, the
@@ -192,12 +213,14 @@ int lmhead_device_status(struct CUstream_st* stream, unsigned* bits);
 int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
 
 /*
- * The tensor-core engine alone, for engine tests: D[M, N] = A[M, K] B[N, K]^T
- * with A, B bf16 row-major (K % 8 == 0, 16-byte aligned), D f32 row-major
- * (N % 8 == 0, 16-byte aligned), fp32 accumulation in K order.
+ * The tensor-core engine alone, for engine tests: D[M, N] = sum_k A[m, k] B[n, k]
+ * with bf16 operands and an f32 row-major D (N % 8 == 0, 16-byte aligned),
+ * fp32 accumulation in K order. layout bit 0: A is stored [K][M] (else
+ * [M][K]); bit 1: B is stored [K][N] (else [N][K]). Leading dimensions equal
+ * the stored row length, which must be a multiple of 8.
  */
 int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
-                       float* D, struct CUstream_st* stream);
+                       int layout, float* D, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

@@ -58,7 +58,9 @@ SIGNATURES = {
     "lmhead_timing_kind_name": ([ctypes.c_int], ctypes.c_char_p),
     "lmhead_device_status": ([_P, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
     "lmhead_selftest_wait_timeout": ([ctypes.c_uint64, _P], ctypes.c_int),
-    "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, _P, _P], ctypes.c_int),
+    "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P], ctypes.c_int),
+    "lmhead_logprob_entropy_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P,
+                                    ctypes.c_size_t, _P], ctypes.c_int),
     "lmhead_logprob_fwd_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P],
                                    ctypes.c_int),
 }
@@ -191,6 +193,34 @@ def lmhead_logprob_bwd(hidden, weight, labels, grad_logprob, inv_temperature: fl
     return grad_hidden, grad_weight
 
 
+def lmhead_logprob_entropy_bwd(hidden, weight, labels, grad_logprob, grad_entropy,
+                               inv_temperature: float = 1.0, *, lse=None, entropy=None,
+                               grad_hidden=None, grad_weight=None, workspace=None, stream=None):
+    """Backward of sum g*logprob + gH*entropy. Returns (grad_hidden bf16, grad_weight f32)."""
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight, "weight", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    for t, n in ((grad_logprob, "grad_logprob"), (grad_entropy, "grad_entropy"), (lse, "lse"),
+                 (entropy, "entropy")):
+        if t is not None:
+            _need(t, n, torch.float32, dev, 1)
+    T, H = hidden.shape
+    V = weight.shape[0]
+    if grad_hidden is None:
+        grad_hidden = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if grad_weight is None:
+        grad_weight = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws, ws_bytes = _workspace(LMH_OP_BWD, T, H, V, workspace, dev)
+    rc = library().lmhead_logprob_entropy_bwd(
+        _ptr(hidden), _ptr(weight), _ptr(labels), _ptr(grad_logprob), _ptr(grad_entropy),
+        _ptr(lse), _ptr(entropy), T, H, V, float(inv_temperature), _ptr(grad_hidden),
+        _ptr(grad_weight), _ptr(ws), ws_bytes, _stream_ptr(stream))
+    _check("lmhead_logprob_entropy_bwd", rc)
+    return grad_hidden, grad_weight
+
+
 def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_logprob=None,
                         out_entropy=None, out_lse=None, want_entropy: bool = True,
                         want_lse: bool = False, stream=None):
@@ -246,16 +276,22 @@ def lmhead_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
     return library().lmhead_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
 
 
-def lmhead_engine_gemm(A, B, out=None, stream=None):
-    """D = A @ B^T through the tensor-core engine (A [M,K], B [N,K] bf16; D f32)."""
+def lmhead_engine_gemm(A, B, out=None, a_kmajor: bool = True, b_kmajor: bool = True,
+                       stream=None):
+    """D = sum_k A[m,k] B[n,k] through the tensor-core engine; D f32 [M, N].
+
+    A is [M, K] when a_kmajor else [K, M]; B is [N, K] when b_kmajor else [K, N].
+    """
     torch = _torch()
     dev = A.device
     _need(A, "A", torch.bfloat16, dev, 2)
     _need(B, "B", torch.bfloat16, dev, 2)
-    M, K = A.shape
-    N = B.shape[0]
+    M, K = A.shape if a_kmajor else (A.shape[1], A.shape[0])
+    N = B.shape[0] if b_kmajor else B.shape[1]
+    layout = (0 if a_kmajor else 1) | (0 if b_kmajor else 2)
     if out is None:
         out = torch.empty(M, N, dtype=torch.float32, device=dev)
-    rc = library().lmhead_engine_gemm(_ptr(A), _ptr(B), M, N, K, _ptr(out), _stream_ptr(stream))
+    rc = library().lmhead_engine_gemm(_ptr(A), _ptr(B), M, N, K, layout, _ptr(out),
+                                      _stream_ptr(stream))
     _check("lmhead_engine_gemm", rc)
     return out

@@ -149,27 +149,23 @@ FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
 
 struct BwdWs {
   FwdWs fwd;
-  float* lse;
+  float* lse;  // recomputed statistics when the caller passes none
   float* lp;
-  uint16_t* wt;  // [H][Vpad]
-  uint16_t* dl;  // [Tc][Vpad]
-  uint16_t* dlt; // [V][Tcpad]
-  uint16_t* ht;  // [H][Tcpad]
-  int64_t vpad, tc, tcpad;
+  float* ent;
+  uint16_t* dl;  // [Tc][Vpad] bf16 dlogits of one row chunk
+  int64_t vpad, tc;
 };
 
 BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
+  (void)H;
   BwdWs w;
   w.vpad = round_up(V, 8);
   w.tc = T < lmh::kBwdRowChunk ? T : lmh::kBwdRowChunk;
-  w.tcpad = round_up(w.tc > 0 ? w.tc : 1, 8);
   w.fwd = carve_fwd(c, T, V);
   w.lse = c.take<float>(T);
   w.lp = c.take<float>(T);
-  w.wt = c.take<uint16_t>(H * w.vpad);
+  w.ent = c.take<float>(T);
   w.dl = c.take<uint16_t>(w.tc * w.vpad);
-  w.dlt = c.take<uint16_t>(V * w.tcpad);
-  w.ht = c.take<uint16_t>(H * w.tcpad);
   return w;
 }
 
@@ -218,16 +214,14 @@ enum Kind : int {
   K_DLOGITS_GEMM,
   K_DHIDDEN_GEMM,
   K_DWEIGHT_GEMM,
-  K_TRANSPOSE_W,
-  K_TRANSPOSE_H,
   K_LOGITS_ROWWISE,
   K_ENGINE_GEMM,
   K_SELFTEST,
   K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {
-    "fused_fwd_gemm", "fwd_merge", "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm",
-    "transpose_weight", "transpose_hidden", "logits_rowwise", "engine_gemm", "selftest_wait"};
+    "fused_fwd_gemm",   "fwd_merge",      "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm",
+    "logits_rowwise",   "engine_gemm",    "selftest_wait"};
 
 struct TimingRec {
   int kind;
@@ -304,6 +298,110 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
                                    out_ent, out_lse, st),
              "forward merge");
   return LMH_OK;
+}
+
+// Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
+// chunk of kBwdRowChunk rows, in ascending order:
+//   dl   = recomputed logits -> dlogits (bf16 [rows][Vpad])
+//   dH   = dl * W          (A = dl K-major, B = W MN-major)
+//   dW  (+)= dl^T * hidden (A = dl MN-major, B = hidden MN-major)
+int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                 const float* grad_lp, const float* grad_ent, const float* lse, const float* ent,
+                 int64_t T, int64_t H, int64_t V, float s, uint16_t* grad_hidden,
+                 float* grad_weight, void* workspace, size_t workspace_bytes,
+                 struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(s));
+  LMH_TRY(check_ptr(grad_weight, 16, "grad_weight"));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceInfo* dev = nullptr;
+  if (T == 0) {  // only grad_weight is written (zeros); other pointers may be NULL
+    LMH_TRY(device_info(&dev));
+    LMH_TRY(launch_status(
+        cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * sizeof(float), st),
+        "zero grad_weight"));
+    return ok();
+  }
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(grad_lp, 4, "grad_logprob", true));
+  LMH_TRY(check_ptr(grad_ent, 4, "grad_entropy", true));
+  LMH_TRY(check_ptr(lse, 4, "lse", true));
+  LMH_TRY(check_ptr(ent, 4, "entropy", true));
+  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
+  if (!grad_lp && !grad_ent)
+    return fail(LMH_ERR_INVALID_ARG, "grad_logprob and grad_entropy are both NULL");
+  const size_t need = lmhead_workspace_size(LMH_OP_BWD, T, H, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  LMH_TRY(check_ptr(workspace, 16, "workspace"));
+  LMH_TRY(device_info(&dev));
+  Carver c{static_cast<char*>(workspace)};
+  const BwdWs w = carve_bwd(c, T, H, V);
+
+  if (!lse || (grad_ent && !ent)) {
+    LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, s, w.lp, w.ent, w.lse, w.fwd, st));
+    lse = w.lse;
+    ent = w.ent;
+  }
+  CUtensorMap t_w, t_w_mn;
+  LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));   // [V][H], K = H
+  LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));      // [K=V][N=H]
+
+  for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
+    const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
+    const uint16_t* h_c = hidden + c0 * H;
+    CUtensorMap t_h, t_h_mn, t_dl, t_dl_mn;
+    LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
+    LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][N=H]
+    LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
+    LMH_TRY(make_tmap(&t_dl_mn, w.dl, V, rows, w.vpad * 2, 64, lmh::kBK));    // [K=rows][M=V]
+
+    lmh::GemmParams p{};
+    p.status = dev->status;
+    p.M = static_cast<int>(rows);
+    p.N = static_cast<int>(V);
+    p.K = static_cast<int>(H);
+    p.scale2 = s * lmh::kLog2e;
+    p.inv_temp = s;
+    p.labels = labels + c0;
+    p.grad = grad_lp ? grad_lp + c0 : nullptr;
+    p.grad_ent = grad_ent ? grad_ent + c0 : nullptr;
+    p.lse = lse + c0;
+    p.ent = grad_ent ? ent + c0 : nullptr;
+    p.out_bf16 = w.dl;
+    p.ld_out = w.vpad;
+    LMH_LAUNCH(K_DLOGITS_GEMM, st, lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
+               "dlogits");
+
+    lmh::GemmParams q{};
+    q.status = dev->status;
+    q.M = static_cast<int>(rows);
+    q.N = static_cast<int>(H);
+    q.K = static_cast<int>(V);
+    q.b_mn = 1;
+    q.out_bf16 = grad_hidden + c0 * H;
+    q.ld_out = H;
+    LMH_LAUNCH(K_DHIDDEN_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st),
+               "grad_hidden");
+
+    lmh::GemmParams r{};
+    r.status = dev->status;
+    r.M = static_cast<int>(V);
+    r.N = static_cast<int>(H);
+    r.K = static_cast<int>(rows);
+    r.a_mn = 1;
+    r.b_mn = 1;
+    r.out_f32 = grad_weight;
+    r.ld_out_f32 = H;
+    r.accumulate = c0 > 0 ? 1 : 0;
+    LMH_LAUNCH(K_DWEIGHT_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st),
+               "grad_weight");
+  }
+  return ok();
 }
 
 }  // namespace
@@ -427,98 +525,21 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
                        int64_t V, float inv_temperature, uint16_t* grad_hidden,
                        float* grad_weight, void* workspace, size_t workspace_bytes,
                        struct CUstream_st* stream) {
-  LMH_TRY(check_dims(T, H, V, true));
-  LMH_TRY(check_temperature(inv_temperature));
-  LMH_TRY(check_ptr(grad_weight, 16, "grad_weight"));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  DeviceInfo* dev = nullptr;
-  if (T == 0) {  // only grad_weight is written (zeros); other pointers may be NULL
-    LMH_TRY(device_info(&dev));
-    LMH_TRY(launch_status(
-        cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * sizeof(float), st),
-        "zero grad_weight"));
-    return ok();
-  }
-  LMH_TRY(check_ptr(hidden, 16, "hidden"));
-  LMH_TRY(check_ptr(weight, 16, "weight"));
-  LMH_TRY(check_ptr(labels, 4, "labels"));
-  LMH_TRY(check_ptr(grad_logprob, 4, "grad_logprob"));
-  LMH_TRY(check_ptr(lse, 4, "lse", true));
-  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
-  const size_t need = lmhead_workspace_size(LMH_OP_BWD, T, H, V);
-  if (!workspace || workspace_bytes < need)
-    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
-  LMH_TRY(check_ptr(workspace, 16, "workspace"));
-  LMH_TRY(device_info(&dev));
-  Carver c{static_cast<char*>(workspace)};
-  const BwdWs w = carve_bwd(c, T, H, V);
+  if (T > 0 && !grad_logprob) return fail(LMH_ERR_INVALID_ARG, "grad_logprob is NULL");
+  return run_backward(hidden, weight, labels, grad_logprob, nullptr, lse, nullptr, T, H, V,
+                      inv_temperature, grad_hidden, grad_weight, workspace, workspace_bytes,
+                      stream);
+}
 
-  if (!lse) {
-    LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, w.lp, nullptr,
-                        w.lse, w.fwd, st));
-    lse = w.lse;
-  }
-  // weight^T [H][Vpad]: K-major B operand of grad_hidden = dl * weight.
-  LMH_LAUNCH(K_TRANSPOSE_W, st, lmh::launch_transpose_bf16(weight, V, H, H, w.wt, w.vpad, st),
-             "transpose weight");
-  CUtensorMap t_w, t_wt;
-  LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
-  LMH_TRY(make_tmap(&t_wt, w.wt, V, H, w.vpad * 2, lmh::kBK, lmh::kBN));
-
-  for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
-    const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
-    const uint16_t* h_c = hidden + c0 * H;
-    // hidden^T [H][Tcpad]: K-major B operand of grad_weight = dl^T * hidden.
-    LMH_LAUNCH(K_TRANSPOSE_H, st, lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st),
-               "transpose hidden");
-    CUtensorMap t_h, t_dl, t_dlt, t_ht;
-    LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));
-    LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM));
-    LMH_TRY(make_tmap(&t_dlt, w.dlt, rows, V, w.tcpad * 2, lmh::kBK, lmh::kBM));
-    LMH_TRY(make_tmap(&t_ht, w.ht, rows, H, w.tcpad * 2, lmh::kBK, lmh::kBN));
-
-    lmh::GemmParams p{};
-    p.status = dev->status;
-    // dlogits for this row chunk (recomputed logits; dl and dl^T in bf16)
-    p.M = static_cast<int>(rows);
-    p.N = static_cast<int>(V);
-    p.K = static_cast<int>(H);
-    p.scale2 = inv_temperature * lmh::kLog2e;
-    p.inv_temp = inv_temperature;
-    p.labels = labels + c0;
-    p.grad = grad_logprob + c0;
-    p.lse = lse + c0;
-    p.out_bf16 = w.dl;
-    p.ld_out = w.vpad;
-    p.out_bf16_t = w.dlt;
-    p.ld_out_t = w.tcpad;
-    LMH_LAUNCH(K_DLOGITS_GEMM, st, lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
-               "dlogits");
-    // grad_hidden rows = dl * weight   (K = V)
-    lmh::GemmParams q{};
-    q.status = dev->status;
-    q.M = static_cast<int>(rows);
-    q.N = static_cast<int>(H);
-    q.K = static_cast<int>(V);
-    q.out_bf16 = grad_hidden + c0 * H;
-    q.ld_out = H;
-    LMH_LAUNCH(K_DHIDDEN_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_wt, q, 1, dev->sms, st),
-               "grad_hidden");
-    // grad_weight (+)= dl^T * hidden   (K = rows of this chunk)
-    lmh::GemmParams r{};
-    r.status = dev->status;
-    r.M = static_cast<int>(V);
-    r.N = static_cast<int>(H);
-    r.K = static_cast<int>(rows);
-    r.out_f32 = grad_weight;
-    r.ld_out_f32 = H;
-    r.accumulate = c0 > 0 ? 1 : 0;
-    LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32, t_dlt, t_ht, r, 1, dev->sms, st),
-               "grad_weight");
-  }
-  return ok();
+int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* labels, const float* grad_logprob,
+                               const float* grad_entropy, const float* lse, const float* entropy,
+                               int64_t T, int64_t H, int64_t V, float inv_temperature,
+                               uint16_t* grad_hidden, float* grad_weight, void* workspace,
+                               size_t workspace_bytes, struct CUstream_st* stream) {
+  return run_backward(hidden, weight, labels, grad_logprob, grad_entropy, lse, entropy, T, H, V,
+                      inv_temperature, grad_hidden, grad_weight, workspace, workspace_bytes,
+                      stream);
 }
 
 int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
@@ -578,10 +599,14 @@ int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) 
 }
 
 int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,
-                       float* D, struct CUstream_st* stream) {
+                       int layout, float* D, struct CUstream_st* stream) {
   if (M < 0 || M > LMH_MAX_DIM || N < 8 || N > LMH_MAX_DIM || K < 8 || K > LMH_MAX_DIM)
     return fail(LMH_ERR_INVALID_ARG, "bad engine GEMM sizes");
-  if (K % 8 != 0 || N % 8 != 0) return fail(LMH_ERR_ALIGNMENT, "K and N must be multiples of 8");
+  if (layout < 0 || layout > 3) return fail(LMH_ERR_INVALID_ARG, "layout must be 0..3");
+  const bool a_mn = (layout & 1) != 0;
+  const bool b_mn = (layout & 2) != 0;
+  if (K % 8 != 0 || N % 8 != 0 || (a_mn && M % 8 != 0))
+    return fail(LMH_ERR_ALIGNMENT, "K, N (and M when A is [K][M]) must be multiples of 8");
   LMH_TRY(check_ptr(A, 16, "A"));
   LMH_TRY(check_ptr(B, 16, "B"));
   LMH_TRY(check_ptr(D, 16, "D"));
@@ -589,13 +614,21 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   CUtensorMap ta, tb;
-  LMH_TRY(make_tmap(&ta, A, K, M, K * 2, lmh::kBK, lmh::kBM));
-  LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
+  if (a_mn)
+    LMH_TRY(make_tmap(&ta, A, M, K, M * 2, 64, lmh::kBK));
+  else
+    LMH_TRY(make_tmap(&ta, A, K, M, K * 2, lmh::kBK, lmh::kBM));
+  if (b_mn)
+    LMH_TRY(make_tmap(&tb, B, N, K, N * 2, 64, lmh::kBK));
+  else
+    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
   lmh::GemmParams p{};
   p.status = dev->status;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
+  p.a_mn = a_mn ? 1 : 0;
+  p.b_mn = b_mn ? 1 : 0;
   p.out_f32 = D;
   p.ld_out_f32 = N;
   p.accumulate = 0;

@@ -1,9 +1,15 @@
 // Tensor-core engine for every contraction of the LM head (sm_103a).
 //
-//   D[M, N] = A[M, K] * B[N, K]^T      A, B bf16, K-major; D fp32 in TMEM
+//   D[M, N] = sum_k A[m, k] * B[n, k]    A, B bf16; D fp32 in TMEM
+//
+// Each operand is either K-major (stored [rows][K]) or MN-major (stored
+// [K][rows]); TMA brings it into shared memory with 128-byte swizzle and the
+// MMA's instruction descriptor carries the matching major bit, so no operand
+// is ever transposed in memory.
 //
 // One persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer: 128x64 A box + 256x64 B box per stage, 4 stages
+//   warp 0      TMA producer: a 128x64 A tile and a 256x64 B tile per stage
+//               (one box each when K-major, 64-wide boxes when MN-major), 4 stages
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=256, K=16, four per 64-wide stage) into one of two
 //               256-column accumulators, and tcgen05.commit frees the stage
@@ -17,13 +23,14 @@
 //              softmax over vocab tiles): per row and per 1024-column vocab
 //              chunk, the base-2 online statistics (m, s, u) and the label
 //              logit; no logit ever reaches HBM.
-//   DLogits    the recomputed-logits backward: dl = g*s*(onehot - p) with
-//              p = exp(z - lse), no one-hot term for an out-of-vocab label
-//              (same page, out-of-vocab gradient fix), written as bf16 dl and
-//              its transpose.
-//   StoreBf16  grad_hidden = dl * W, rounded once to bf16.
-//   StoreF32   grad_weight = dl^T * hidden in fp32, accumulated over row
-//              chunks in ascending order.
+//   DLogits    the recomputed-logits backward: dl = s*(g*onehot - p*(g +
+//              gH*(z - lse + H))) with p = exp(z - lse); the gH term is the
+//              entropy gradient (dH/dz = -p (z - lse + H)); no one-hot term
+//              for an out-of-vocab label (same page, out-of-vocab gradient
+//              fix); written as bf16 dl [rows][V].
+//   StoreBf16  grad_hidden = dl * W (B = W read MN-major), rounded once to bf16.
+//   StoreF32   grad_weight = dl^T * hidden (A = dl and B = hidden read
+//              MN-major) in fp32, accumulated over row chunks in ascending order.
 //
 // Batch invariance: K is walked in the same order for every tile, the work
 // split depends only on N (vocab) and never on M (rows), each row is reduced
@@ -44,6 +51,7 @@ namespace {
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kMnBoxBytes = 64 * kBK * 2;  // one 64(MN) x 64(K) bf16 box
 constexpr int kTmemCols = 512;
 constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
@@ -158,8 +166,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             const uint32_t sA = smem_base + stage * kStageBytes;
             mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-            tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
-            tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+            if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
+#pragma unroll
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d(sA + j * kMnBoxBytes, &tmA, full_bar(stage), m_tile * kBM + 64 * j,
+                            kb * kBK);
+            } else {
+              tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+            }
+            if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
+#pragma unroll
+              for (int j = 0; j < kBN / 64; ++j)
+                tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
+                            n_tile * kBN + 64 * j, kb * kBK);
+            } else {
+              tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+            }
             ++issued;
             if (++stage == kStages) {
               stage = 0;
@@ -188,7 +210,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+      const uint32_t idesc = idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
@@ -210,13 +232,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_fence_after();
             const uint32_t sA = smem_base + stage * kStageBytes;
-            const uint64_t adesc = sw128_kmajor_desc(sA);
-            const uint64_t bdesc = sw128_kmajor_desc(sA + kABytes);
+            const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
+            const uint64_t bdesc =
+                p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
+            // One K=16 step: +32 bytes inside a K-major 128-byte row, or +16
+            // rows of 128 bytes (two 8-row atoms) in an MN-major tile; in the
+            // descriptor's 16-byte address units that is +2 or +128.
+            const uint64_t astep = p.a_mn ? 128ull : 2ull;
+            const uint64_t bstep = p.b_mn ? 128ull : 2ull;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              // +32 bytes along K inside the 128-byte swizzled row = +2 in the
-              // descriptor's 16-byte address units.
-              tc_mma_bf16(d_tmem, adesc + 2ull * k, bdesc + 2ull * k, idesc,
+              tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc,
                           (kb > 0 || k > 0) ? 1u : 0u);
             }
             tc_commit(empty_bar(stage));
@@ -247,14 +273,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
       // per-row constants
       int lab = -1;
-      float gs = 0.f, lse2 = 0.f;
+      float lse2 = 0.f, gs = 0.f, c0 = 0.f, c1 = 0.f;
       if constexpr (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
         if (row_ok) lab = p.labels[row];
       }
       if constexpr (E == (int)Epi::DLogits) {
         if (row_ok) {
-          gs = p.grad[row] * p.inv_temp;
+          // dl = s * (g * onehot - p * (g + gH * (z - lse + H))), z - lse = ln2 * t
+          // with t = y - lse2: the coefficient of p is c0 + c1 * t.
+          const float g = p.grad ? p.grad[row] : 0.f;
+          const float ge = p.grad_ent ? p.grad_ent[row] : 0.f;
           lse2 = p.lse[row] * kLog2e;
+          gs = g * p.inv_temp;
+          c0 = p.inv_temp * (p.grad_ent ? fmaf(ge, p.ent[row], g) : g);
+          c1 = p.inv_temp * ge * kLn2;
         }
       }
       OnlineStat st = stat_empty();
@@ -294,18 +326,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int rel = lab - col0;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float pr = ex2(fmaf(v[i], p.scale2, -lse2));
-              float d = -gs * pr;
+              const float t = fmaf(v[i], p.scale2, -lse2);
+              const float pr = ex2(t);
+              float d = -pr * fmaf(c1, t, c0);
               if (i == rel) d += gs;
               v[i] = d;
             }
-            if (row_ok) {
+            if (row_ok)
               store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);
-              uint16_t* dt = p.out_bf16_t + static_cast<int64_t>(col0) * p.ld_out_t + row;
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (i < nvalid) dt[static_cast<int64_t>(i) * p.ld_out_t] = to_bf16_bits(v[i]);
-            }
           } else if constexpr (E == (int)Epi::StoreBf16) {
             if (row_ok)
               store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);

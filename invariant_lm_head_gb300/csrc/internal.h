@@ -28,27 +28,31 @@ constexpr int64_t kBwdRowChunk = 8192;
 
 enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3 };
 
+// Operand layouts. K-major: the operand is stored [rows][K] (K contiguous);
+// MN-major: stored [K][rows] (rows contiguous). Both are read by TMA with
+// 128-byte swizzle and described to tcgen05.mma with the matching major bit.
 struct GemmParams {
-  int M, N, K;  // D[M, N] = A[M, K] * B[N, K]^T
+  int M, N, K;  // D[M, N] = sum_k A[m, k] * B[n, k]
+  int a_mn, b_mn;  // 1 = operand stored MN-major ([K][M] / [K][N])
   int n_m_tiles, n_n_tiles, tiles_per_unit, n_vunits, n_units, group_m;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
   float inv_temp;  // inv_temperature
   const int32_t* labels;
-  const float* grad;
-  const float* lse;
+  const float* grad;       // DLogits: upstream grad of logprob [M] (may be NULL = 0)
+  const float* grad_ent;   // DLogits: upstream grad of entropy [M] (NULL = none)
+  const float* lse;        // DLogits: natural-log lse [M]
+  const float* ent;        // DLogits: entropy [M] (read only with grad_ent)
   // FwdStats partials: planes [n_vunits][part_ld] for m, s, u; zl [M]
   float* part_m;
   float* part_s;
   float* part_u;
   float* part_zl;
   int64_t part_ld;
-  // DLogits: dl [M][ld_out] and dl^T [N][ld_out_t]; StoreBf16: D [M][ld_out]
+  // DLogits: dl [M][ld_out]; StoreBf16: D [M][ld_out]
   uint16_t* out_bf16;
   int64_t ld_out;
-  uint16_t* out_bf16_t;
-  int64_t ld_out_t;
   // StoreF32: D [M][ld_out_f32], D += old when accumulate != 0
   float* out_f32;
   int64_t ld_out_f32;
@@ -79,10 +83,6 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
                              const int32_t* labels, int64_t T, int n_vunits, int64_t V,
                              float* out_logprob, float* out_entropy, float* out_lse,
                              cudaStream_t stream);
-
-// out[c * ld_out + r] = in[r * ld_in + c] for r < rows, c < cols (bf16 bits).
-cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t ld_in,
-                                  uint16_t* out, int64_t ld_out, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, int* result,
                                  cudaStream_t stream);

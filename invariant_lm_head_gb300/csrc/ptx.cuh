@@ -167,12 +167,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B (both K-major) and
-// an fp32 accumulator: [4,6) D format 1 = f32, [7,10) A format 1 = bf16,
-// [10,13) B format 1 = bf16, bits 15/16 = 0 (K-major), [17,23) N >> 3,
-// [24,29) M >> 4.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+// Shared-memory matrix descriptor for an MN-major bf16 tile written by TMA as
+// 64(MN) x 64(K) boxes with 128-byte swizzle: each K row holds 64 MN-contiguous
+// elements (128 B), 8 K rows form a 1024 B atom. Leading offset = 8192 B from
+// one 64-element MN block (one box) to the next; stride offset = 1024 B from
+// one 8-row K group to the next.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B and an fp32
+// accumulator: [4,6) D format 1 = f32, [7,10) A format 1 = bf16, [10,13) B
+// format 1 = bf16, bit 15 / 16 = A / B MN-major, [17,23) N >> 3, [24,29) M >> 4.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false,
+                                                      bool b_mn = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- math

@@ -3,7 +3,6 @@
 //     row: fp32 scale by the temperature factor, online max / sum-exp /
 //     entropy accumulator, label gather),
 //   * the fixed-order merge of the fused forward's per-vocab-chunk partials,
-//   * a bf16 tile transpose used to lay out backward operands K-major,
 //   * a self-test of the bounded wait (a barrier that nothing completes).
 //
 // The sampler formula is the one of the verl pull request "batch-invariant
@@ -183,55 +182,6 @@ __global__ void fwd_merge_kernel(const float* __restrict__ pm, const float* __re
   write_row_outputs(row, st, ok ? pzl[row] : 0.f, ok, out_lp, out_ent, out_lse);
 }
 
-// 64 x 64 tile transpose of 16-bit values through shared memory. Rows and
-// columns are read and written two at a time as 32-bit words (the host keeps
-// both leading dimensions even and the bases 4-byte aligned).
-__global__ void __launch_bounds__(256)
-    transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows, int64_t cols,
-                          int64_t ld_in, uint16_t* __restrict__ out, int64_t ld_out) {
-  __shared__ uint16_t tile[64][66];
-  const int tx = threadIdx.x & 31;  // 2 columns each
-  const int ty = threadIdx.x >> 5;  // 8 rows per pass
-  const int64_t c0 = (int64_t)blockIdx.x * 64;
-  for (int64_t r0 = (int64_t)blockIdx.y * 64; r0 < rows; r0 += (int64_t)gridDim.y * 64) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int rr = ty + 8 * k;
-      const int64_t r = r0 + rr;
-      const int64_t c = c0 + 2 * tx;
-      uint16_t a = 0, b = 0;
-      if (r < rows) {
-        if (c + 1 < cols) {
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(in + r * ld_in + c);
-          a = static_cast<uint16_t>(w & 0xffffu);
-          b = static_cast<uint16_t>(w >> 16);
-        } else if (c < cols) {
-          a = in[r * ld_in + c];
-        }
-      }
-      tile[rr][2 * tx] = a;
-      tile[rr][2 * tx + 1] = b;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int cc = ty + 8 * k;
-      const int64_t c = c0 + cc;      // output row
-      const int64_t r = r0 + 2 * tx;  // output column
-      if (c < cols) {
-        if (r + 1 < rows) {
-          const uint32_t w = static_cast<uint32_t>(tile[2 * tx][cc]) |
-                             (static_cast<uint32_t>(tile[2 * tx + 1][cc]) << 16);
-          *reinterpret_cast<uint32_t*>(out + c * ld_out + r) = w;
-        } else if (r < rows) {
-          out[c * ld_out + r] = tile[2 * tx][cc];
-        }
-      }
-    }
-    __syncthreads();
-  }
-}
-
 // Waits on an mbarrier that nothing will complete; the bounded wait must give
 // up after limit_ns, record the timeout in *status and let the kernel return.
 __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_ns, int* result) {
@@ -277,17 +227,6 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
   const int64_t blocks = (T + threads - 1) / threads;
   fwd_merge_kernel<<<(unsigned)blocks, threads, 0, stream>>>(pm, ps, pu, pzl, labels, T, n_vunits,
                                                              V, out_lp, out_ent, out_lse);
-  const cudaError_t e = cudaGetLastError();
-  if (e == cudaSuccess) note_launch();
-  return e;
-}
-
-cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t ld_in,
-                                  uint16_t* out, int64_t ld_out, cudaStream_t stream) {
-  if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const int64_t gy = (rows + 63) / 64;
-  dim3 grid((unsigned)((cols + 63) / 64), (unsigned)(gy < 65535 ? gy : 65535));
-  transpose_bf16_kernel<<<grid, 256, 0, stream>>>(in, rows, cols, ld_in, out, ld_out);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

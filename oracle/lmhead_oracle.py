@@ -36,6 +36,10 @@ stored, each step written out as the pages define it):
 * Backward of ``sum_t g[t] * logprob[t]`` with respect to the projection:
   ``dz = g * (onehot - p)``, ``dlogit = s * dz``, ``grad_hidden = dlogit @
   weight``, ``grad_weight = dlogit^T @ hidden``.
+* Optional entropy term (the SkyRL page notes entropy under the fused head is
+  metric-only until its gradient is wired): for ``sum_t gH[t] * entropy[t]``,
+  ``dH/dz_j = -p_j * (log p_j + H) = -p_j * (z_j - lse + H)``, added to ``dz``
+  before the temperature factor.
 
 Pins (tests/test_oracle_pins.py): closed forms (uniform rows, two-value rows,
 one-hot-dominant rows), invariants (sum of probabilities, sign, entropy
@@ -57,6 +61,7 @@ __all__ = [
     "fused_forward",
     "logprob_from_logits",
     "dlogits",
+    "dlogits_entropy",
     "fused_backward",
     "fused_forward_rows",
     "fused_grad_hidden_rows",
@@ -138,12 +143,31 @@ def dlogits(z, labels, grad, inv_temperature: float, lse=None) -> np.ndarray:
     return fp32_scalar(inv_temperature) * dz
 
 
-def fused_backward(hidden, weight, labels, grad, inv_temperature: float):
-    """(grad_hidden [T, H], grad_weight [V, H]) in float64."""
+def dlogits_entropy(z, grad_entropy, inv_temperature: float) -> np.ndarray:
+    """Gradient of sum_t gH[t] * entropy[t] with respect to the unscaled logits.
+
+    d entropy / d z_j = -p_j * (z_j - lse + entropy); times s (z = s * logits).
+    """
+    z = _f64(z)
+    gh = _f64(grad_entropy)
+    lse, ent = row_lse_entropy(z)
+    p = np.exp(z - lse[:, None])
+    dz = -gh[:, None] * p * (z - lse[:, None] + ent[:, None])
+    return fp32_scalar(inv_temperature) * dz
+
+
+def fused_backward(hidden, weight, labels, grad, inv_temperature: float, grad_entropy=None):
+    """(grad_hidden [T, H], grad_weight [V, H]) in float64.
+
+    Differentiates sum_t grad[t] * logprob[t] (+ sum_t grad_entropy[t] * entropy[t]
+    when grad_entropy is given).
+    """
     h = _f64(hidden)
     w = _f64(weight)
     z = scaled_logits(h, w, inv_temperature)
     dl = dlogits(z, labels, grad, inv_temperature)
+    if grad_entropy is not None:
+        dl = dl + dlogits_entropy(z, grad_entropy, inv_temperature)
     return dl @ w, dl.T @ h
 
 
@@ -170,7 +194,8 @@ def fused_forward_rows(hidden, weight, labels, inv_temperature: float, rows):
     return tuple(np.concatenate(x) if x else np.zeros(0) for x in out)
 
 
-def fused_grad_hidden_rows(hidden, weight, labels, grad, inv_temperature: float, rows):
+def fused_grad_hidden_rows(hidden, weight, labels, grad, inv_temperature: float, rows,
+                           grad_entropy=None):
     """grad_hidden for the listed rows only, [len(rows), H]."""
     w = _f64(weight)
     labels = np.asarray(labels, dtype=np.int64)
@@ -178,12 +203,15 @@ def fused_grad_hidden_rows(hidden, weight, labels, grad, inv_temperature: float,
     out = []
     for r in _row_blocks(rows):
         z = fp32_scalar(inv_temperature) * (_f64(hidden[r]) @ w.T)
-        out.append(dlogits(z, labels[r], g[r], inv_temperature) @ w)
+        dl = dlogits(z, labels[r], g[r], inv_temperature)
+        if grad_entropy is not None:
+            dl = dl + dlogits_entropy(z, _f64(grad_entropy)[r], inv_temperature)
+        out.append(dl @ w)
     return np.concatenate(out) if out else np.zeros((0, w.shape[1]))
 
 
 def grad_weight_from_rows(hidden, weight, labels, grad, inv_temperature: float, rows,
-                          vocab_rows=None):
+                          vocab_rows=None, grad_entropy=None):
     """sum over the listed rows t of dlogit[t, :]^T hidden[t, :], [V, H].
 
     Equals the full grad_weight when grad[t] = 0 for every row not listed.
@@ -199,6 +227,8 @@ def grad_weight_from_rows(hidden, weight, labels, grad, inv_temperature: float, 
         h = _f64(hidden[r])
         z = fp32_scalar(inv_temperature) * (h @ w.T)
         dl = dlogits(z, labels[r], g[r], inv_temperature)
+        if grad_entropy is not None:
+            dl = dl + dlogits_entropy(z, _f64(grad_entropy)[r], inv_temperature)
         if vocab_rows is not None:
             dl = dl[:, np.asarray(vocab_rows, dtype=np.int64)]
         acc += dl.T @ h

@@ -43,8 +43,12 @@ def forward(hidden, weight, labels, inv_temperature):
     return lp_out, ent_out, lse_out
 
 
-def backward(hidden, weight, labels, grad, inv_temperature):
-    """Nested lists (grad_hidden [T][H], grad_weight [V][H]) from explicit loops."""
+def backward(hidden, weight, labels, grad, inv_temperature, grad_entropy=None):
+    """Nested lists (grad_hidden [T][H], grad_weight [V][H]) from explicit loops.
+
+    With grad_entropy, d(gH * entropy)/dz_v = -gH * p_v * (z_v - lse + entropy)
+    is added to each row's logit gradient.
+    """
     s = _s(inv_temperature)
     T, H = len(hidden), len(hidden[0])
     V = len(weight)
@@ -55,11 +59,14 @@ def backward(hidden, weight, labels, grad, inv_temperature):
         m = max(z)
         lse = m + math.log(math.fsum(math.exp(zv - m) for zv in z))
         g = float(grad[t])
+        ge = 0.0 if grad_entropy is None else float(grad_entropy[t])
+        ent = -math.fsum(math.exp(zv - lse) * (zv - lse) for zv in z)
         lab = int(labels[t])
         row = []
         for v in range(V):
             onehot = 1.0 if v == lab else 0.0
-            row.append(s * g * (onehot - math.exp(z[v] - lse)))
+            p = math.exp(z[v] - lse)
+            row.append(s * (g * (onehot - p) - ge * p * (z[v] - lse + ent)))
         dl.append(row)
     gh = [[math.fsum(dl[t][v] * float(weight[v][h]) for v in range(V)) for h in range(H)]
           for t in range(T)]

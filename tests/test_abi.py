@@ -52,11 +52,12 @@ def test_workspace_sizes(lib):
     fwd = f(lmh.LMH_OP_FWD, 16384, 3584, 152064)
     assert fwd >= (3 * n_chunks + 1) * 16384 * 4
     assert fwd < (3 * n_chunks + 1) * 16384 * 4 + 8 * 256
-    # backward grows with min(T, 8192) beyond the forward partials
+    # backward: forward partials + lse, logprob, entropy per row + bf16 dlogits [min(T,8192), V]
     b1 = f(lmh.LMH_OP_BWD, 8192, 3584, 152064)
     b2 = f(lmh.LMH_OP_BWD, 16384, 3584, 152064)
-    extra = (3 * n_chunks + 3) * 8192 * 4
+    extra = (3 * n_chunks + 4) * 8192 * 4
     assert 0 <= (b2 - b1) - extra < 64 * 256
+    assert b1 > 8192 * 152064 * 2
     assert f(lmh.LMH_OP_FWD, 0, 256, 4096) > 0
     for bad in [(lmh.LMH_OP_FWD, -1, 256, 4096), (lmh.LMH_OP_FWD, 4, 12, 4096),
                 (lmh.LMH_OP_FWD, 4, 256, 0), (7, 4, 256, 4096)]:
@@ -96,6 +97,10 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     rc = lib.lmhead_logprob_bwd(16, 16, 16, None, None, 4, 256, 4096, 1.0, 16, 16, 256, 1 << 30,
                                 None)
     assert rc == lmh.LMH_ERR_INVALID_ARG
+    rc = lib.lmhead_logprob_entropy_bwd(16, 16, 16, None, None, None, None, 4, 256, 4096, 1.0, 16,
+                                        16, 256, 1 << 30, None)
+    assert rc == lmh.LMH_ERR_INVALID_ARG  # both upstream grads missing
+    assert lib.lmhead_engine_gemm(16, 16, 8, 8, 8, 4, 16, None) == lmh.LMH_ERR_INVALID_ARG
     assert lib.lmhead_selftest_wait_timeout(10, None) == lmh.LMH_ERR_INVALID_ARG
 
 

@@ -113,6 +113,21 @@ def test_grad_hidden_rows_invariant_across_batches(lmh):
     torch.cuda.synchronize()
 
 
+def test_entropy_grad_hidden_rows_invariant_across_batches(lmh):
+    import torch
+
+    T, H, V = 300, 136, 3000
+    hidden, weight, labels, grad = fused_case(73, T, H, V)
+    gent = W.random_f32(74, T)
+    h, w, lab, g, ge = (to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad),
+                        to_dev(gent))
+    full, _ = lmh.lmhead_logprob_entropy_bwd(h, w, lab, g, ge, S07)
+    for r0, r1 in [(0, 1), (1, 8), (8, 264), (17, 300)]:
+        part, _ = lmh.lmhead_logprob_entropy_bwd(h[r0:r1], w, lab[r0:r1], g[r0:r1], ge[r0:r1], S07)
+        assert torch.equal(part, full[r0:r1]), (r0, r1)
+    torch.cuda.synchronize()
+
+
 def test_grad_hidden_rows_invariant_across_row_chunk_boundary(lmh):
     import torch
 

@@ -39,13 +39,18 @@ def _fwd(lmh, hidden, weight, labels, s):
 
 
 # ----------------------------------------------------------------- engine
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 520, 200), (7, 8, 4096), (1000, 264, 72)])
-def test_engine_gemm_matches_fp64(lmh, M, N, K):
+@pytest.mark.parametrize("layout", [0, 1, 2, 3])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (304, 520, 200), (8, 8, 4096), (1000, 264, 72)])
+def test_engine_gemm_matches_fp64(lmh, M, N, K, layout):
+    """D = A B^T with A [M,K] or [K,M] (bit 0) and B [N,K] or [K,N] (bit 1)."""
     import torch
 
     a = W.random_bf16(11, (M, K))
     b = W.random_bf16(12, (N, K))
-    d = lmh.lmhead_engine_gemm(to_dev_bf16(a), to_dev_bf16(b))
+    a_k, b_k = not (layout & 1), not (layout & 2)
+    A = to_dev_bf16(a if a_k else np.ascontiguousarray(a.T))
+    B = to_dev_bf16(b if b_k else np.ascontiguousarray(b.T))
+    d = lmh.lmhead_engine_gemm(A, B, a_kmajor=a_k, b_kmajor=b_k)
     torch.cuda.synchronize()
     lmh.lmhead_device_status()
     ref = f64(a) @ f64(b).T
@@ -177,6 +182,43 @@ def test_fused_backward_all_out_of_vocab(lmh):
     assert rel_frob(gw, rgw) < RTOL_FROB_GRAD
 
 
+@pytest.mark.parametrize("s", [1.0, S07])
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (3, 8, 16), (8192 + 40, 72, 700)])
+def test_entropy_backward_matches_oracle(lmh, T, H, V, s):
+    import torch
+
+    hidden, weight, labels, grad = fused_case(33, T, H, V, w_std=0.2, oov=[(1, -100)])
+    gent = W.random_f32(34, T)
+    h, w, lab = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels)
+    g, ge = to_dev(grad), to_dev(gent)
+    lp, ent, lse = lmh.lmhead_logprob_fwd(h, w, lab, s, want_lse=True)
+    gh, gw = lmh.lmhead_logprob_entropy_bwd(h, w, lab, g, ge, s, lse=lse, entropy=ent)
+    gh2, gw2 = lmh.lmhead_logprob_entropy_bwd(h, w, lab, g, ge, s)  # statistics recomputed
+    gh3, gw3 = lmh.lmhead_logprob_entropy_bwd(h, w, lab, None, ge, s)  # entropy term alone
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    assert torch.equal(gh, gh2) and torch.equal(gw, gw2)
+    h64, w64 = f64(hidden), f64(weight)
+    rgh, rgw = oracle.fused_backward(h64, w64, labels, grad, s, grad_entropy=gent)
+    assert rel_frob(gh.float().cpu().numpy(), rgh) < RTOL_FROB_GRAD
+    assert rel_frob(gw.cpu().numpy(), rgw) < RTOL_FROB_GRAD
+    rgh3, rgw3 = oracle.fused_backward(h64, w64, labels, np.zeros(T), s, grad_entropy=gent)
+    assert rel_frob(gh3.float().cpu().numpy(), rgh3) < RTOL_FROB_GRAD
+    assert rel_frob(gw3.cpu().numpy(), rgw3) < RTOL_FROB_GRAD
+
+
+def test_entropy_backward_without_entropy_grad_equals_plain_backward(lmh):
+    import torch
+
+    T, H, V = 200, 128, 3000
+    hidden, weight, labels, grad = fused_case(35, T, H, V)
+    h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
+    a = lmh.lmhead_logprob_bwd(h, w, lab, g, S07)
+    b = lmh.lmhead_logprob_entropy_bwd(h, w, lab, g, None, S07)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 def test_backward_deterministic_run_to_run(lmh):
     import torch
 
@@ -232,4 +274,4 @@ def test_bounded_wait_selftest_reports_timeout(lmh):
     assert e.value.code == lmh.LMH_ERR_DEVICE_TIMEOUT
     assert lmh.lmhead_device_status() == 0  # cleared by the read
     # the context is still usable
-    test_engine_gemm_matches_fp64(lmh, 128, 256, 64)
+    test_engine_gemm_matches_fp64(lmh, 128, 256, 64, 3)

@@ -121,6 +121,34 @@ def check_finite_differences(fwd, bwd, seed, s, oov_row=None, eps=1e-6):
     return worst
 
 
+def _fd_objective_entropy(h, w, lab, g, gh, s, fwd):
+    """The log-prob objective plus sum_t gH[t] * entropy[t]."""
+    _, ent, _ = fwd(h, w, lab, s)
+    return _fd_objective(h, w, lab, g, s, fwd) + float(np.sum(gh * ent))
+
+
+def check_finite_differences_entropy(fwd, bwd, seed, s, oov_row=None, eps=1e-6):
+    h, w, lab, g = _tiny(seed, oov_row=oov_row)
+    h = h.astype(np.float64)
+    w = w.astype(np.float64)
+    g = g.astype(np.float64)
+    gh = np.random.default_rng(seed + 100).standard_normal(len(g))
+    dh, dw = bwd(h, w, lab, g, s, gh)
+    worst = 0.0
+    for arr, grad in ((h, dh), (w, dw)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            old = arr[idx]
+            arr[idx] = old + eps
+            fp = _fd_objective_entropy(h, w, lab, g, gh, s, fwd)
+            arr[idx] = old - eps
+            fm = _fd_objective_entropy(h, w, lab, g, gh, s, fwd)
+            arr[idx] = old
+            num[idx] = (fp - fm) / (2 * eps)
+        worst = max(worst, float(np.max(np.abs(num - grad)) / (np.max(np.abs(num)) + 1e-300)))
+    return worst
+
+
 def check_torch_autograd(bwd, seed, s):
     h, w, lab, g = _tiny(seed, T=5, H=16, V=24)
     th = torch.from_numpy(h.astype(np.float64)).requires_grad_(True)
@@ -220,6 +248,37 @@ def test_finite_differences_out_of_vocab(s):
 @pytest.mark.parametrize("s", [1.0, S07])
 def test_torch_autograd_of_sampler_formula(s):
     assert check_torch_autograd(oracle.fused_backward, 13, s) < 1e-12
+
+
+@pytest.mark.parametrize("s", [1.0, S07])
+def test_entropy_gradient_finite_differences(s):
+    bwd = lambda h, w, lab, g, s_, gh: oracle.fused_backward(h, w, lab, g, s_, grad_entropy=gh)
+    assert check_finite_differences_entropy(oracle.fused_forward, bwd, 14, s, oov_row=1) < 1e-6
+
+
+def test_entropy_gradient_torch_autograd_and_loops():
+    h, w, lab, g = _tiny(15, T=5, H=16, V=24)
+    gh = np.random.default_rng(3).standard_normal(5)
+    th = torch.from_numpy(h.astype(np.float64)).requires_grad_(True)
+    tw = torch.from_numpy(w.astype(np.float64)).requires_grad_(True)
+    z = S07 * (th @ tw.T)
+    logp = torch.log_softmax(z, dim=-1)
+    ent = -(logp.exp() * logp).sum(-1)
+    lp = logp.gather(-1, torch.from_numpy(lab.astype(np.int64)).unsqueeze(-1)).squeeze(-1)
+    (lp * torch.from_numpy(g.astype(np.float64)) + ent * torch.from_numpy(gh)).sum().backward()
+    dh, dw = oracle.fused_backward(h, w, lab, g, S07, grad_entropy=gh)
+    assert np.max(np.abs(dh - th.grad.numpy())) < 1e-12
+    assert np.max(np.abs(dw - tw.grad.numpy())) < 1e-12
+    rdh, rdw = loops.backward(h.tolist(), w.tolist(), lab.tolist(), g.tolist(), S07, gh.tolist())
+    assert np.max(np.abs(dh - np.array(rdh))) < 1e-12
+    assert np.max(np.abs(dw - np.array(rdw))) < 1e-12
+
+
+def test_entropy_gradient_row_sums_vanish():
+    h, w, lab, _ = _tiny(16, T=4, H=8, V=32)
+    z = oracle.scaled_logits(h, w, S07)
+    d = oracle.dlogits_entropy(z, np.array([1.0, -2.0, 0.5, 3.0]), S07)
+    assert np.all(np.abs(d.sum(axis=1)) < 1e-12)  # sum_j p_j (z_j - lse + H) = 0
 
 
 def test_dlogit_row_sums():
@@ -338,6 +397,21 @@ def _forward_transposed_index(h, w, lab, s):
     return lp, ent, lse
 
 
+def _backward_entropy_sign_flip(h, w, lab, g, s, gh):
+    z = oracle.scaled_logits(h, w, s)
+    dl = oracle.dlogits(z, lab, g, s) - oracle.dlogits_entropy(z, gh, s)
+    return dl @ np.asarray(w, np.float64), dl.T @ np.asarray(h, np.float64)
+
+
+def _backward_entropy_missing_h(h, w, lab, g, s, gh):
+    z = oracle.scaled_logits(h, w, s)
+    lse, _ = oracle.row_lse_entropy(z)
+    p = np.exp(z - lse[:, None])
+    dz = -np.asarray(gh)[:, None] * p * (z - lse[:, None])  # dropped "+ H"
+    dl = oracle.dlogits(z, lab, g, s) + oracle.fp32_scalar(s) * dz
+    return dl @ np.asarray(w, np.float64), dl.T @ np.asarray(h, np.float64)
+
+
 def test_planted_mistakes_are_caught():
     assert check_scipy_lse_entropy(_sampler_entropy_missing_lse, 0) > 1e-3
     assert check_two_value(_sampler_entropy_missing_lse, 4096, 7, 5.5, 0.25) > 1e-3
@@ -348,3 +422,7 @@ def test_planted_mistakes_are_caught():
     assert check_finite_differences(oracle.fused_forward, _backward_missing_temperature, 11, S07) > 1e-3
     assert check_finite_differences(oracle.fused_forward, _backward_oov_zeroed, 12, 1.0, oov_row=0) > 1e-3
     assert check_loops_forward(_forward_transposed_index, 0, 1.0) > 1e-3
+    assert check_finite_differences_entropy(oracle.fused_forward, _backward_entropy_sign_flip, 14,
+                                            1.0) > 1e-3
+    assert check_finite_differences_entropy(oracle.fused_forward, _backward_entropy_missing_h, 14,
+                                            S07) > 1e-3
