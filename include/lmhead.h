@@ -68,7 +68,7 @@ struct CUstream_st; /* cudaStream_t */
 
 /*
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
- * Returns SIZE_MAX for invalid arguments. The forward needs 12 bytes per row
+ * Returns SIZE_MAX for invalid arguments. The forward needs 16 bytes per row
  * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
  * row and a bf16 dlogits buffer of min(T, 8192) x V.
  */
@@ -93,6 +93,20 @@ int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int
                        int64_t T, int64_t H, int64_t V, float inv_temperature,
                        float* out_logprob, float* out_entropy, float* out_lse, void* workspace,
                        size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * lmhead_logprob_fwd plus sum_pi_squared: out_sum_p2[t] = sum_v p[t, v]^2 of
+ * the same distribution (verl page, the review note that lists entropy and
+ * sum_pi_squared as the per-token statistics still taken from the logits).
+ * Same pass, one more accumulator; out_sum_p2 f32 [T] or NULL. Same
+ * workspace as lmhead_logprob_fwd. logprob, entropy and lse are bit-identical
+ * to those of lmhead_logprob_fwd.
+ */
+int lmhead_logprob_fwd_stats(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                             int64_t T, int64_t H, int64_t V, float inv_temperature,
+                             float* out_logprob, float* out_entropy, float* out_lse,
+                             float* out_sum_p2, void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream);
 
 /*
  * Fused backward of sum_t grad_logprob[t] * logprob[t] (SkyRL page: logits
@@ -144,6 +158,15 @@ int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
 int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
                         float inv_temperature, float* out_logprob, float* out_entropy,
                         float* out_lse, struct CUstream_st* stream);
+
+/*
+ * logprob_from_logits plus sum_pi_squared (out_sum_p2 f32 [T] or NULL), in the
+ * same single pass over the logits; the other outputs are bit-identical to
+ * those of logprob_from_logits.
+ */
+int logprob_from_logits_stats(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                              float inv_temperature, float* out_logprob, float* out_entropy,
+                              float* out_lse, float* out_sum_p2, struct CUstream_st* stream);
 
 /*
  * Forward without a workspace, for callers that cannot allocate device memory

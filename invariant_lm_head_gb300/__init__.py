@@ -49,6 +49,9 @@ SIGNATURES = {
     "lmhead_logprob_bwd": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, ctypes.c_size_t,
                             _P], ctypes.c_int),
     "logprob_from_logits": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P], ctypes.c_int),
+    "lmhead_logprob_fwd_stats": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P,
+                                  ctypes.c_size_t, _P], ctypes.c_int),
+    "logprob_from_logits_stats": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P, _P], ctypes.c_int),
     "lmhead_last_error_string": ([], ctypes.c_char_p),
     "lmhead_abi_version": ([], ctypes.c_int),
     "lmhead_kernel_launches": ([], ctypes.c_ulonglong),
@@ -145,6 +148,21 @@ def lmhead_logprob_fwd(hidden, weight, labels, inv_temperature: float = 1.0, *, 
                        out_entropy=None, out_lse=None, want_entropy: bool = True,
                        want_lse: bool = False, workspace=None, stream=None):
     """Fused LM-head forward. Returns (logprob, entropy or None, lse or None), f32 [T]."""
+    return _fwd("lmhead_logprob_fwd", hidden, weight, labels, inv_temperature, out_logprob,
+                out_entropy, out_lse, None, want_entropy, want_lse, False, workspace, stream)[:3]
+
+
+def lmhead_logprob_fwd_stats(hidden, weight, labels, inv_temperature: float = 1.0, *,
+                             out_logprob=None, out_entropy=None, out_lse=None, out_sum_p2=None,
+                             want_entropy: bool = True, want_lse: bool = False, workspace=None,
+                             stream=None):
+    """Fused forward with sum_pi_squared. Returns (logprob, entropy, lse, sum_p2)."""
+    return _fwd("lmhead_logprob_fwd_stats", hidden, weight, labels, inv_temperature, out_logprob,
+                out_entropy, out_lse, out_sum_p2, want_entropy, want_lse, True, workspace, stream)
+
+
+def _fwd(name, hidden, weight, labels, inv_temperature, out_logprob, out_entropy, out_lse,
+         out_sum_p2, want_entropy, want_lse, want_sum_p2, workspace, stream):
     torch = _torch()
     dev = hidden.device
     _need(hidden, "hidden", torch.bfloat16, dev, 2)
@@ -160,12 +178,17 @@ def lmhead_logprob_fwd(hidden, weight, labels, inv_temperature: float = 1.0, *, 
         out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
     if out_lse is None and want_lse:
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_sum_p2 is None and want_sum_p2:
+        out_sum_p2 = torch.empty(T, dtype=torch.float32, device=dev)
     ws, ws_bytes = _workspace(LMH_OP_FWD, T, H, V, workspace, dev)
-    rc = library().lmhead_logprob_fwd(_ptr(hidden), _ptr(weight), _ptr(labels), T, H, V,
-                                      float(inv_temperature), _ptr(out_logprob), _ptr(out_entropy),
-                                      _ptr(out_lse), _ptr(ws), ws_bytes, _stream_ptr(stream))
-    _check("lmhead_logprob_fwd", rc)
-    return out_logprob, out_entropy, out_lse
+    lib = library()
+    args = [_ptr(hidden), _ptr(weight), _ptr(labels), T, H, V, float(inv_temperature),
+            _ptr(out_logprob), _ptr(out_entropy), _ptr(out_lse)]
+    if name == "lmhead_logprob_fwd_stats":
+        args.append(_ptr(out_sum_p2))
+    rc = getattr(lib, name)(*args, _ptr(ws), ws_bytes, _stream_ptr(stream))
+    _check(name, rc)
+    return out_logprob, out_entropy, out_lse, out_sum_p2
 
 
 def lmhead_logprob_bwd(hidden, weight, labels, grad_logprob, inv_temperature: float = 1.0, *,
@@ -225,6 +248,20 @@ def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_log
                         out_entropy=None, out_lse=None, want_entropy: bool = True,
                         want_lse: bool = False, stream=None):
     """Sampler formula on bf16 logits [T, V]. Returns (logprob, entropy or None, lse or None)."""
+    return _logits("logprob_from_logits", logits, labels, inv_temperature, out_logprob,
+                   out_entropy, out_lse, None, want_entropy, want_lse, False, stream)[:3]
+
+
+def logprob_from_logits_stats(logits, labels, inv_temperature: float = 1.0, *, out_logprob=None,
+                              out_entropy=None, out_lse=None, out_sum_p2=None,
+                              want_entropy: bool = True, want_lse: bool = False, stream=None):
+    """Sampler formula with sum_pi_squared. Returns (logprob, entropy, lse, sum_p2)."""
+    return _logits("logprob_from_logits_stats", logits, labels, inv_temperature, out_logprob,
+                   out_entropy, out_lse, out_sum_p2, want_entropy, want_lse, True, stream)
+
+
+def _logits(name, logits, labels, inv_temperature, out_logprob, out_entropy, out_lse, out_sum_p2,
+            want_entropy, want_lse, want_sum_p2, stream):
     torch = _torch()
     dev = logits.device
     _need(logits, "logits", torch.bfloat16, dev, 2)
@@ -236,11 +273,15 @@ def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_log
         out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
     if out_lse is None and want_lse:
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
-    rc = library().logprob_from_logits(_ptr(logits), _ptr(labels), T, V, float(inv_temperature),
-                                       _ptr(out_logprob), _ptr(out_entropy), _ptr(out_lse),
-                                       _stream_ptr(stream))
-    _check("logprob_from_logits", rc)
-    return out_logprob, out_entropy, out_lse
+    if out_sum_p2 is None and want_sum_p2:
+        out_sum_p2 = torch.empty(T, dtype=torch.float32, device=dev)
+    args = [_ptr(logits), _ptr(labels), T, V, float(inv_temperature), _ptr(out_logprob),
+            _ptr(out_entropy), _ptr(out_lse)]
+    if name == "logprob_from_logits_stats":
+        args.append(_ptr(out_sum_p2))
+    rc = getattr(library(), name)(*args, _stream_ptr(stream))
+    _check(name, rc)
+    return out_logprob, out_entropy, out_lse, out_sum_p2
 
 
 def lmhead_kernel_launches() -> int:

@@ -134,7 +134,7 @@ int n_fwd_chunks(int64_t V) {
 }
 
 struct FwdWs {
-  float *pm, *ps, *pu, *pzl;
+  float *pm, *ps, *pu, *pq, *pzl;
 };
 
 FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
@@ -143,6 +143,7 @@ FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
   w.pm = c.take<float>(n);
   w.ps = c.take<float>(n);
   w.pu = c.take<float>(n);
+  w.pq = c.take<float>(n);
   w.pzl = c.take<float>(T);
   return w;
 }
@@ -270,13 +271,15 @@ struct KernelTimer {
     if (_rc != LMH_OK) return _rc;                        \
   } while (0)
 
-// Forward statistics into `w`, merged into the outputs.
+// Forward statistics into `w`, merged into the outputs. out_sum_p2 may be NULL.
 int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* weight,
                 const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
-                float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st) {
+                float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st,
+                float* out_sum_p2 = nullptr) {
+  const int cm = lmh::gemm_cluster_m(static_cast<int>(T));
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
-  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::gemm_b_box_rows(cm, false)));
   lmh::GemmParams p{};
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
@@ -288,16 +291,68 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_m = w.pm;
   p.part_s = w.ps;
   p.part_u = w.pu;
+  p.part_q = out_sum_p2 ? w.pq : nullptr;
   p.part_zl = w.pzl;
   p.part_ld = T;
   LMH_LAUNCH(K_FWD_GEMM, st,
-             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
+             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st,
+                              cm),
              "fused forward");
   LMH_LAUNCH(K_FWD_MERGE, st,
-             lmh::launch_fwd_merge(w.pm, w.ps, w.pu, w.pzl, labels, T, n_fwd_chunks(V), V, out_lp,
-                                   out_ent, out_lse, st),
+             lmh::launch_fwd_merge(w.pm, w.ps, w.pu, out_sum_p2 ? w.pq : nullptr, w.pzl, labels, T,
+                                   n_fwd_chunks(V), V, out_lp, out_ent, out_lse, out_sum_p2, st),
              "forward merge");
   return LMH_OK;
+}
+
+int fwd_entry(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels, int64_t T,
+              int64_t H, int64_t V, float inv_temperature, float* out_logprob, float* out_entropy,
+              float* out_lse, float* out_sum_p2, void* workspace, size_t workspace_bytes,
+              struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(inv_temperature));
+  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  LMH_TRY(check_ptr(out_sum_p2, 4, "out_sum_p2", true));
+  const size_t need = lmhead_workspace_size(LMH_OP_FWD, T, H, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  LMH_TRY(check_ptr(workspace, 16, "workspace"));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  Carver c{static_cast<char*>(workspace)};
+  const FwdWs w = carve_fwd(c, T, V);
+  LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, out_logprob,
+                      out_entropy, out_lse, w, reinterpret_cast<cudaStream_t>(stream),
+                      out_sum_p2));
+  return ok();
+}
+
+int logits_entry(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                 float inv_temperature, float* out_logprob, float* out_entropy, float* out_lse,
+                 float* out_sum_p2, struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, 8, V, false));
+  LMH_TRY(check_temperature(inv_temperature));
+  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
+  LMH_TRY(check_ptr(logits, (V % 8 == 0) ? 16 : 2, "logits"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  LMH_TRY(check_ptr(out_sum_p2, 4, "out_sum_p2", true));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_LAUNCH(K_LOGITS_ROWWISE, st,
+             lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob,
+                                        out_entropy, out_lse, out_sum_p2, dev->sms, st),
+             "logits log-prob");
+  return ok();
 }
 
 // Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
@@ -345,14 +400,17 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     lse = w.lse;
     ent = w.ent;
   }
-  CUtensorMap t_w, t_w_mn;
-  LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));   // [V][H], K = H
-  LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));      // [K=V][N=H]
+  CUtensorMap t_w_mn;
+  LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));  // [K=V][N=H]
+  const int cm_w = lmh::gemm_cluster_m(static_cast<int>(V));
 
   for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
-    CUtensorMap t_h, t_h_mn, t_dl, t_dl_mn;
+    const int cm_r = lmh::gemm_cluster_m(static_cast<int>(rows));
+    CUtensorMap t_w, t_h, t_h_mn, t_dl, t_dl_mn;
+    LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK,
+                      lmh::gemm_b_box_rows(cm_r, false)));                     // [V][K=H]
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
     LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][N=H]
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
@@ -372,7 +430,8 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     p.ent = grad_ent ? ent + c0 : nullptr;
     p.out_bf16 = w.dl;
     p.ld_out = w.vpad;
-    LMH_LAUNCH(K_DLOGITS_GEMM, st, lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st),
+    LMH_LAUNCH(K_DLOGITS_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, cm_r),
                "dlogits");
 
     lmh::GemmParams q{};
@@ -384,7 +443,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     q.out_bf16 = grad_hidden + c0 * H;
     q.ld_out = H;
     LMH_LAUNCH(K_DHIDDEN_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st),
+               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, cm_r),
                "grad_hidden");
 
     lmh::GemmParams r{};
@@ -398,7 +457,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     r.ld_out_f32 = H;
     r.accumulate = c0 > 0 ? 1 : 0;
     LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st),
+               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, cm_w),
                "grad_weight");
   }
   return ok();
@@ -498,26 +557,17 @@ int lmhead_logprob_fwd(const uint16_t* hidden, const uint16_t* weight, const int
                        int64_t T, int64_t H, int64_t V, float inv_temperature,
                        float* out_logprob, float* out_entropy, float* out_lse, void* workspace,
                        size_t workspace_bytes, struct CUstream_st* stream) {
-  LMH_TRY(check_dims(T, H, V, true));
-  LMH_TRY(check_temperature(inv_temperature));
-  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
-  LMH_TRY(check_ptr(hidden, 16, "hidden"));
-  LMH_TRY(check_ptr(weight, 16, "weight"));
-  LMH_TRY(check_ptr(labels, 4, "labels"));
-  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
-  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
-  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
-  const size_t need = lmhead_workspace_size(LMH_OP_FWD, T, H, V);
-  if (!workspace || workspace_bytes < need)
-    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
-  LMH_TRY(check_ptr(workspace, 16, "workspace"));
-  DeviceInfo* dev = nullptr;
-  LMH_TRY(device_info(&dev));
-  Carver c{static_cast<char*>(workspace)};
-  const FwdWs w = carve_fwd(c, T, V);
-  LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, out_logprob,
-                      out_entropy, out_lse, w, reinterpret_cast<cudaStream_t>(stream)));
-  return ok();
+  return fwd_entry(hidden, weight, labels, T, H, V, inv_temperature, out_logprob, out_entropy,
+                   out_lse, nullptr, workspace, workspace_bytes, stream);
+}
+
+int lmhead_logprob_fwd_stats(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
+                             int64_t T, int64_t H, int64_t V, float inv_temperature,
+                             float* out_logprob, float* out_entropy, float* out_lse,
+                             float* out_sum_p2, void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream) {
+  return fwd_entry(hidden, weight, labels, T, H, V, inv_temperature, out_logprob, out_entropy,
+                   out_lse, out_sum_p2, workspace, workspace_bytes, stream);
 }
 
 int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
@@ -545,22 +595,15 @@ int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
 int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
                         float inv_temperature, float* out_logprob, float* out_entropy,
                         float* out_lse, struct CUstream_st* stream) {
-  LMH_TRY(check_dims(T, 8, V, false));
-  LMH_TRY(check_temperature(inv_temperature));
-  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
-  LMH_TRY(check_ptr(logits, (V % 8 == 0) ? 16 : 2, "logits"));
-  LMH_TRY(check_ptr(labels, 4, "labels"));
-  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
-  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
-  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
-  DeviceInfo* dev = nullptr;
-  LMH_TRY(device_info(&dev));
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_LOGITS_ROWWISE, st,
-             lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob,
-                                        out_entropy, out_lse, dev->sms, st),
-             "logits log-prob");
-  return ok();
+  return logits_entry(logits, labels, T, V, inv_temperature, out_logprob, out_entropy, out_lse,
+                      nullptr, stream);
+}
+
+int logprob_from_logits_stats(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                              float inv_temperature, float* out_logprob, float* out_entropy,
+                              float* out_lse, float* out_sum_p2, struct CUstream_st* stream) {
+  return logits_entry(logits, labels, T, V, inv_temperature, out_logprob, out_entropy, out_lse,
+                      out_sum_p2, stream);
 }
 
 int lmhead_device_status(struct CUstream_st* stream, unsigned* bits) {
@@ -613,6 +656,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (M == 0) return ok();
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
+  const int cm = lmh::gemm_cluster_m(static_cast<int>(M));
   CUtensorMap ta, tb;
   if (a_mn)
     LMH_TRY(make_tmap(&ta, A, M, K, M * 2, 64, lmh::kBK));
@@ -621,7 +665,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (b_mn)
     LMH_TRY(make_tmap(&tb, B, N, K, N * 2, 64, lmh::kBK));
   else
-    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
+    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::gemm_b_box_rows(cm, false)));
   lmh::GemmParams p{};
   p.status = dev->status;
   p.M = static_cast<int>(M);
@@ -633,7 +677,8 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   p.ld_out_f32 = N;
   p.accumulate = 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_ENGINE_GEMM, st, lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st),
+  LMH_LAUNCH(K_ENGINE_GEMM, st,
+             lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, cm),
              "engine gemm");
   return ok();
 }

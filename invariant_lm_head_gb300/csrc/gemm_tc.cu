@@ -16,12 +16,18 @@
 //   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
+// With a cluster of CM CTAs along M (CM = 2 for large M), the CTAs take
+// consecutive 128-row tiles of one 128*CM-row block and the same N tiles; each
+// loads 1/CM of the shared B tile and multicasts it to all of them, and each
+// MMA warp multicasts its stage-release commit, so a stage is refilled only
+// when every CTA of the cluster has consumed it. Per-SM operand traffic drops
+// from 48 KB to 16 + 32/CM KB per 64-deep stage.
 //
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
 //              fused LM-head log-prob" (vocab projection folded into an online
 //              softmax over vocab tiles): per row and per 1024-column vocab
-//              chunk, the base-2 online statistics (m, s, u) and the label
+//              chunk, the base-2 online statistics (m, s, u, q) and the label
 //              logit; no logit ever reaches HBM.
 //   DLogits    the recomputed-logits backward: dl = s*(g*onehot - p*(g +
 //              gH*(z - lse + H))) with p = exp(z - lse); the gH term is the
@@ -56,15 +62,19 @@ constexpr int kTmemCols = 512;
 constexpr int kBarrierBytes = 256;
 constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
 
-__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
-                                            int& n_count, int& vunit) {
+// Unit u of a cluster -> (m tile of this CTA, N tiles). Units enumerate
+// (m block, vocab unit) pairs in groups of group_m m blocks, unit-major inside
+// a group, so concurrently running clusters share B tiles in L2.
+template <int CM>
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int rank, int& m_tile,
+                                            int& n_first, int& n_count, int& vunit) {
   const int per_group = p.group_m * p.n_vunits;
   const int g = u / per_group;
   const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.n_m_tiles - first_m);
+  const int gm = min(p.group_m, p.n_mblocks - first_m);
   const int r = u - g * per_group;
   vunit = r / gm;
-  m_tile = first_m + (r - vunit * gm);
+  m_tile = (first_m + (r - vunit * gm)) * CM + rank;
   n_first = vunit * p.tiles_per_unit;
   n_count = min(p.tiles_per_unit, p.n_n_tiles - n_first);
 }
@@ -99,7 +109,7 @@ __device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[3
   }
 }
 
-template <int E>
+template <int E, int CM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -120,11 +130,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cluster = blockIdx.x / CM;
+  const int n_clusters = gridDim.x / CM;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), CM);  // one release per CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -144,6 +158,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CM > 1) {  // peers' barriers are initialised before any multicast
+    __syncwarp();
+    cluster_sync();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kb_total = (p.K + kBK - 1) / kBK;
@@ -154,9 +172,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
         int m_tile, n_first, n_count, vunit;
-        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+        unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
           for (int kb = 0; kb < kb_total; ++kb) {
@@ -174,13 +192,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else {
               tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
             }
-            if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
+            if (CM == 1) {
+              if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
 #pragma unroll
-              for (int j = 0; j < kBN / 64; ++j)
-                tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
-                            n_tile * kBN + 64 * j, kb * kBK);
+                for (int j = 0; j < kBN / 64; ++j)
+                  tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
+                              n_tile * kBN + 64 * j, kb * kBK);
+              } else {
+                tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+              }
             } else {
-              tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+              // This CTA's 1/CM slice of the B tile, multicast to the cluster.
+              constexpr int kRows = kBN / CM;
+              if (p.b_mn) {
+#pragma unroll
+                for (int j = 0; j < kRows / 64; ++j) {
+                  const int box = rank * (kRows / 64) + j;
+                  tma_load_2d_mc(sA + kABytes + box * kMnBoxBytes, &tmB, full_bar(stage),
+                                 n_tile * kBN + 64 * box, kb * kBK, kMask);
+                }
+              } else {
+                tma_load_2d_mc(sA + kABytes + rank * (kBBytes / CM), &tmB, full_bar(stage),
+                               kb * kBK, n_tile * kBN + rank * kRows, kMask);
+              }
             }
             ++issued;
             if (++stage == kStages) {
@@ -213,9 +247,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
         int m_tile, n_first, n_count, vunit;
-        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+        unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j, ++it) {
           const uint32_t acc = it & 1u;
           const uint32_t aph = (it >> 1) & 1u;
@@ -245,7 +279,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc,
                           (kb > 0 || k > 0) ? 1u : 0u);
             }
-            tc_commit(empty_bar(stage));
+            if (CM == 1)
+              tc_commit(empty_bar(stage));
+            else
+              tc_commit_mc(empty_bar(stage), kMask);  // release the stage in every CTA
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -265,9 +302,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_in_tile = q * 32 + lane;
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       int m_tile, n_first, n_count, vunit;
-      unit_coords(p, u, m_tile, n_first, n_count, vunit);
+      unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
       const int row = m_tile * kBM + row_in_tile;
       const bool row_ok = row < p.M;
 
@@ -283,10 +320,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // with t = y - lse2: the coefficient of p is c0 + c1 * t.
           const float g = p.grad ? p.grad[row] : 0.f;
           const float ge = p.grad_ent ? p.grad_ent[row] : 0.f;
-          lse2 = p.lse[row] * kLog2e;
-          gs = g * p.inv_temp;
-          c0 = p.inv_temp * (p.grad_ent ? fmaf(ge, p.ent[row], g) : g);
-          c1 = p.inv_temp * ge * kLn2;
+          lse2 = __fmul_rn(p.lse[row], kLog2e);
+          gs = __fmul_rn(g, p.inv_temp);
+          c0 = __fmul_rn(p.inv_temp, p.grad_ent ? __fmaf_rn(ge, p.ent[row], g) : g);
+          c1 = __fmul_rn(__fmul_rn(p.inv_temp, ge), kLn2);
         }
       }
       OnlineStat st = stat_empty();
@@ -312,11 +349,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
           if constexpr (E == (int)Epi::FwdStats) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= p.scale2;
+            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], p.scale2);
             if (nvalid == 32)
-              stat_fold<32>(st, v);
+              stat_fold<32, true>(st, v);
             else
-              stat_fold<32>(st, v, nvalid);
+              stat_fold<32, true>(st, v, nvalid);
             const int rel = lab - col0;
             if (__any_sync(0xffffffffu, rel >= 0 && rel < nvalid)) {
 #pragma unroll
@@ -326,10 +363,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int rel = lab - col0;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float t = fmaf(v[i], p.scale2, -lse2);
+              const float t = __fmaf_rn(v[i], p.scale2, -lse2);
               const float pr = ex2(t);
-              float d = -pr * fmaf(c1, t, c0);
-              if (i == rel) d += gs;
+              float d = -__fmul_rn(pr, __fmaf_rn(c1, t, c0));
+              if (i == rel) d = __fadd_rn(d, gs);
               v[i] = d;
             }
             if (row_ok)
@@ -373,6 +410,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           p.part_m[o] = st.m;
           p.part_s[o] = st.s;
           p.part_u[o] = st.u;
+          if (p.part_q) p.part_q[o] = st.q;
           const int c0 = n_first * kBN;
           const int c1 = min(p.N, (n_first + n_count) * kBN);
           if (lab >= c0 && lab < c1) p.part_zl[row] = zl;
@@ -383,6 +421,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while a peer may still multicast into it or release its stages.
+  if (CM > 1) {
+    __syncwarp();
+    cluster_sync();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -390,42 +433,75 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int E>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int grid,
-                       cudaStream_t stream) {
+template <int E, int CM>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                       int num_sms, cudaStream_t stream) {
   // Set on every launch: the attribute belongs to the current device's context.
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E, CM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  gemm_tc_kernel<E><<<grid, kGemmThreads, kSmemBytes, stream>>>(a, b, p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  int max_clusters = num_sms / CM;
+  if (CM > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CM;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Persistent grid: no more clusters than can be resident at once.
+    cfg.gridDim = dim3(static_cast<unsigned>(max_clusters * CM), 1, 1);
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, gemm_tc_kernel<E, CM>, &cfg) == cudaSuccess &&
+        resident > 0 && resident < max_clusters)
+      max_clusters = resident;
+  }
+  const int clusters = p.n_units < max_clusters ? p.n_units : max_clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CM), 1, 1);
+  e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<E, CM>, a, b, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
+}
+
+template <int E>
+cudaError_t launch_cm(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                      int num_sms, cudaStream_t stream, int cm) {
+  if (cm == 4) return launch_one<E, 4>(a, b, p, num_sms, stream);
+  if (cm == 2) return launch_one<E, 2>(a, b, p, num_sms, stream);
+  return launch_one<E, 1>(a, b, p, num_sms, stream);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
+int gemm_cluster_m(int M) { return M > kBM ? 2 : 1; }
+
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream) {
+                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm) {
+  if (cm != 1 && cm != 2 && cm != 4) return cudaErrorInvalidValue;
   p.n_m_tiles = (p.M + kBM - 1) / kBM;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
+  p.n_mblocks = (p.n_m_tiles + cm - 1) / cm;
   p.tiles_per_unit = tiles_per_unit;
   p.n_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
-  p.n_units = p.n_m_tiles * p.n_vunits;
-  p.group_m = 16;
+  p.n_units = p.n_mblocks * p.n_vunits;
+  p.group_m = cm == 4 ? 4 : 16 / cm;
   if (p.n_units <= 0) return cudaSuccess;
-  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
   switch (e) {
     case Epi::FwdStats:
-      return launch_one<(int)Epi::FwdStats>(a, b, p, grid, stream);
+      return launch_cm<(int)Epi::FwdStats>(a, b, p, num_sms, stream, cm);
     case Epi::DLogits:
-      return launch_one<(int)Epi::DLogits>(a, b, p, grid, stream);
+      return launch_cm<(int)Epi::DLogits>(a, b, p, num_sms, stream, cm);
     case Epi::StoreBf16:
-      return launch_one<(int)Epi::StoreBf16>(a, b, p, grid, stream);
+      return launch_cm<(int)Epi::StoreBf16>(a, b, p, num_sms, stream, cm);
     case Epi::StoreF32:
-      return launch_one<(int)Epi::StoreF32>(a, b, p, grid, stream);
+      return launch_cm<(int)Epi::StoreF32>(a, b, p, num_sms, stream, cm);
   }
   return cudaErrorInvalidValue;
 }

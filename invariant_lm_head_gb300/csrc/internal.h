@@ -35,6 +35,7 @@ struct GemmParams {
   int M, N, K;  // D[M, N] = sum_k A[m, k] * B[n, k]
   int a_mn, b_mn;  // 1 = operand stored MN-major ([K][M] / [K][N])
   int n_m_tiles, n_n_tiles, tiles_per_unit, n_vunits, n_units, group_m;
+  int n_mblocks;  // ceil(n_m_tiles / cluster size along M)
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -44,10 +45,12 @@ struct GemmParams {
   const float* grad_ent;   // DLogits: upstream grad of entropy [M] (NULL = none)
   const float* lse;        // DLogits: natural-log lse [M]
   const float* ent;        // DLogits: entropy [M] (read only with grad_ent)
-  // FwdStats partials: planes [n_vunits][part_ld] for m, s, u; zl [M]
+  // FwdStats partials: planes [n_vunits][part_ld] for m, s, u (and q when
+  // part_q is not NULL); zl [M]
   float* part_m;
   float* part_s;
   float* part_u;
+  float* part_q;
   float* part_zl;
   int64_t part_ld;
   // DLogits: dl [M][ld_out]; StoreBf16: D [M][ld_out]
@@ -71,18 +74,29 @@ int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
 size_t gemm_smem_bytes();
-cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream);
 
+// Cluster size along M for a GEMM with M rows: CTAs of a cluster take
+// consecutive 128-row tiles and share each B tile, every CTA loading 1/cm of
+// it and multicasting it to the others. The B tensor map of a K-major B must
+// then use a box of kBN / cm rows (see gemm_b_box_rows).
+int gemm_cluster_m(int M);
+inline int gemm_b_box_rows(int cm, bool b_mn) { return b_mn ? 64 : kBN / cm; }
+
+// b_box_rows of tmB must match gemm_b_box_rows(cm, p.b_mn).
+cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm = 1);
+
+// out_sum_p2 may be NULL; when it is not, sum_v p^2 is accumulated too.
 cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
                                   int64_t V, float inv_temperature, float* out_logprob,
-                                  float* out_entropy, float* out_lse, int num_sms,
-                                  cudaStream_t stream);
+                                  float* out_entropy, float* out_lse, float* out_sum_p2,
+                                  int num_sms, cudaStream_t stream);
 
-cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pzl,
-                             const int32_t* labels, int64_t T, int n_vunits, int64_t V,
-                             float* out_logprob, float* out_entropy, float* out_lse,
-                             cudaStream_t stream);
+// pq and out_sum_p2 may be NULL (both or neither).
+cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pq,
+                             const float* pzl, const int32_t* labels, int64_t T, int n_vunits,
+                             int64_t V, float* out_logprob, float* out_entropy, float* out_lse,
+                             float* out_sum_p2, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, int* result,
                                  cudaStream_t stream);

@@ -137,8 +137,8 @@ extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t
   cudaError_t e =
       lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, sms, st);
   if (e == cudaSuccess)
-    e = lmh::launch_fwd_merge(pm, ps, pu, pzl, labels, T, static_cast<int>(n_chunks), V,
-                              out_logprob, out_entropy, out_lse, st);
+    e = lmh::launch_fwd_merge(pm, ps, pu, nullptr, pzl, labels, T, static_cast<int>(n_chunks), V,
+                              out_logprob, out_entropy, out_lse, nullptr, st);
   if (e != cudaSuccess) {
     char msg[256];
     snprintf(msg, sizeof(msg), "no-alloc forward launch: %s", cudaGetErrorString(e));

@@ -33,6 +33,9 @@ stored, each step written out as the pages define it):
   returned (verl page, review note that an entropy taken elsewhere is not the
   entropy of the fp32 log-softmax): ``entropy[t] = -sum_v p log p`` with
   ``p = exp(z - lse)``, natural log.
+* ``sum_pi_squared`` (verl page, the review note listing entropy and
+  sum_pi_squared as the per-token statistics still taken from the logits):
+  ``sum_p2[t] = sum_v p[t, v]^2`` of the same distribution.
 * Backward of ``sum_t g[t] * logprob[t]`` with respect to the projection:
   ``dz = g * (onehot - p)``, ``dlogit = s * dz``, ``grad_hidden = dlogit @
   weight``, ``grad_weight = dlogit^T @ hidden``.
@@ -58,6 +61,8 @@ __all__ = [
     "scaled_logits",
     "row_lse_entropy",
     "sampler_logprob",
+    "row_sum_p2",
+    "fused_sum_p2",
     "fused_forward",
     "logprob_from_logits",
     "dlogits",
@@ -96,6 +101,14 @@ def row_lse_entropy(z) -> tuple[np.ndarray, np.ndarray]:
     return lse, entropy
 
 
+def row_sum_p2(z) -> np.ndarray:
+    """Per row: sum_v p_v^2 with p = softmax(z)."""
+    z = _f64(z)
+    lse, _ = row_lse_entropy(z)
+    p = np.exp(z - lse[:, None])
+    return (p * p).sum(axis=1)
+
+
 def sampler_logprob(z, labels) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
     """log_softmax over the full row, then gather of the label.
 
@@ -116,6 +129,11 @@ def sampler_logprob(z, labels) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
 def fused_forward(hidden, weight, labels, inv_temperature: float):
     """(logprob, entropy, lse) of the fused LM head: z = s * hidden @ weight^T."""
     return sampler_logprob(scaled_logits(hidden, weight, inv_temperature), labels)
+
+
+def fused_sum_p2(hidden, weight, inv_temperature: float) -> np.ndarray:
+    """sum_v p[t, v]^2 of the fused LM head's distribution, per row."""
+    return row_sum_p2(scaled_logits(hidden, weight, inv_temperature))
 
 
 def logprob_from_logits(logits, labels, inv_temperature: float = 1.0):

@@ -43,6 +43,21 @@ def forward(hidden, weight, labels, inv_temperature):
     return lp_out, ent_out, lse_out
 
 
+def sum_p2(hidden, weight, inv_temperature):
+    """List of sum_v p_v^2 per row, from explicit loops."""
+    s = _s(inv_temperature)
+    T, H = len(hidden), len(hidden[0])
+    V = len(weight)
+    out = []
+    for t in range(T):
+        z = [s * math.fsum(float(hidden[t][h]) * float(weight[v][h]) for h in range(H))
+             for v in range(V)]
+        m = max(z)
+        lse = m + math.log(math.fsum(math.exp(zv - m) for zv in z))
+        out.append(math.fsum(math.exp(2.0 * (zv - lse)) for zv in z))
+    return out
+
+
 def backward(hidden, weight, labels, grad, inv_temperature, grad_entropy=None):
     """Nested lists (grad_hidden [T][H], grad_weight [V][H]) from explicit loops.
 

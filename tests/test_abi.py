@@ -47,15 +47,15 @@ def test_abi_version(lib):
 def test_workspace_sizes(lib):
     f = lmh.lmhead_workspace_size
     assert f(lmh.LMH_OP_LOGITS, 8192, 0, 152064) == 0
-    # forward: 3 planes of ceil(V / 1024) floats per row + the label logit
+    # forward: 4 planes of ceil(V / 1024) floats per row + the label logit
     n_chunks = -(-152064 // 1024)
     fwd = f(lmh.LMH_OP_FWD, 16384, 3584, 152064)
-    assert fwd >= (3 * n_chunks + 1) * 16384 * 4
-    assert fwd < (3 * n_chunks + 1) * 16384 * 4 + 8 * 256
+    assert fwd >= (4 * n_chunks + 1) * 16384 * 4
+    assert fwd < (4 * n_chunks + 1) * 16384 * 4 + 8 * 256
     # backward: forward partials + lse, logprob, entropy per row + bf16 dlogits [min(T,8192), V]
     b1 = f(lmh.LMH_OP_BWD, 8192, 3584, 152064)
     b2 = f(lmh.LMH_OP_BWD, 16384, 3584, 152064)
-    extra = (3 * n_chunks + 4) * 8192 * 4
+    extra = (4 * n_chunks + 4) * 8192 * 4
     assert 0 <= (b2 - b1) - extra < 64 * 256
     assert b1 > 8192 * 152064 * 2
     assert f(lmh.LMH_OP_FWD, 0, 256, 4096) > 0

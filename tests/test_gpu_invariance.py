@@ -70,6 +70,19 @@ def test_forward_sub_batches_offsets_and_shuffles(lmh, T, H, V, s):
             assert _mismatch(a[inv], b) == 0
 
 
+def test_sum_p2_invariant_across_batches(lmh):
+    import torch
+
+    T, H, V = 300, 264, 5000
+    hidden, weight, labels, _ = fused_case(63, T, H, V)
+    h, w, lab = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels)
+    full = lmh.lmhead_logprob_fwd_stats(h, w, lab, S07)[3]
+    for r0, r1 in [(0, 1), (1, 8), (8, 264), (131, 300)]:
+        part = lmh.lmhead_logprob_fwd_stats(h[r0:r1], w, lab[r0:r1], S07)[3]
+        assert _mismatch(part, full[r0:r1]) == 0
+    torch.cuda.synchronize()
+
+
 def test_logits_path_sub_batches_and_shuffles(lmh):
     import torch
 

@@ -266,6 +266,45 @@ def test_logits_path_equals_fused_path_on_same_logits(lmh):
     assert max_abs(ent1.cpu().numpy(), ent2.cpu().numpy()) < 1e-4
 
 
+# ----------------------------------------------------------------- sum_pi_squared
+@pytest.mark.parametrize("s", [1.0, S07])
+def test_sum_p2_fused_and_logits_match_oracle(lmh, s):
+    import torch
+
+    T, H, V = 300, 264, 5000
+    hidden, weight, labels, _ = fused_case(37, T, H, V, w_std=0.2)
+    h, w, lab = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels)
+    lp, ent, lse, q = lmh.lmhead_logprob_fwd_stats(h, w, lab, s, want_lse=True)
+    lp0, ent0, lse0 = lmh.lmhead_logprob_fwd(h, w, lab, s, want_lse=True)
+    torch.cuda.synchronize()
+    for a, b in ((lp, lp0), (ent, ent0), (lse, lse0)):  # the extra output changes nothing else
+        assert torch.equal(a, b)
+    ref = oracle.fused_sum_p2(f64(hidden), f64(weight), s)
+    assert max_abs(q.cpu().numpy(), ref) < 1e-5
+    inp = W.logits_inputs(W.LOGITS, T=130, V=4999)  # scalar path
+    for V_, x in ((4999, inp["logits"]), (5000, W.logits_inputs(W.LOGITS, T=130, V=5000)["logits"])):
+        lab2 = to_dev(W.random_labels(3, 130, V_))
+        out = lmh.logprob_from_logits_stats(to_dev_bf16(x), lab2, s, want_lse=True)
+        base = lmh.logprob_from_logits(to_dev_bf16(x), lab2, s, want_lse=True)
+        torch.cuda.synchronize()
+        for a, b in zip(out[:3], base):
+            assert torch.equal(a, b)
+        ref = oracle.row_sum_p2(oracle.fp32_scalar(s) * f64(x))
+        assert max_abs(out[3].cpu().numpy(), ref) < 1e-5
+
+
+def test_sum_p2_uniform_and_dominant_rows(lmh):
+    import torch
+
+    T, H, V = 20, 64, 4096
+    hidden = W.random_bf16(8, (T, H))
+    weight = np.zeros((V, H), dtype=np.uint16)
+    q = lmh.lmhead_logprob_fwd_stats(to_dev_bf16(hidden), to_dev_bf16(weight),
+                                     to_dev(W.random_labels(8, T, V)), 1.0)[3]
+    torch.cuda.synchronize()
+    assert np.allclose(q.cpu().numpy(), 1.0 / V, rtol=1e-4, atol=0)
+
+
 # ----------------------------------------------------------------- status
 def test_bounded_wait_selftest_reports_timeout(lmh):
     assert lmh.lmhead_selftest_wait_timeout(2_000_000) == lmh.LMH_ERR_DEVICE_TIMEOUT

@@ -281,6 +281,32 @@ def test_entropy_gradient_row_sums_vanish():
     assert np.all(np.abs(d.sum(axis=1)) < 1e-12)  # sum_j p_j (z_j - lse + H) = 0
 
 
+def test_sum_p2_closed_forms_library_and_bounds():
+    # uniform row: 1/V; two-value row: k pa^2 + (V-k) pb^2; dominant row: ~1
+    for V in (16, 4096):
+        assert abs(oracle.row_sum_p2(np.zeros((1, V)))[0] - 1.0 / V) < 1e-15
+    V, k, a, b = 4096, 7, 5.5, 0.25
+    z = np.full((1, V), b)
+    z[0, :k] = a
+    zs = k * math.exp(a) + (V - k) * math.exp(b)
+    ref = k * (math.exp(a) / zs) ** 2 + (V - k) * (math.exp(b) / zs) ** 2
+    assert abs(oracle.row_sum_p2(z)[0] - ref) < 1e-14
+    z = np.zeros((1, 100))
+    z[0, 3] = 60.0
+    assert abs(oracle.row_sum_p2(z)[0] - 1.0) < 1e-20 + 1e-12
+    rng = np.random.default_rng(17)
+    z = 3.0 * rng.standard_normal((12, 777)) + 500.0
+    sp = scipy.special.softmax(z, axis=1)
+    got = oracle.row_sum_p2(z)
+    assert np.max(np.abs(got - (sp ** 2).sum(axis=1))) < 1e-12
+    _, ent, _ = oracle.sampler_logprob(z, np.zeros(12, dtype=np.int64))
+    assert np.all(got <= sp.max(axis=1) + 1e-15) and np.all(got >= 1.0 / 777)
+    assert np.all(got >= np.exp(-ent) - 1e-15)  # Renyi-2 entropy <= Shannon entropy
+    h, w, _, _ = _tiny(18)
+    ref = loops.sum_p2(h.tolist(), w.tolist(), S07)
+    assert np.max(np.abs(oracle.fused_sum_p2(h, w, S07) - np.array(ref))) < 1e-14
+
+
 def test_dlogit_row_sums():
     h, w, lab, g = _tiny(21, T=4, H=8, V=32, oov_row=3)
     z = oracle.scaled_logits(h, w, S07)
@@ -412,6 +438,12 @@ def _backward_entropy_missing_h(h, w, lab, g, s, gh):
     return dl @ np.asarray(w, np.float64), dl.T @ np.asarray(h, np.float64)
 
 
+def _sum_p2_unnormalised(z):
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    return (e * e).sum(axis=1) / e.sum(axis=1)  # divides by s instead of s^2
+
+
 def test_planted_mistakes_are_caught():
     assert check_scipy_lse_entropy(_sampler_entropy_missing_lse, 0) > 1e-3
     assert check_two_value(_sampler_entropy_missing_lse, 4096, 7, 5.5, 0.25) > 1e-3
@@ -422,6 +454,7 @@ def test_planted_mistakes_are_caught():
     assert check_finite_differences(oracle.fused_forward, _backward_missing_temperature, 11, S07) > 1e-3
     assert check_finite_differences(oracle.fused_forward, _backward_oov_zeroed, 12, 1.0, oov_row=0) > 1e-3
     assert check_loops_forward(_forward_transposed_index, 0, 1.0) > 1e-3
+    assert abs(_sum_p2_unnormalised(np.zeros((1, 4096)))[0] - 1.0 / 4096) > 1e-3
     assert check_finite_differences_entropy(oracle.fused_forward, _backward_entropy_sign_flip, 14,
                                             1.0) > 1e-3
     assert check_finite_differences_entropy(oracle.fused_forward, _backward_entropy_missing_h, 14,
