@@ -269,6 +269,44 @@ def make_inputs(T, H, V, seed, dev):
     return hidden, weight, labels, grad
 
 
+def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
+    import torch
+
+    def bits(t):
+        return t.view(torch.int32)
+
+    lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp, out_entropy=ent, out_lse=lse)
+    full = [x.clone() for x in (lp, ent, lse)]
+    T = hidden.shape[0]
+    out = {"rows_compared": 0, "mismatched_values": 0, "cases": []}
+
+    def compare(rows, part):
+        n = sum(int((bits(a) != bits(b[rows])).sum().item()) for a, b in zip(part, full))
+        out["rows_compared"] += int(rows.numel())
+        out["mismatched_values"] += n
+        return n
+
+    dev = hidden.device
+    for bs, starts in ((1, (0, 1, T - 1)), (7, (0, 4093)), (256, (0, 8000))):
+        for r0 in starts:
+            rows = torch.arange(r0, r0 + bs, device=dev)
+            part = lmh.lmhead_logprob_fwd(hidden[r0:r0 + bs], weight, labels[r0:r0 + bs], s,
+                                          want_lse=True)
+            out["cases"].append({"batch": bs, "start": r0, "mismatched": compare(rows, part)})
+    for shift in (1, 63, 127):
+        rows = torch.arange(shift, min(T, shift + 1024), device=dev)
+        part = lmh.lmhead_logprob_fwd(hidden[rows].contiguous(), weight, labels[rows].contiguous(),
+                                      s, want_lse=True)
+        out["cases"].append({"batch": int(rows.numel()), "shift": shift,
+                             "mismatched": compare(rows, part)})
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(11)).to(dev)
+    part = lmh.lmhead_logprob_fwd(hidden[perm].contiguous(), weight, labels[perm].contiguous(), s,
+                                  want_lse=True)
+    out["cases"].append({"batch": T, "shuffled": True, "mismatched": compare(perm, part)})
+    torch.cuda.synchronize()
+    return out
+
+
 def timed(fn, steps, warmup):
     import torch
 
@@ -398,6 +436,13 @@ def run_gpu(args):
         "gpu_launches": launches, "roofline": roofline, "kernels": kernels, "clocks": clk,
         "model_tflops_per_gpu": 6.0 * T * H * V / (ms_per_step * 1e-3) / 1e12,
     }
+
+    # ------------------------------------------------- batch invariance (bit mismatches)
+    # Forward outputs of the full batch against the same rows run as
+    # sub-batches of 1, 7 and 256 rows, shifted by 1..127 rows and in one
+    # shuffled packing; counted in fp32 bits (target 0).
+    if not args.no_extras:
+        line["invariance"] = invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse)
 
     # ------------------------------------------------------------- e2e (host buffers)
     h_host = hidden.cpu().pin_memory()

@@ -110,6 +110,26 @@ int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
   return LMH_OK;
 }
 
+// Output map of a store epilogue: `cols` x `rows` elements, rows `row_bytes`
+// apart. fp32: 32 x 128 box, 128-byte swizzle; bf16: 32 x 128 box, 64-byte
+// swizzle (the staging layouts the epilogue writes). Stores outside the
+// tensor are clipped by TMA.
+int make_out_tmap(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
+                  bool f32) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {32, 128};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LMH_ERR_LAUNCH, "cuTensorMapEncodeTiled (output) failed (%d) for %llu x %llu",
+                (int)r, (unsigned long long)cols, (unsigned long long)rows);
+  return LMH_OK;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
@@ -276,7 +296,7 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
                 const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
                 float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st,
                 float* out_sum_p2 = nullptr) {
-  const int cm = lmh::gemm_cluster_m(static_cast<int>(T));
+  const int cm = lmh::gemm_cluster_m(static_cast<int>(T), false, false);
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
   LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::gemm_b_box_rows(cm, false)));
@@ -402,12 +422,12 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   }
   CUtensorMap t_w_mn;
   LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));  // [K=V][N=H]
-  const int cm_w = lmh::gemm_cluster_m(static_cast<int>(V));
+  const int cm_w = lmh::gemm_cluster_m(static_cast<int>(V), true, true);
 
   for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
-    const int cm_r = lmh::gemm_cluster_m(static_cast<int>(rows));
+    const int cm_r = lmh::gemm_cluster_m(static_cast<int>(rows), false, false);
     CUtensorMap t_w, t_h, t_h_mn, t_dl, t_dl_mn;
     LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK,
                       lmh::gemm_b_box_rows(cm_r, false)));                     // [V][K=H]
@@ -428,10 +448,12 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     p.grad_ent = grad_ent ? grad_ent + c0 : nullptr;
     p.lse = lse + c0;
     p.ent = grad_ent ? ent + c0 : nullptr;
-    p.out_bf16 = w.dl;
-    p.ld_out = w.vpad;
+    CUtensorMap o_dl, o_gh, o_gw;
+    LMH_TRY(make_out_tmap(&o_dl, w.dl, V, rows, w.vpad * 2, false));
+    LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
+    LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true));
     LMH_LAUNCH(K_DLOGITS_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, cm_r),
+               lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, cm_r, &o_dl),
                "dlogits");
 
     lmh::GemmParams q{};
@@ -440,10 +462,8 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     q.N = static_cast<int>(H);
     q.K = static_cast<int>(V);
     q.b_mn = 1;
-    q.out_bf16 = grad_hidden + c0 * H;
-    q.ld_out = H;
     LMH_LAUNCH(K_DHIDDEN_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, cm_r),
+               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, cm_r, &o_gh),
                "grad_hidden");
 
     lmh::GemmParams r{};
@@ -453,11 +473,9 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     r.K = static_cast<int>(rows);
     r.a_mn = 1;
     r.b_mn = 1;
-    r.out_f32 = grad_weight;
-    r.ld_out_f32 = H;
-    r.accumulate = c0 > 0 ? 1 : 0;
+    r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
     LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, cm_w),
+               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, cm_w, &o_gw),
                "grad_weight");
   }
   return ok();
@@ -656,7 +674,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (M == 0) return ok();
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
-  const int cm = lmh::gemm_cluster_m(static_cast<int>(M));
+  const int cm = lmh::gemm_cluster_m(static_cast<int>(M), a_mn, b_mn);
   CUtensorMap ta, tb;
   if (a_mn)
     LMH_TRY(make_tmap(&ta, A, M, K, M * 2, 64, lmh::kBK));
@@ -673,12 +691,12 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   p.K = static_cast<int>(K);
   p.a_mn = a_mn ? 1 : 0;
   p.b_mn = b_mn ? 1 : 0;
-  p.out_f32 = D;
-  p.ld_out_f32 = N;
   p.accumulate = 0;
+  CUtensorMap tc;
+  LMH_TRY(make_out_tmap(&tc, D, N, M, N * 4, true));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   LMH_LAUNCH(K_ENGINE_GEMM, st,
-             lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, cm),
+             lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, cm, &tc),
              "engine gemm");
   return ok();
 }

@@ -60,7 +60,12 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kMnBoxBytes = 64 * kBK * 2;  // one 64(MN) x 64(K) bf16 box
 constexpr int kTmemCols = 512;
 constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
+// Two staging buffers for the TMA-store epilogues: 128 rows x 128 bytes
+// (32 fp32 or, using half of it, 32 bf16 columns).
+constexpr int kStagingBytes = kBM * 128;
+constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
 
 // Unit u of a cluster -> (m tile of this CTA, N tiles). Units enumerate
 // (m block, vocab unit) pairs in groups of group_m m blocks, unit-major inside
@@ -84,40 +89,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint16_t to_bf16_bits(float x) {
-  const __nv_bfloat16 v = __float2bfloat16_rn(x);
-  return *reinterpret_cast<const uint16_t*>(&v);
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
-// Store 32 values of one row as bf16; n valid columns; dst 16-byte aligned when n == 32.
-__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const float (&v)[32], int n) {
-  if (n == 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+// One row's 32 columns into a staging buffer laid out as the TMA store reads
+// it. fp32: 128-byte rows with 128-byte swizzle (16-byte chunk j of row r at
+// chunk j ^ (r % 8)). bf16: 64-byte rows with 64-byte swizzle (chunk j at
+// j ^ ((r / 2) % 4)). Either way a warp's 32 rows spread evenly over the banks.
+__device__ __forceinline__ void stage_row_f32(uint32_t buf, int r, const float (&v)[32]) {
+  const uint32_t row = buf + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-      d4[q] = w;
-    }
-  } else {
+  for (int j = 0; j < 8; ++j)
+    st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (r & 7)) << 4), __float_as_uint(v[4 * j]),
+                 __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                 __float_as_uint(v[4 * j + 3]));
+}
+__device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float (&v)[32]) {
+  const uint32_t row = buf + static_cast<uint32_t>(r) * 64u;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < n) dst[i] = to_bf16_bits(v[i]);
-  }
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4(row + ((static_cast<uint32_t>(j) ^ ((r >> 1) & 3)) << 4),
+                 pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
+                 pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
 }
 
 template <int E, int CM>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  const uint32_t staging = smem_base + kStages * kStageBytes;  // 2 x kStagingBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 2 * kStagingBytes);
   // barrier layout: full[kStages], empty[kStages], tfull[2], tempty[2], final
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -125,8 +134,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
   const uint32_t final_bar = bar0 + 8u * (2 * kStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kStages * kStageBytes + 8 * (2 * kStages + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) +
+                                                    8 * (2 * kStages + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* epi_go = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,6 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (E != (int)Epi::FwdStats) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -298,9 +310,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // Control flow is uniform over the 128 epilogue threads: epilogue thread 0
+    // does the bounded wait for each accumulator and publishes the outcome,
+    // so no thread can be left waiting at a named barrier the others skipped.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
-    uint32_t it = 0;
+    const int etid = threadIdx.x - 64;
+    uint32_t it = 0, chunk_ctr = 0;
     bool ok = true;
     for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
       int m_tile, n_first, n_count, vunit;
@@ -333,7 +349,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int n_tile = n_first + j;
         const uint32_t acc = it & 1u;
         const uint32_t aph = (it >> 1) & 1u;
-        if (!mbar_wait(tfull_bar(acc), aph, abort_flag, p.status)) {
+        if (etid == 0) epi_go[it & 1u] = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
+        named_barrier(kEpiBarrier, 128);
+        if (!epi_go[it & 1u]) {
           ok = false;
           break;
         }
@@ -359,44 +377,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) zl = (i == rel) ? v[i] : zl;
             }
-          } else if constexpr (E == (int)Epi::DLogits) {
-            const int rel = lab - col0;
+          } else {
+            if constexpr (E == (int)Epi::DLogits) {
+              const int rel = lab - col0;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float t = __fmaf_rn(v[i], p.scale2, -lse2);
-              const float pr = ex2(t);
-              float d = -__fmul_rn(pr, __fmaf_rn(c1, t, c0));
-              if (i == rel) d = __fadd_rn(d, gs);
-              v[i] = d;
-            }
-            if (row_ok)
-              store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);
-          } else if constexpr (E == (int)Epi::StoreBf16) {
-            if (row_ok)
-              store_row_bf16(p.out_bf16 + static_cast<int64_t>(row) * p.ld_out + col0, v, nvalid);
-          } else {  // StoreF32
-            if (row_ok) {
-              float* dst = p.out_f32 + static_cast<int64_t>(row) * p.ld_out_f32 + col0;
-              if (nvalid == 32) {
-                float4* d4 = reinterpret_cast<float4*>(dst);
-#pragma unroll
-                for (int q4 = 0; q4 < 8; ++q4) {
-                  float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-                  if (p.accumulate) {
-                    const float4 o = d4[q4];
-                    w.x += o.x;
-                    w.y += o.y;
-                    w.z += o.z;
-                    w.w += o.w;
-                  }
-                  d4[q4] = w;
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                  if (i < nvalid) dst[i] = p.accumulate ? dst[i] + v[i] : v[i];
+              for (int i = 0; i < 32; ++i) {
+                const float t = __fmaf_rn(v[i], p.scale2, -lse2);
+                const float pr = ex2(t);
+                float d = -__fmul_rn(pr, __fmaf_rn(c1, t, c0));
+                if (i == rel) d = __fadd_rn(d, gs);
+                v[i] = d;
               }
             }
+            // Stage the 128 x 32 chunk and store it with one TMA bulk store
+            // (or reduce-add); rows and columns outside the output are clipped.
+            const uint32_t buf = staging + (chunk_ctr & 1u) * kStagingBytes;
+            if (etid == 0) bulk_wait_group_read<1>();  // this buffer's last store has read it
+            named_barrier(kEpiBarrier, 128);
+            if constexpr (E == (int)Epi::StoreF32)
+              stage_row_f32(buf, row_in_tile, v);
+            else
+              stage_row_bf16(buf, row_in_tile, v);
+            fence_proxy_async_smem();
+            named_barrier(kEpiBarrier, 128);
+            // A tile wholly past the last row (the spare tile of a cluster pair)
+            // stores nothing.
+            if (etid == 0 && m_tile * kBM < p.M) {
+              if (E == (int)Epi::StoreF32 && p.accumulate)
+                tma_reduce_add_2d(&tmC, buf, col0, m_tile * kBM);
+              else
+                tma_store_2d(&tmC, buf, col0, m_tile * kBM);
+              bulk_commit_group();
+            }
+            ++chunk_ctr;
           }
         }
         tc_fence_before();
@@ -417,6 +430,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
       }
     }
+    if (etid == 0) bulk_wait_group<0>();  // every output store has completed
   }
 
   tc_fence_before();
@@ -434,8 +448,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int E, int CM>
-cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                       int num_sms, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                       const GemmParams& p, int num_sms, cudaStream_t stream) {
   // Set on every launch: the attribute belongs to the current device's context.
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E, CM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -462,46 +476,54 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const GemmPar
   }
   const int clusters = p.n_units < max_clusters ? p.n_units : max_clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CM), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<E, CM>, a, b, p);
+  e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<E, CM>, a, b, c, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }
 
 template <int E>
-cudaError_t launch_cm(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
-                      int num_sms, cudaStream_t stream, int cm) {
-  if (cm == 4) return launch_one<E, 4>(a, b, p, num_sms, stream);
-  if (cm == 2) return launch_one<E, 2>(a, b, p, num_sms, stream);
-  return launch_one<E, 1>(a, b, p, num_sms, stream);
+cudaError_t launch_cm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                      const GemmParams& p, int num_sms, cudaStream_t stream, int cm) {
+  if (cm == 2) return launch_one<E, 2>(a, b, c, p, num_sms, stream);
+  return launch_one<E, 1>(a, b, c, p, num_sms, stream);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
-int gemm_cluster_m(int M) { return M > kBM ? 2 : 1; }
+// Measured on GB300 (same-session A/B, Qwen-like shapes): pairing CTAs slows
+// the contractions with a K-major B operand (forward -4 %, grad_hidden -6 %:
+// the lock-step coupling costs more than the halved B traffic saves) and
+// speeds up only the all-MN-major grad_weight contraction (+5 %: half the TMA
+// boxes per stage). Clusters of 4 were slower for every contraction.
+int gemm_cluster_m(int M, bool a_mn, bool b_mn) { return (M > kBM && a_mn && b_mn) ? 2 : 1; }
 
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm) {
-  if (cm != 1 && cm != 2 && cm != 4) return cudaErrorInvalidValue;
+                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm,
+                        const CUtensorMap* c) {
+  if (cm != 1 && cm != 2) return cudaErrorInvalidValue;
+  if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
+  CUtensorMap none{};
+  const CUtensorMap& c_map = c ? *c : none;
   p.n_m_tiles = (p.M + kBM - 1) / kBM;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
   p.n_mblocks = (p.n_m_tiles + cm - 1) / cm;
   p.tiles_per_unit = tiles_per_unit;
   p.n_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
   p.n_units = p.n_mblocks * p.n_vunits;
-  p.group_m = cm == 4 ? 4 : 16 / cm;
+  p.group_m = 16 / cm;
   if (p.n_units <= 0) return cudaSuccess;
   switch (e) {
     case Epi::FwdStats:
-      return launch_cm<(int)Epi::FwdStats>(a, b, p, num_sms, stream, cm);
+      return launch_cm<(int)Epi::FwdStats>(a, b, c_map, p, num_sms, stream, cm);
     case Epi::DLogits:
-      return launch_cm<(int)Epi::DLogits>(a, b, p, num_sms, stream, cm);
+      return launch_cm<(int)Epi::DLogits>(a, b, c_map, p, num_sms, stream, cm);
     case Epi::StoreBf16:
-      return launch_cm<(int)Epi::StoreBf16>(a, b, p, num_sms, stream, cm);
+      return launch_cm<(int)Epi::StoreBf16>(a, b, c_map, p, num_sms, stream, cm);
     case Epi::StoreF32:
-      return launch_cm<(int)Epi::StoreF32>(a, b, p, num_sms, stream, cm);
+      return launch_cm<(int)Epi::StoreF32>(a, b, c_map, p, num_sms, stream, cm);
   }
   return cudaErrorInvalidValue;
 }

@@ -53,12 +53,8 @@ struct GemmParams {
   float* part_q;
   float* part_zl;
   int64_t part_ld;
-  // DLogits: dl [M][ld_out]; StoreBf16: D [M][ld_out]
-  uint16_t* out_bf16;
-  int64_t ld_out;
-  // StoreF32: D [M][ld_out_f32], D += old when accumulate != 0
-  float* out_f32;
-  int64_t ld_out_f32;
+  // StoreF32: D += result (TMA reduce-add) instead of D = result. The output
+  // of every store epilogue is described by the C tensor map of launch_gemm.
   int accumulate;
 };
 
@@ -79,12 +75,16 @@ size_t gemm_smem_bytes();
 // consecutive 128-row tiles and share each B tile, every CTA loading 1/cm of
 // it and multicasting it to the others. The B tensor map of a K-major B must
 // then use a box of kBN / cm rows (see gemm_b_box_rows).
-int gemm_cluster_m(int M);
+int gemm_cluster_m(int M, bool a_mn, bool b_mn);
 inline int gemm_b_box_rows(int cm, bool b_mn) { return b_mn ? 64 : kBN / cm; }
 
-// b_box_rows of tmB must match gemm_b_box_rows(cm, p.b_mn).
+// b_box_rows of tmB must match gemm_b_box_rows(cm, p.b_mn). c is the output
+// tensor map of the store epilogues (NULL for FwdStats): fp32 [M][N] with a
+// 32 x 128 box and 128-byte swizzle for StoreF32, bf16 [M][N] with a 32 x 128
+// box and 64-byte swizzle for StoreBf16 and DLogits.
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm = 1);
+                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm = 1,
+                        const CUtensorMap* c = nullptr);
 
 // out_sum_p2 may be NULL; when it is not, sum_v p^2 is accumulated too.
 cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
