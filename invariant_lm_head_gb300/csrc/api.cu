@@ -296,10 +296,9 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
                 const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
                 float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st,
                 float* out_sum_p2 = nullptr) {
-  const int cm = lmh::gemm_cluster_m(static_cast<int>(T), false, false);
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
-  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::gemm_b_box_rows(cm, false)));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
   lmh::GemmParams p{};
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
@@ -315,8 +314,7 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_zl = w.pzl;
   p.part_ld = T;
   LMH_LAUNCH(K_FWD_GEMM, st,
-             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st,
-                              cm),
+             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
              "fused forward");
   LMH_LAUNCH(K_FWD_MERGE, st,
              lmh::launch_fwd_merge(w.pm, w.ps, w.pu, out_sum_p2 ? w.pq : nullptr, w.pzl, labels, T,
@@ -370,7 +368,8 @@ int logits_entry(const uint16_t* logits, const int32_t* labels, int64_t T, int64
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   LMH_LAUNCH(K_LOGITS_ROWWISE, st,
              lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob,
-                                        out_entropy, out_lse, out_sum_p2, dev->sms, st),
+                                        out_entropy, out_lse, out_sum_p2, dev->sms, dev->status,
+                                        st),
              "logits log-prob");
   return ok();
 }
@@ -422,15 +421,12 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   }
   CUtensorMap t_w_mn;
   LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));  // [K=V][N=H]
-  const int cm_w = lmh::gemm_cluster_m(static_cast<int>(V), true, true);
 
   for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
-    const int cm_r = lmh::gemm_cluster_m(static_cast<int>(rows), false, false);
     CUtensorMap t_w, t_h, t_h_mn, t_dl, t_dl_mn;
-    LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK,
-                      lmh::gemm_b_box_rows(cm_r, false)));                     // [V][K=H]
+    LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));        // [V][K=H]
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
     LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][N=H]
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
@@ -453,7 +449,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
     LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true));
     LMH_LAUNCH(K_DLOGITS_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, cm_r, &o_dl),
+               lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, &o_dl),
                "dlogits");
 
     lmh::GemmParams q{};
@@ -463,7 +459,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     q.K = static_cast<int>(V);
     q.b_mn = 1;
     LMH_LAUNCH(K_DHIDDEN_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, cm_r, &o_gh),
+               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
                "grad_hidden");
 
     lmh::GemmParams r{};
@@ -475,7 +471,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     r.b_mn = 1;
     r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
     LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, cm_w, &o_gw),
+               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, &o_gw),
                "grad_weight");
   }
   return ok();
@@ -674,7 +670,6 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (M == 0) return ok();
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
-  const int cm = lmh::gemm_cluster_m(static_cast<int>(M), a_mn, b_mn);
   CUtensorMap ta, tb;
   if (a_mn)
     LMH_TRY(make_tmap(&ta, A, M, K, M * 2, 64, lmh::kBK));
@@ -683,7 +678,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (b_mn)
     LMH_TRY(make_tmap(&tb, B, N, K, N * 2, 64, lmh::kBK));
   else
-    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::gemm_b_box_rows(cm, false)));
+    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
   lmh::GemmParams p{};
   p.status = dev->status;
   p.M = static_cast<int>(M);
@@ -696,7 +691,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   LMH_TRY(make_out_tmap(&tc, D, N, M, N * 4, true));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   LMH_LAUNCH(K_ENGINE_GEMM, st,
-             lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, cm, &tc),
+             lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, &tc),
              "engine gemm");
   return ok();
 }

@@ -16,12 +16,6 @@
 //   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
-// With a cluster of CM CTAs along M (CM = 2 for large M), the CTAs take
-// consecutive 128-row tiles of one 128*CM-row block and the same N tiles; each
-// loads 1/CM of the shared B tile and multicasts it to all of them, and each
-// MMA warp multicasts its stage-release commit, so a stage is refilled only
-// when every CTA of the cluster has consumed it. Per-SM operand traffic drops
-// from 48 KB to 16 + 32/CM KB per 64-deep stage.
 //
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
@@ -67,19 +61,18 @@ constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierB
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
 
-// Unit u of a cluster -> (m tile of this CTA, N tiles). Units enumerate
-// (m block, vocab unit) pairs in groups of group_m m blocks, unit-major inside
-// a group, so concurrently running clusters share B tiles in L2.
-template <int CM>
-__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int rank, int& m_tile,
-                                            int& n_first, int& n_count, int& vunit) {
+// Unit u -> (m tile, N tiles). Units enumerate (m tile, vocab unit) pairs in
+// groups of group_m m tiles, unit-major inside a group, so concurrently
+// running CTAs share B tiles in L2. The order changes no value.
+__device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
+                                            int& n_count, int& vunit) {
   const int per_group = p.group_m * p.n_vunits;
   const int g = u / per_group;
   const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.n_mblocks - first_m);
+  const int gm = min(p.group_m, p.n_m_tiles - first_m);
   const int r = u - g * per_group;
   vunit = r / gm;
-  m_tile = (first_m + (r - vunit * gm)) * CM + rank;
+  m_tile = first_m + (r - vunit * gm);
   n_first = vunit * p.tiles_per_unit;
   n_count = min(p.tiles_per_unit, p.n_n_tiles - n_first);
 }
@@ -117,7 +110,7 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float 
                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
 }
 
-template <int E, int CM>
+template <int E>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -141,15 +134,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = CM > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int cluster = blockIdx.x / CM;
-  const int n_clusters = gridDim.x / CM;
-  constexpr uint16_t kMask = static_cast<uint16_t>((1u << CM) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CM);  // one release per CTA of the cluster
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -170,10 +159,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CM > 1) {  // peers' barriers are initialised before any multicast
-    __syncwarp();
-    cluster_sync();
-  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kb_total = (p.K + kBK - 1) / kBK;
@@ -184,9 +169,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         int m_tile, n_first, n_count, vunit;
-        unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
+        unit_coords(p, u, m_tile, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
           for (int kb = 0; kb < kb_total; ++kb) {
@@ -204,29 +189,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             } else {
               tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
             }
-            if (CM == 1) {
-              if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
+            if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
 #pragma unroll
-                for (int j = 0; j < kBN / 64; ++j)
-                  tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
-                              n_tile * kBN + 64 * j, kb * kBK);
-              } else {
-                tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
-              }
+              for (int j = 0; j < kBN / 64; ++j)
+                tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
+                            n_tile * kBN + 64 * j, kb * kBK);
             } else {
-              // This CTA's 1/CM slice of the B tile, multicast to the cluster.
-              constexpr int kRows = kBN / CM;
-              if (p.b_mn) {
-#pragma unroll
-                for (int j = 0; j < kRows / 64; ++j) {
-                  const int box = rank * (kRows / 64) + j;
-                  tma_load_2d_mc(sA + kABytes + box * kMnBoxBytes, &tmB, full_bar(stage),
-                                 n_tile * kBN + 64 * box, kb * kBK, kMask);
-                }
-              } else {
-                tma_load_2d_mc(sA + kABytes + rank * (kBBytes / CM), &tmB, full_bar(stage),
-                               kb * kBK, n_tile * kBN + rank * kRows, kMask);
-              }
+              tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
             }
             ++issued;
             if (++stage == kStages) {
@@ -259,9 +228,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
         int m_tile, n_first, n_count, vunit;
-        unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
+        unit_coords(p, u, m_tile, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j, ++it) {
           const uint32_t acc = it & 1u;
           const uint32_t aph = (it >> 1) & 1u;
@@ -291,10 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc,
                           (kb > 0 || k > 0) ? 1u : 0u);
             }
-            if (CM == 1)
-              tc_commit(empty_bar(stage));
-            else
-              tc_commit_mc(empty_bar(stage), kMask);  // release the stage in every CTA
+            tc_commit(empty_bar(stage));
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
@@ -318,9 +284,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int etid = threadIdx.x - 64;
     uint32_t it = 0, chunk_ctr = 0;
     bool ok = true;
-    for (int u = cluster; ok && u < p.n_units; u += n_clusters) {
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
       int m_tile, n_first, n_count, vunit;
-      unit_coords<CM>(p, u, rank, m_tile, n_first, n_count, vunit);
+      unit_coords(p, u, m_tile, n_first, n_count, vunit);
       const int row = m_tile * kBM + row_in_tile;
       const bool row_ok = row < p.M;
 
@@ -400,9 +366,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               stage_row_bf16(buf, row_in_tile, v);
             fence_proxy_async_smem();
             named_barrier(kEpiBarrier, 128);
-            // A tile wholly past the last row (the spare tile of a cluster pair)
-            // stores nothing.
-            if (etid == 0 && m_tile * kBM < p.M) {
+            if (etid == 0) {
               if (E == (int)Epi::StoreF32 && p.accumulate)
                 tma_reduce_add_2d(&tmC, buf, col0, m_tile * kBM);
               else
@@ -435,11 +399,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  // No CTA leaves while a peer may still multicast into it or release its stages.
-  if (CM > 1) {
-    __syncwarp();
-    cluster_sync();
-  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -447,83 +406,49 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-template <int E, int CM>
+template <int E>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                        const GemmParams& p, int num_sms, cudaStream_t stream) {
   // Set on every launch: the attribute belongs to the current device's context.
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E, CM>,
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  int max_clusters = num_sms / CM;
-  if (CM > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CM;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // Persistent grid: no more clusters than can be resident at once.
-    cfg.gridDim = dim3(static_cast<unsigned>(max_clusters * CM), 1, 1);
-    int resident = 0;
-    if (cudaOccupancyMaxActiveClusters(&resident, gemm_tc_kernel<E, CM>, &cfg) == cudaSuccess &&
-        resident > 0 && resident < max_clusters)
-      max_clusters = resident;
-  }
-  const int clusters = p.n_units < max_clusters ? p.n_units : max_clusters;
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CM), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<E, CM>, a, b, c, p);
-  if (e == cudaSuccess) e = cudaGetLastError();
+  const int grid = p.n_units < num_sms ? p.n_units : num_sms;  // persistent: <= one CTA per SM
+  gemm_tc_kernel<E><<<grid, kGemmThreads, kSmemBytes, stream>>>(a, b, c, p);
+  e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
-}
-
-template <int E>
-cudaError_t launch_cm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                      const GemmParams& p, int num_sms, cudaStream_t stream, int cm) {
-  if (cm == 2) return launch_one<E, 2>(a, b, c, p, num_sms, stream);
-  return launch_one<E, 1>(a, b, c, p, num_sms, stream);
 }
 
 }  // namespace
 
 size_t gemm_smem_bytes() { return kSmemBytes; }
 
-// Measured on GB300 (same-session A/B, Qwen-like shapes): pairing CTAs slows
-// the contractions with a K-major B operand (forward -4 %, grad_hidden -6 %:
-// the lock-step coupling costs more than the halved B traffic saves) and
-// speeds up only the all-MN-major grad_weight contraction (+5 %: half the TMA
-// boxes per stage). Clusters of 4 were slower for every contraction.
-int gemm_cluster_m(int M, bool a_mn, bool b_mn) { return (M > kBM && a_mn && b_mn) ? 2 : 1; }
-
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream,
                         const CUtensorMap* c) {
-  if (cm != 1 && cm != 2) return cudaErrorInvalidValue;
   if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
   CUtensorMap none{};
   const CUtensorMap& c_map = c ? *c : none;
   p.n_m_tiles = (p.M + kBM - 1) / kBM;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
-  p.n_mblocks = (p.n_m_tiles + cm - 1) / cm;
   p.tiles_per_unit = tiles_per_unit;
   p.n_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
-  p.n_units = p.n_mblocks * p.n_vunits;
-  p.group_m = 16 / cm;
+  p.n_units = p.n_m_tiles * p.n_vunits;
+  // m tiles per raster group, per contraction (same-session sweep of 4/8/16/32
+  // on the Qwen-like step): the N = V contractions (forward, dlogits) share W
+  // tiles across more m tiles, the K = V grad_hidden prefers small groups.
+  p.group_m = (e == Epi::FwdStats || e == Epi::DLogits) ? 32 : (e == Epi::StoreBf16 ? 4 : 8);
   if (p.n_units <= 0) return cudaSuccess;
   switch (e) {
     case Epi::FwdStats:
-      return launch_cm<(int)Epi::FwdStats>(a, b, c_map, p, num_sms, stream, cm);
+      return launch_one<(int)Epi::FwdStats>(a, b, c_map, p, num_sms, stream);
     case Epi::DLogits:
-      return launch_cm<(int)Epi::DLogits>(a, b, c_map, p, num_sms, stream, cm);
+      return launch_one<(int)Epi::DLogits>(a, b, c_map, p, num_sms, stream);
     case Epi::StoreBf16:
-      return launch_cm<(int)Epi::StoreBf16>(a, b, c_map, p, num_sms, stream, cm);
+      return launch_one<(int)Epi::StoreBf16>(a, b, c_map, p, num_sms, stream);
     case Epi::StoreF32:
-      return launch_cm<(int)Epi::StoreF32>(a, b, c_map, p, num_sms, stream, cm);
+      return launch_one<(int)Epi::StoreF32>(a, b, c_map, p, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

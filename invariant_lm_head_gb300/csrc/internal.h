@@ -35,7 +35,6 @@ struct GemmParams {
   int M, N, K;  // D[M, N] = sum_k A[m, k] * B[n, k]
   int a_mn, b_mn;  // 1 = operand stored MN-major ([K][M] / [K][N])
   int n_m_tiles, n_n_tiles, tiles_per_unit, n_vunits, n_units, group_m;
-  int n_mblocks;  // ceil(n_m_tiles / cluster size along M)
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -71,26 +70,20 @@ int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
 
 size_t gemm_smem_bytes();
 
-// Cluster size along M for a GEMM with M rows: CTAs of a cluster take
-// consecutive 128-row tiles and share each B tile, every CTA loading 1/cm of
-// it and multicasting it to the others. The B tensor map of a K-major B must
-// then use a box of kBN / cm rows (see gemm_b_box_rows).
-int gemm_cluster_m(int M, bool a_mn, bool b_mn);
-inline int gemm_b_box_rows(int cm, bool b_mn) { return b_mn ? 64 : kBN / cm; }
-
-// b_box_rows of tmB must match gemm_b_box_rows(cm, p.b_mn). c is the output
-// tensor map of the store epilogues (NULL for FwdStats): fp32 [M][N] with a
-// 32 x 128 box and 128-byte swizzle for StoreF32, bf16 [M][N] with a 32 x 128
-// box and 64-byte swizzle for StoreBf16 and DLogits.
+// a / b: operand maps with boxes of 64(K) x 128 rows (A) and 64(K) x 256 rows
+// (B) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map
+// of the store epilogues (NULL for FwdStats): fp32 [M][N] with a 32 x 128 box
+// and 128-byte swizzle for StoreF32, bf16 [M][N] with a 32 x 128 box and
+// 64-byte swizzle for StoreBf16 and DLogits.
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream, int cm = 1,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream,
                         const CUtensorMap* c = nullptr);
 
 // out_sum_p2 may be NULL; when it is not, sum_v p^2 is accumulated too.
 cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
                                   int64_t V, float inv_temperature, float* out_logprob,
                                   float* out_entropy, float* out_lse, float* out_sum_p2,
-                                  int num_sms, cudaStream_t stream);
+                                  int num_sms, unsigned* status, cudaStream_t stream);
 
 // pq and out_sum_p2 may be NULL (both or neither).
 cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pq,

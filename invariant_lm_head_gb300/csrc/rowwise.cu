@@ -25,18 +25,9 @@ namespace {
 
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
-constexpr int kVecPerIter = 4;  // 16-byte loads in flight per thread per step
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
 
 // Fixed-order CTA reduction of per-thread states: shuffle-down tree inside
 // each warp, then warp 0's lane 0 folds the warp results in warp order.
@@ -75,59 +66,169 @@ __device__ __forceinline__ void write_row_outputs(int64_t row, const OnlineStat&
   if (out_sum_p2) out_sum_p2[row] = __fdiv_rn(st.q, __fmul_rn(st.s, st.s));
 }
 
-// V % 8 == 0: each thread owns the 16-byte vectors tid, tid + 512, ... of its
-// row, folded kVecPerIter vectors (32 values) at a time. kQ adds sum p^2.
+// V % 8 == 0, streamed through shared memory. Warp 0 (one thread) copies each
+// row in 16 KB chunks into a kLStages-deep ring with untiled bulk copies, so
+// the next chunks (and the next row) are in flight while 8 consumer warps
+// fold the current one. Consumer thread t owns the 16-byte vectors t, t+256,
+// t+512, t+768 of every chunk, so a row's fold order depends only on V.
+// Every wait is bounded; after a timeout the loops still run to the end
+// (skipping work) so all consumers reach the same named barriers.
+constexpr int kLConsumers = 256;
+constexpr int kLThreads = 32 + kLConsumers;
+constexpr int kLChunkBytes = 16384;
+constexpr int kLVecPerThread = kLChunkBytes / 16 / kLConsumers;  // 4
+constexpr int kLStages = 6;
+constexpr int kLSmemBytes = kLStages * kLChunkBytes + 1024;
+
 template <bool kQ>
-__global__ void __launch_bounds__(kRowThreads)
-    logits_logprob_vec_kernel(const uint16_t* __restrict__ logits, const int32_t* __restrict__ labels,
-                              int64_t T, int64_t V, float scale2, float* __restrict__ out_lp,
+__global__ void __launch_bounds__(kLThreads, 2)
+    logits_logprob_tma_kernel(const uint16_t* __restrict__ logits,
+                              const int32_t* __restrict__ labels, int64_t T, int64_t V,
+                              float scale2, float* __restrict__ out_lp,
                               float* __restrict__ out_ent, float* __restrict__ out_lse,
-                              float* __restrict__ out_sum_p2) {
-  __shared__ OnlineStat sh[kRowWarps];
-  const int64_t nvec = V >> 3;
-  for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
-    const uint4* rp = reinterpret_cast<const uint4*>(logits + row * V);
-    OnlineStat st = stat_empty();
-    for (int64_t base = threadIdx.x; base < nvec; base += (int64_t)kVecPerIter * kRowThreads) {
-      uint4 w[kVecPerIter];
-      int nv = 0;
-#pragma unroll
-      for (int k = 0; k < kVecPerIter; ++k) {
-        const int64_t idx = base + (int64_t)k * kRowThreads;
-        if (idx < nvec) {
-          w[k] = ld_stream(rp + idx);
-          nv = k + 1;
-        } else {
-          w[k] = make_uint4(0, 0, 0, 0);
+                              float* __restrict__ out_sum_p2, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                             ~static_cast<uintptr_t>(127));
+  __shared__ __align__(8) uint64_t bars[2 * kLStages];
+  __shared__ OnlineStat sh[2][kLConsumers / 32];
+  __shared__ int abort_word;
+  const uint32_t ring = smem_u32(smem);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int st) { return bar0 + 8u * st; };
+  auto empty_bar = [&](int st) { return bar0 + 8u * (kLStages + st); };
+  volatile int* abort_flag = &abort_word;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kLStages; ++st) {
+      mbar_init(full_bar(st), 1);
+      mbar_init(empty_bar(st), kLConsumers / 32);
+    }
+    abort_word = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int64_t row_bytes = V * 2;
+  const int64_t n_chunks = (row_bytes + kLChunkBytes - 1) / kLChunkBytes;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------- producer
+      uint32_t stage = 0, phase = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int64_t row = blockIdx.x; ok && row < T; row += gridDim.x) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(logits + row * V);
+        for (int64_t c = 0; c < n_chunks; ++c) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const int64_t off = c * kLChunkBytes;
+          const uint32_t bytes = static_cast<uint32_t>(
+              row_bytes - off < kLChunkBytes ? row_bytes - off : kLChunkBytes);
+          mbar_arrive_expect_tx(full_bar(stage), bytes);
+          bulk_load_1d(ring + stage * kLChunkBytes, src + off, bytes, full_bar(stage));
+          ++issued;
+          if (++stage == kLStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-      float y[8 * kVecPerIter];
-#pragma unroll
-      for (int k = 0; k < kVecPerIter; ++k) {
-        y[8 * k + 0] = __fmul_rn(bf16_lo(w[k].x), scale2);
-        y[8 * k + 1] = __fmul_rn(bf16_hi(w[k].x), scale2);
-        y[8 * k + 2] = __fmul_rn(bf16_lo(w[k].y), scale2);
-        y[8 * k + 3] = __fmul_rn(bf16_hi(w[k].y), scale2);
-        y[8 * k + 4] = __fmul_rn(bf16_lo(w[k].z), scale2);
-        y[8 * k + 5] = __fmul_rn(bf16_hi(w[k].z), scale2);
-        y[8 * k + 6] = __fmul_rn(bf16_lo(w[k].w), scale2);
-        y[8 * k + 7] = __fmul_rn(bf16_hi(w[k].w), scale2);
+      if (!ok) {  // drain this thread's copies (bounded) before the CTA can exit
+        volatile int no_abort = 0;
+        const long long n = issued < kLStages ? issued : kLStages;
+        uint32_t st = stage, ph = phase;
+        for (long long i = 0; i < n; ++i) {
+          if (st == 0) {
+            st = kLStages - 1;
+            ph ^= 1u;
+          } else {
+            --st;
+          }
+          mbar_wait(full_bar(st), ph, &no_abort, status);
+        }
       }
-      if (nv == kVecPerIter)
-        stat_fold<8 * kVecPerIter, kQ>(st, y);
-      else
-        stat_fold<8 * kVecPerIter, kQ>(st, y, 8 * nv);
     }
-    const OnlineStat r = cta_reduce<kQ>(st, sh);
-    if (threadIdx.x == 0) {
-      const int lab = labels[row];
-      const bool ok = lab >= 0 && (int64_t)lab < V;
-      float yl = 0.f;
-      if (ok) {
-        const uint16_t b = logits[row * V + lab];
-        yl = __fmul_rn(__uint_as_float(static_cast<uint32_t>(b) << 16), scale2);
+  } else {
+    // ------------------------------------------------------------ consumers
+    const int ct = threadIdx.x - 32;
+    const int cw = warp - 1;
+    uint32_t stage = 0, phase = 0, parity = 0;
+    bool ok = true;
+    for (int64_t row = blockIdx.x; row < T; row += gridDim.x, parity ^= 1u) {
+      OnlineStat st = stat_empty();
+      for (int64_t c = 0; c < n_chunks; ++c) {
+        if (ok) ok = mbar_wait(full_bar(stage), phase, abort_flag, status);
+        if (ok) {
+          const int64_t off = c * kLChunkBytes;
+          const int64_t bytes = row_bytes - off < kLChunkBytes ? row_bytes - off : kLChunkBytes;
+          const int nvec = static_cast<int>(bytes >> 4);
+          const uint32_t base = ring + stage * kLChunkBytes;
+          uint4 w[kLVecPerThread];
+          int nv = 0;
+#pragma unroll
+          for (int k = 0; k < kLVecPerThread; ++k) {
+            const int idx = ct + k * kLConsumers;
+            if (idx < nvec) {
+              w[k] = ld_shared_v4(base + (static_cast<uint32_t>(idx) << 4));
+              nv = k + 1;
+            } else {
+              w[k] = make_uint4(0, 0, 0, 0);
+            }
+          }
+          if (nv > 0) {
+            float y[8 * kLVecPerThread];
+#pragma unroll
+            for (int k = 0; k < kLVecPerThread; ++k) {
+              y[8 * k + 0] = __fmul_rn(bf16_lo(w[k].x), scale2);
+              y[8 * k + 1] = __fmul_rn(bf16_hi(w[k].x), scale2);
+              y[8 * k + 2] = __fmul_rn(bf16_lo(w[k].y), scale2);
+              y[8 * k + 3] = __fmul_rn(bf16_hi(w[k].y), scale2);
+              y[8 * k + 4] = __fmul_rn(bf16_lo(w[k].z), scale2);
+              y[8 * k + 5] = __fmul_rn(bf16_hi(w[k].z), scale2);
+              y[8 * k + 6] = __fmul_rn(bf16_lo(w[k].w), scale2);
+              y[8 * k + 7] = __fmul_rn(bf16_hi(w[k].w), scale2);
+            }
+            if (nv == kLVecPerThread)
+              stat_fold<8 * kLVecPerThread, kQ>(st, y);
+            else
+              stat_fold<8 * kLVecPerThread, kQ>(st, y, 8 * nv);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(stage));  // this warp is done with the chunk
+        if (++stage == kLStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      write_row_outputs(row, r, yl, ok, out_lp, out_ent, out_lse, out_sum_p2);
+      // fixed-order reduction: shuffle-down tree, then warp order
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        OnlineStat o;
+        o.m = __shfl_down_sync(0xffffffffu, st.m, off);
+        o.s = __shfl_down_sync(0xffffffffu, st.s, off);
+        o.u = __shfl_down_sync(0xffffffffu, st.u, off);
+        o.q = kQ ? __shfl_down_sync(0xffffffffu, st.q, off) : 0.f;
+        if (lane + off < 32) stat_merge<kQ>(st, o);
+      }
+      if (lane == 0) sh[parity][cw] = st;
+      named_barrier(1, kLConsumers);
+      if (ct == 0 && ok) {
+        OnlineStat r = sh[parity][0];
+        for (int k = 1; k < kLConsumers / 32; ++k) stat_merge<kQ>(r, sh[parity][k]);
+        const int lab = labels[row];
+        const bool lab_ok = lab >= 0 && (int64_t)lab < V;
+        float yl = 0.f;
+        if (lab_ok)
+          yl = __fmul_rn(__uint_as_float(static_cast<uint32_t>(logits[row * V + lab]) << 16), scale2);
+        write_row_outputs(row, r, yl, lab_ok, out_lp, out_ent, out_lse, out_sum_p2);
+      }
     }
   }
 }
@@ -213,20 +314,31 @@ __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_
 
 cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
                                   int64_t V, float inv_temperature, float* out_lp, float* out_ent,
-                                  float* out_lse, float* out_sum_p2, int num_sms,
+                                  float* out_lse, float* out_sum_p2, int num_sms, unsigned* status,
                                   cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const float scale2 = inv_temperature * kLog2e;
   const int64_t max_grid = (int64_t)num_sms * 4;
   const int grid = (int)(T < max_grid ? T : max_grid);
   const bool vec = (V & 7) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
-  if (vec && out_sum_p2)
-    logits_logprob_vec_kernel<true><<<grid, kRowThreads, 0, stream>>>(
-        logits, labels, T, V, scale2, out_lp, out_ent, out_lse, out_sum_p2);
-  else if (vec)
-    logits_logprob_vec_kernel<false><<<grid, kRowThreads, 0, stream>>>(
-        logits, labels, T, V, scale2, out_lp, out_ent, out_lse, nullptr);
-  else if (out_sum_p2)
+  if (vec) {
+    const int64_t tgrid = (int64_t)num_sms * 2;
+    const int g2 = (int)(T < tgrid ? T : tgrid);
+    cudaError_t e;
+    if (out_sum_p2) {
+      e = cudaFuncSetAttribute(logits_logprob_tma_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
+      if (e != cudaSuccess) return e;
+      logits_logprob_tma_kernel<true><<<g2, kLThreads, kLSmemBytes, stream>>>(
+          logits, labels, T, V, scale2, out_lp, out_ent, out_lse, out_sum_p2, status);
+    } else {
+      e = cudaFuncSetAttribute(logits_logprob_tma_kernel<false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
+      if (e != cudaSuccess) return e;
+      logits_logprob_tma_kernel<false><<<g2, kLThreads, kLSmemBytes, stream>>>(
+          logits, labels, T, V, scale2, out_lp, out_ent, out_lse, nullptr, status);
+    }
+  } else if (out_sum_p2)
     logits_logprob_scalar_kernel<true><<<grid, kRowThreads, 0, stream>>>(
         logits, labels, T, V, scale2, out_lp, out_ent, out_lse, out_sum_p2);
   else
