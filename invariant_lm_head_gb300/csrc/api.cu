@@ -115,10 +115,21 @@ int make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
 // swizzle (the staging layouts the epilogue writes). Stores outside the
 // tensor are clipped by TMA.
 int make_out_tmap(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t row_bytes,
-                  bool f32) {
+                  bool f32, bool transposed = false) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {32, 128};
+  if (transposed) {  // StoreF32T: 128 columns x 32 rows of fp32, no swizzle
+    box[0] = 128;
+    box[1] = 32;
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(LMH_ERR_LAUNCH, "cuTensorMapEncodeTiled (transposed output) failed (%d)", (int)r);
+    return LMH_OK;
+  }
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -428,9 +439,9 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     CUtensorMap t_w, t_h, t_h_mn, t_dl, t_dl_mn;
     LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));        // [V][K=H]
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
-    LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][N=H]
+    LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][M=H]
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
-    LMH_TRY(make_tmap(&t_dl_mn, w.dl, V, rows, w.vpad * 2, 64, lmh::kBK));    // [K=rows][M=V]
+    LMH_TRY(make_tmap(&t_dl_mn, w.dl, V, rows, w.vpad * 2, 64, lmh::kBK));    // [K=rows][N=V]
 
     lmh::GemmParams p{};
     p.status = dev->status;
@@ -447,7 +458,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     CUtensorMap o_dl, o_gh, o_gw;
     LMH_TRY(make_out_tmap(&o_dl, w.dl, V, rows, w.vpad * 2, false));
     LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
-    LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true));
+    LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true, true));
     LMH_LAUNCH(K_DLOGITS_GEMM, st,
                lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, &o_dl),
                "dlogits");
@@ -464,14 +475,15 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
 
     lmh::GemmParams r{};
     r.status = dev->status;
-    r.M = static_cast<int>(V);
-    r.N = static_cast<int>(H);
+    // grad_weight^T [H][V] = hidden^T * dl, stored transposed into grad_weight [V][H]
+    r.M = static_cast<int>(H);
+    r.N = static_cast<int>(V);
     r.K = static_cast<int>(rows);
     r.a_mn = 1;
     r.b_mn = 1;
     r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
     LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32, t_dl_mn, t_h_mn, r, 1, dev->sms, st, &o_gw),
+               lmh::launch_gemm(lmh::Epi::StoreF32T, t_h_mn, t_dl_mn, r, 1, dev->sms, st, &o_gw),
                "grad_weight");
   }
   return ok();

@@ -29,7 +29,12 @@
 //              for an out-of-vocab label (same page, out-of-vocab gradient
 //              fix); written as bf16 dl [rows][V].
 //   StoreBf16  grad_hidden = dl * W (B = W read MN-major), rounded once to bf16.
-//   StoreF32   grad_weight = dl^T * hidden (A = dl and B = hidden read
+//   StoreF32T  grad_weight^T = hidden^T * dl (A = hidden and B = dl read
+//              MN-major), written transposed as grad_weight [V][H] in fp32,
+//              accumulated over row chunks in ascending order. Taking the
+//              small hidden operand as A keeps it resident in L2 while dl
+//              streams through once.
+//   StoreF32   D = A * B^T in fp32 (the bare engine GEMM; A = dl and B = hidden read
 //              MN-major) in fp32, accumulated over row chunks in ascending order.
 //
 // Batch invariance: K is walked in the same order for every tile, the work
@@ -100,6 +105,17 @@ __device__ __forceinline__ void stage_row_f32(uint32_t buf, int r, const float (
     st_shared_v4(row + ((static_cast<uint32_t>(j) ^ (r & 7)) << 4), __float_as_uint(v[4 * j]),
                  __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
                  __float_as_uint(v[4 * j + 3]));
+}
+// Transposed staging for StoreF32T: value i of row r goes to [i][r] of a
+// 32 x 128 fp32 box (512-byte rows, no swizzle); for a fixed i the 32 lanes of
+// a warp write 32 consecutive words, one per bank.
+__device__ __forceinline__ void stage_col_f32(uint32_t buf, int r, const float (&v)[32]) {
+  const uint32_t col = buf + static_cast<uint32_t>(r) * 4u;
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(col + static_cast<uint32_t>(i) * 512u),
+                 "r"(__float_as_uint(v[i]))
+                 : "memory");
 }
 __device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float (&v)[32]) {
   const uint32_t row = buf + static_cast<uint32_t>(r) * 64u;
@@ -362,15 +378,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             named_barrier(kEpiBarrier, 128);
             if constexpr (E == (int)Epi::StoreF32)
               stage_row_f32(buf, row_in_tile, v);
+            else if constexpr (E == (int)Epi::StoreF32T)
+              stage_col_f32(buf, row_in_tile, v);
             else
               stage_row_bf16(buf, row_in_tile, v);
             fence_proxy_async_smem();
             named_barrier(kEpiBarrier, 128);
             if (etid == 0) {
-              if (E == (int)Epi::StoreF32 && p.accumulate)
-                tma_reduce_add_2d(&tmC, buf, col0, m_tile * kBM);
+              // (x, y) of the box in the output: transposed for StoreF32T
+              const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
+              const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM;
+              if ((E == (int)Epi::StoreF32 || E == (int)Epi::StoreF32T) && p.accumulate)
+                tma_reduce_add_2d(&tmC, buf, ox, oy);
               else
-                tma_store_2d(&tmC, buf, col0, m_tile * kBM);
+                tma_store_2d(&tmC, buf, ox, oy);
               bulk_commit_group();
             }
             ++chunk_ctr;
@@ -438,7 +459,9 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   // m tiles per raster group, per contraction (same-session sweep of 4/8/16/32
   // on the Qwen-like step): the N = V contractions (forward, dlogits) share W
   // tiles across more m tiles, the K = V grad_hidden prefers small groups.
-  p.group_m = (e == Epi::FwdStats || e == Epi::DLogits) ? 32 : (e == Epi::StoreBf16 ? 4 : 8);
+  p.group_m = (e == Epi::FwdStats || e == Epi::DLogits || e == Epi::StoreF32T)
+                  ? 32
+                  : (e == Epi::StoreBf16 ? 4 : 8);
   if (p.n_units <= 0) return cudaSuccess;
   switch (e) {
     case Epi::FwdStats:
@@ -449,6 +472,8 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
       return launch_one<(int)Epi::StoreBf16>(a, b, c_map, p, num_sms, stream);
     case Epi::StoreF32:
       return launch_one<(int)Epi::StoreF32>(a, b, c_map, p, num_sms, stream);
+    case Epi::StoreF32T:
+      return launch_one<(int)Epi::StoreF32T>(a, b, c_map, p, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

@@ -26,7 +26,8 @@ constexpr int kFwdChunkCols = kFwdTilesPerChunk * kBN;
 // Backward: rows are processed in fixed chunks of kBwdRowChunk.
 constexpr int64_t kBwdRowChunk = 8192;
 
-enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3 };
+// StoreF32T stores the transpose: D[m][n] goes to out[n][m].
+enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3, StoreF32T = 4 };
 
 // Operand layouts. K-major: the operand is stored [rows][K] (K contiguous);
 // MN-major: stored [K][rows] (rows contiguous). Both are read by TMA with
@@ -52,7 +53,7 @@ struct GemmParams {
   float* part_q;
   float* part_zl;
   int64_t part_ld;
-  // StoreF32: D += result (TMA reduce-add) instead of D = result. The output
+  // StoreF32(T): D += result (TMA reduce-add) instead of D = result. The output
   // of every store epilogue is described by the C tensor map of launch_gemm.
   int accumulate;
 };
@@ -73,7 +74,8 @@ size_t gemm_smem_bytes();
 // a / b: operand maps with boxes of 64(K) x 128 rows (A) and 64(K) x 256 rows
 // (B) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map
 // of the store epilogues (NULL for FwdStats): fp32 [M][N] with a 32 x 128 box
-// and 128-byte swizzle for StoreF32, bf16 [M][N] with a 32 x 128 box and
+// and 128-byte swizzle for StoreF32, fp32 [N][M] with a 128 x 32 box and no
+// swizzle for StoreF32T, bf16 [M][N] with a 32 x 128 box and
 // 64-byte swizzle for StoreBf16 and DLogits.
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
                         int tiles_per_unit, int num_sms, cudaStream_t stream,
