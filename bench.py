@@ -405,7 +405,7 @@ def run_gpu(args):
         per.setdefault(name, []).append(ms)
     kernels = {k: {"launches": len(v), "avg_ms": sum(v) / len(v), "total_ms": sum(v)}
                for k, v in per.items()}
-    rows_per_chunk = 8192
+    rows_per_chunk = 16384
     flops_per_launch = {
         "fused_fwd_gemm": 2.0 * T * H * V,
         "dlogits_gemm": 2.0 * min(T, rows_per_chunk) * H * V,

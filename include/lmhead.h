@@ -70,7 +70,7 @@ struct CUstream_st; /* cudaStream_t */
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
  * Returns SIZE_MAX for invalid arguments. The forward needs 16 bytes per row
  * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
- * row and a bf16 dlogits buffer of min(T, 8192) x V.
+ * row and a bf16 dlogits buffer of min(T, 16384) x V.
  */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 
@@ -118,7 +118,7 @@ int lmhead_logprob_fwd_stats(const uint16_t* hidden, const uint16_t* weight, con
  *   grad_logprob  f32 [T]
  *   lse           f32 [T] from lmhead_logprob_fwd, or NULL to recompute it
  *   workspace     >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) bytes
- * Rows are processed in fixed chunks of 8192; dlogits of a chunk are rounded
+ * Rows are processed in fixed chunks of 16384; dlogits of a chunk are rounded
  * to bf16 before both contractions; grad_weight sums the chunks in ascending
  * order. T == 0 zeroes grad_weight (then only grad_weight has to be a valid
  * pointer).

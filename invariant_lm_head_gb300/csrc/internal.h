@@ -24,7 +24,7 @@ constexpr int kFwdTilesPerChunk = 4;
 constexpr int kFwdChunkCols = kFwdTilesPerChunk * kBN;
 
 // Backward: rows are processed in fixed chunks of kBwdRowChunk.
-constexpr int64_t kBwdRowChunk = 8192;
+constexpr int64_t kBwdRowChunk = 16384;
 
 // StoreF32T stores the transpose: D[m][n] goes to out[n][m].
 enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3, StoreF32T = 4 };

@@ -20,6 +20,8 @@
 // kernel that folds the same values gets the same bits.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "ptx.cuh"
 
 namespace lmh {
@@ -76,6 +78,61 @@ __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], i
       s1 = __fadd_rn(s1, eb);
       u1 = __fmaf_rn(eb, db, u1);
       if (kQ) q1 = __fmaf_rn(eb, eb, q1);
+    }
+  }
+  if (kQ) st.q = __fmaf_rn(st.q, __fmul_rn(a, a), __fadd_rn(q0, q1));
+  st.s = __fadd_rn(s, __fadd_rn(s0, s1));
+  st.u = __fadd_rn(u, __fadd_rn(u0, u1));
+  st.m = mn;
+}
+
+// Fold 32 bf16 values, given as 4 x 16-byte words (8 values each, of which
+// the first nv words are valid), scaled by c > 0, into the state. Same
+// statistics as stat_fold on y = x * c, in fewer instructions: the max is taken
+// on the raw bf16 pairs (exact, and max commutes with the positive scale), and
+// the scale and the max shift are one FMA, d = x * c - m. Every operation is
+// still an explicit round-to-nearest intrinsic in a fixed order.
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+template <bool kQ>
+__device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&w)[4], int nv,
+                                                  float c) {
+  __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0].x);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nv) {
+      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (k > 0 || q > 0) m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&ws[q]));
+    }
+  }
+  const float gmax = fmaxf(__low2float(m2), __high2float(m2));
+  const float mn = fmaxf(st.m, __fmul_rn(gmax, c));
+  const float d0 = __fsub_rn(st.m, mn);
+  const float a = ex2(d0);
+  const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
+  const float s = __fmul_rn(st.s, a);
+  const float nmn = -mn;
+  float s0 = 0.f, s1 = 0.f, u0 = 0.f, u1 = 0.f, q0 = 0.f, q1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (k < nv) {
+      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float da = __fmaf_rn(bf16_lo_f(ws[q]), c, nmn);
+        const float ea = ex2(da);
+        s0 = __fadd_rn(s0, ea);
+        u0 = __fmaf_rn(ea, da, u0);
+        if (kQ) q0 = __fmaf_rn(ea, ea, q0);
+        const float db = __fmaf_rn(bf16_hi_f(ws[q]), c, nmn);
+        const float eb = ex2(db);
+        s1 = __fadd_rn(s1, eb);
+        u1 = __fmaf_rn(eb, db, u1);
+        if (kQ) q1 = __fmaf_rn(eb, eb, q1);
+      }
     }
   }
   if (kQ) st.q = __fmaf_rn(st.q, __fmul_rn(a, a), __fadd_rn(q0, q1));

@@ -77,6 +77,7 @@ constexpr int kLConsumers = 256;
 constexpr int kLThreads = 32 + kLConsumers;
 constexpr int kLChunkBytes = 16384;
 constexpr int kLVecPerThread = kLChunkBytes / 16 / kLConsumers;  // 4
+static_assert(kLVecPerThread == 4, "stat_fold_bf16x32 folds four 16-byte words per thread");
 constexpr int kLStages = 6;
 constexpr int kLSmemBytes = kLStages * kLChunkBytes + 1024;
 
@@ -181,24 +182,7 @@ __global__ void __launch_bounds__(kLThreads, 2)
               w[k] = make_uint4(0, 0, 0, 0);
             }
           }
-          if (nv > 0) {
-            float y[8 * kLVecPerThread];
-#pragma unroll
-            for (int k = 0; k < kLVecPerThread; ++k) {
-              y[8 * k + 0] = __fmul_rn(bf16_lo(w[k].x), scale2);
-              y[8 * k + 1] = __fmul_rn(bf16_hi(w[k].x), scale2);
-              y[8 * k + 2] = __fmul_rn(bf16_lo(w[k].y), scale2);
-              y[8 * k + 3] = __fmul_rn(bf16_hi(w[k].y), scale2);
-              y[8 * k + 4] = __fmul_rn(bf16_lo(w[k].z), scale2);
-              y[8 * k + 5] = __fmul_rn(bf16_hi(w[k].z), scale2);
-              y[8 * k + 6] = __fmul_rn(bf16_lo(w[k].w), scale2);
-              y[8 * k + 7] = __fmul_rn(bf16_hi(w[k].w), scale2);
-            }
-            if (nv == kLVecPerThread)
-              stat_fold<8 * kLVecPerThread, kQ>(st, y);
-            else
-              stat_fold<8 * kLVecPerThread, kQ>(st, y, 8 * nv);
-          }
+          if (nv > 0) stat_fold_bf16x32<kQ>(st, w, nv, scale2);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(stage));  // this warp is done with the chunk

@@ -52,12 +52,12 @@ def test_workspace_sizes(lib):
     fwd = f(lmh.LMH_OP_FWD, 16384, 3584, 152064)
     assert fwd >= (4 * n_chunks + 1) * 16384 * 4
     assert fwd < (4 * n_chunks + 1) * 16384 * 4 + 8 * 256
-    # backward: forward partials + lse, logprob, entropy per row + bf16 dlogits [min(T,8192), V]
-    b1 = f(lmh.LMH_OP_BWD, 8192, 3584, 152064)
-    b2 = f(lmh.LMH_OP_BWD, 16384, 3584, 152064)
-    extra = (4 * n_chunks + 4) * 8192 * 4
+    # backward: forward partials + lse, logprob, entropy per row + bf16 dlogits [min(T,16384), V]
+    b1 = f(lmh.LMH_OP_BWD, 16384, 3584, 152064)
+    b2 = f(lmh.LMH_OP_BWD, 32768, 3584, 152064)
+    extra = (4 * n_chunks + 4) * 16384 * 4
     assert 0 <= (b2 - b1) - extra < 64 * 256
-    assert b1 > 8192 * 152064 * 2
+    assert b1 > 16384 * 152064 * 2
     assert f(lmh.LMH_OP_FWD, 0, 256, 4096) > 0
     for bad in [(lmh.LMH_OP_FWD, -1, 256, 4096), (lmh.LMH_OP_FWD, 4, 12, 4096),
                 (lmh.LMH_OP_FWD, 4, 256, 0), (7, 4, 256, 4096)]:

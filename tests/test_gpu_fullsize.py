@@ -124,7 +124,7 @@ def test_qwen_config_forward_backward_sampled(lmh, qwen):
     gh, gw = lmh.lmhead_logprob_bwd(h, w, lab, g, s, lse=lse)
     torch.cuda.synchronize()
     lmh.lmhead_device_status()
-    rows = _sample_rows(wl.T, 64, 3, extra=(8191, 8192))
+    rows = _sample_rows(wl.T, 64, 3, extra=(8191, 8192, 16383))
     h64 = f64(inp["hidden"][rows])
     rlp, rent, rlse = oracle.fused_forward_rows(h64, w64, inp["labels"][rows], s,
                                                 np.arange(len(rows)))
@@ -148,7 +148,7 @@ def test_qwen_config_grad_weight_with_sparse_upstream_grad(lmh, qwen):
 
     wl, inp, w64 = qwen
     s = wl.inv_temperature
-    active = _sample_rows(wl.T, 48, 4, extra=(8191, 8192))
+    active = _sample_rows(wl.T, 48, 4, extra=(8191, 8192, 16383))
     g = np.zeros(wl.T, dtype=np.float32)
     g[active] = inp["grad"][active]
     h, w = to_dev_bf16(inp["hidden"]), to_dev_bf16(inp["weight"])

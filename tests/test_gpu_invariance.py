@@ -144,11 +144,11 @@ def test_entropy_grad_hidden_rows_invariant_across_batches(lmh):
 def test_grad_hidden_rows_invariant_across_row_chunk_boundary(lmh):
     import torch
 
-    T, H, V = 8192 + 130, 64, 600
+    T, H, V = 16384 + 130, 64, 600
     hidden, weight, labels, grad = fused_case(81, T, H, V)
     h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
     gh_full, _ = lmh.lmhead_logprob_bwd(h, w, lab, g, 1.0)
-    for r0, r1 in [(8100, 8300), (8191, 8193), (0, 1), (8192, T)]:
+    for r0, r1 in [(16300, 16500), (16383, 16385), (0, 1), (16384, T)]:
         gh, _ = lmh.lmhead_logprob_bwd(h[r0:r1], w, lab[r0:r1], g[r0:r1], 1.0)
         assert torch.equal(gh, gh_full[r0:r1]), (r0, r1)
     torch.cuda.synchronize()

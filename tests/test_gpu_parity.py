@@ -164,8 +164,8 @@ def test_fused_backward_matches_oracle(lmh, T, H, V, s, pass_lse):
 
 
 def test_fused_backward_several_row_chunks(lmh):
-    T, H, V = 8192 + 300, 136, 1500  # two row chunks, ragged second one
-    hidden, weight, labels, grad = fused_case(41, T, H, V, w_std=0.1, oov=[(8191, 5000)])
+    T, H, V = 16384 + 300, 136, 1500  # two row chunks, ragged second one
+    hidden, weight, labels, grad = fused_case(41, T, H, V, w_std=0.1, oov=[(16383, 5000)])
     gh, gw = _bwd(lmh, hidden, weight, labels, grad, S07)
     rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, S07)
     assert rel_frob(gh, rgh) < RTOL_FROB_GRAD
@@ -183,7 +183,7 @@ def test_fused_backward_all_out_of_vocab(lmh):
 
 
 @pytest.mark.parametrize("s", [1.0, S07])
-@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (3, 8, 16), (8192 + 40, 72, 700)])
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (3, 8, 16), (16384 + 40, 72, 700)])
 def test_entropy_backward_matches_oracle(lmh, T, H, V, s):
     import torch
 
