@@ -88,6 +88,11 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     assert _call_fwd(lib, wsb=16) == lmh.LMH_ERR_WORKSPACE
     assert _call_fwd(lib, ws=None) == lmh.LMH_ERR_WORKSPACE
     assert b"workspace" in lib.lmhead_last_error_string()
+    big = 2147483392 + 1  # one past LMH_MAX_DIM
+    assert _call_fwd(lib, T=big) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, V=big) == lmh.LMH_ERR_INVALID_ARG
+    assert _call_fwd(lib, H=big + 7) == lmh.LMH_ERR_INVALID_ARG  # a multiple of 8 past the limit
+    assert lmh.library().lmhead_workspace_size(lmh.LMH_OP_FWD, big, 256, 4096) == ctypes.c_size_t(-1).value
     assert _call_fwd(lib, T=0) == lmh.LMH_OK  # empty batch: nothing to do
     assert _call_fwd(lib, T=0, hidden=None, labels=None, lp=None, ws=None) == lmh.LMH_OK
     rc = lib.logprob_from_logits(24, 16, 4, 4096, 1.0, 16, None, None, None)
