@@ -185,12 +185,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t stage = 0, phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      int wave = 0;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++wave) {
         int m_tile, n_first, n_count, vunit;
         unit_coords(p, u, m_tile, n_first, n_count, vunit);
+        // grad_weight walks K (the rows) downwards on odd waves, so a wave
+        // starts on the operand rows the previous wave touched last, while
+        // they are still in L2.
+        const bool k_down = (E == (int)Epi::StoreF32T) && (wave & 1);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
-          for (int kb = 0; kb < kb_total; ++kb) {
+          for (int kstep = 0; kstep < kb_total; ++kstep) {
+            const int kb = k_down ? kb_total - 1 - kstep : kstep;
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
               ok = false;
               break;
