@@ -14,10 +14,14 @@ Prints ONE JSON line (rank 0). Besides the contract keys it carries:
   kernels        per-kernel average durations measured with CUDA events
   fwd_only       forward-only tokens/s of the same workload and of
                  T=4096 H=4096 V=32000
-  logits_path    the sampler formula on bf16 logits [8192, 152064] vs HBM
+  logits_path    the sampler formula on bf16 logits [8192, 152064] vs HBM,
+                 and its division (sampler-parity) form
+  sampler_parity fp32-bit mismatch counts against torch's fp32 sampler
+                 formula on [4096, 152064] logits
   cpu_baseline   the fp64 CPU oracle timed on a bounded sample on host cores
-  e2e            the same step through the binding with pinned host inputs
-                 copied in and log-probs/entropy copied out every step
+  e2e            the same step from pinned host inputs: the host-staged
+                 forward (copies overlapped with the forward) and the
+                 backward, log-probs/entropy copied back every step
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload on its
 own GPU (weak scaling, no data-path collective); the step time is the max over
@@ -308,6 +312,44 @@ def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
     return out
 
 
+def sampler_parity(lmh, x, lab):
+    """Row counts whose fp32 log-prob bits differ from torch's fp32 sampler
+    formula on the GPU (log_softmax of the fp32 logits divided by the
+    temperature, then gather), for the pages' 4096 x 152064 comparison: their
+    two unfused branches, and this library's multiplied and divided forms."""
+    import numpy as np
+    import torch
+
+    T = x.shape[0]
+    idx = lab.long()[:, None]
+
+    def sampler(t):
+        temps = torch.full((T,), t, dtype=torch.float32, device=x.device)
+        return torch.log_softmax(x.float() / temps[:, None], dim=-1).gather(1, idx)[:, 0]
+
+    def count(a, b):
+        return {"mismatched_rows": int((a.view(torch.int32) != b.view(torch.int32)).sum()),
+                "max_abs": float((a.double() - b.double()).abs().max())}
+
+    ref1 = sampler(1.0)
+    out = {"rows": T, "vocab": x.shape[1], "reference": "torch fp32 log_softmax(logits / t).gather",
+           "t=1": {
+               "torch_bf16_log_softmax": count(
+                   torch.log_softmax(x, dim=-1).gather(1, idx)[:, 0].float(), ref1),
+               "torch_gather_minus_logsumexp": count(
+                   x.float().gather(1, idx)[:, 0] - torch.logsumexp(x.float(), dim=-1), ref1),
+               "logprob_from_logits": count(lmh.logprob_from_logits(x, lab, 1.0)[0], ref1),
+               "logprob_from_logits_div": count(lmh.logprob_from_logits_div(x, lab, 1.0)[0],
+                                                ref1)}}
+    ref7 = sampler(0.7)
+    out["t=0.7"] = {
+        "logprob_from_logits (s = fp32(1/0.7))": count(
+            lmh.logprob_from_logits(x, lab, float(np.float32(1.0 / 0.7)))[0], ref7),
+        "logprob_from_logits_div": count(lmh.logprob_from_logits_div(x, lab, 0.7)[0], ref7)}
+    torch.cuda.synchronize()
+    return out
+
+
 def kernel_ms(lmh, fn, steps, warmup, names):
     """Average per-call device time of the named library kernels (CUDA events
     recorded by the library on the launching stream), excluding host gaps."""
@@ -470,20 +512,22 @@ def run_gpu(args):
     ent_host = torch.empty(T, dtype=torch.float32).pin_memory()
 
     def e2e_step():
-        hidden.copy_(h_host, non_blocking=True)
-        weight.copy_(w_host, non_blocking=True)
-        labels.copy_(l_host, non_blocking=True)
+        # host inputs in, host results out, through the library: the staged
+        # forward overlaps the weight's host-to-device copy with the forward
+        lmh.lmhead_logprob_fwd_host(h_host, w_host, l_host, s, hidden=hidden, weight=weight,
+                                    labels=labels, out_logprob=lp, out_entropy=ent, out_lse=lse,
+                                    out_logprob_host=lp_host, out_entropy_host=ent_host,
+                                    workspace=ws_f)
         grad.copy_(g_host, non_blocking=True)
-        fwd()
         bwd()
-        lp_host.copy_(lp, non_blocking=True)
-        ent_host.copy_(ent, non_blocking=True)
 
     barrier(ws)
     e2e_ms = reduce_max(timed(e2e_step, args.steps, 2) * args.steps, ws, dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_host, w_host, l_host, g_host))
     line["e2e"] = {"value": aggregate_tokens_per_s(T, ws, args.steps, e2e_ms), "unit": "tokens/s",
-                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 2 * T * 4}
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 2 * T * 4,
+                   "path": "lmhead_logprob_fwd_host (pinned host inputs, copies overlapped with "
+                           "the forward) + lmhead_logprob_bwd; logprob and entropy to host"}
     del h_host, w_host
 
     if ws == 1 and not args.no_extras:
@@ -537,6 +581,20 @@ def run_gpu(args):
                          "peak_source": f"hbm_gbs {peak_src}",
                          "traffic": traffic_for("logits_rowwise"),
                          "algorithmic_bytes_per_launch": T3 * V3 * 2}}
+        # sampler-parity (division) form on the same logits, and the mismatch
+        # counts against torch's own fp32 sampler formula on the GPU
+        temps = torch.full((T3,), 0.7, dtype=torch.float32, device=dev)
+        lmh.lmhead_timing_enable(True)
+        d_ms = timed(lambda: lmh.logprob_from_logits_div(x, l3, temps, out_logprob=lp3,
+                                                         out_entropy=ent3), args.steps, 3)
+        drec = [ms for name, ms in lmh.lmhead_timing_read() if name == "logits_rowwise_div"]
+        lmh.lmhead_timing_enable(False)
+        dk_ms = sum(drec) / len(drec)
+        dgbs = T3 * V3 * 2 / (dk_ms * 1e-3) / 1e9
+        extras["logits_path"]["division_form"] = {
+            "tokens_per_s": T3 / (d_ms * 1e-3), "ms": d_ms, "kernel_ms": dk_ms,
+            "achieved_gbs": round(dgbs, 1), "frac": round(dgbs / peaks["hbm_gbs"], 4)}
+        extras["sampler_parity"] = sampler_parity(lmh, x[:4096], l3[:4096])
         del x
         torch.cuda.empty_cache()
         line.update(extras)
@@ -553,7 +611,7 @@ def run_gpu(args):
 
 
 def run_case(args):
-    """One kernel family on one shape, for profiling: --case fwd|bwd|logits --shape ..."""
+    """One kernel family on one shape, for profiling: --case fwd|bwd|logits|logits_div --shape ..."""
     import torch
 
     import invariant_lm_head_gb300 as lmh
@@ -563,7 +621,7 @@ def run_case(args):
     lmh.build()
     dims = [int(x) for x in args.shape.split(",")]
     s = inv_temperature()
-    if args.case == "logits":
+    if args.case in ("logits", "logits_div"):
         T, V = dims
         g = torch.Generator(device=dev)
         g.manual_seed(7)
@@ -572,7 +630,13 @@ def run_case(args):
         lab = torch.randint(0, V, (T,), generator=g, device=dev, dtype=torch.int32)
         lp = torch.empty(T, device=dev)
         ent = torch.empty(T, device=dev)
-        fn = lambda: lmh.logprob_from_logits(x, lab, s, out_logprob=lp, out_entropy=ent)  # noqa: E731
+        if args.case == "logits":
+            fn = lambda: lmh.logprob_from_logits(x, lab, s, out_logprob=lp,  # noqa: E731
+                                                 out_entropy=ent)
+        else:
+            temps = torch.full((T,), 0.7, dtype=torch.float32, device=dev)
+            fn = lambda: lmh.logprob_from_logits_div(x, lab, temps, out_logprob=lp,  # noqa: E731
+                                                     out_entropy=ent)
         work = {"bytes": T * V * 2}
     else:
         T, H, V = dims
@@ -622,7 +686,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip fwd-only and logits-path legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits"], default=None,
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_div"], default=None,
                     help="time one entry point on --shape only (profiling aid; no contract line)")
     ap.add_argument("--shape", default="4096,4096,32000", help="T,H,V (fwd/bwd) or T,V (logits)")
     args = ap.parse_args(argv)

@@ -169,6 +169,63 @@ int logprob_from_logits_stats(const uint16_t* logits, const int32_t* labels, int
                               float* out_lse, float* out_sum_p2, struct CUstream_st* stream);
 
 /*
+ * Sampler-parity form of the sampler formula: the temperature is applied as
+ * an fp32 division of the fp32 logits, z = fp32(logits) / t, rounded to
+ * nearest as IEEE division is (verl page, temperature-order table: cast to
+ * fp32 first, then divide by the fp32 temperature), which is what an inference
+ * sampler computes when it divides the logits by a per-request temperature
+ * tensor. logprob_from_logits instead multiplies by an inverse temperature,
+ * which can differ from the division in the last bit of z.
+ *   temperature      t for every row (finite, > 0) when row_temperature is NULL
+ *   row_temperature  f32 [T] device array of per-row temperatures, or NULL;
+ *                    a row whose value is not finite and > 0 gets NaN outputs
+ *                    (the host cannot check device values)
+ *   out_sum_p2       f32 [T] or NULL, as in logprob_from_logits_stats
+ * Everything else (layouts, labels outside [0, V), errors, batch invariance)
+ * as logprob_from_logits.
+ */
+int logprob_from_logits_div(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                            float temperature, const float* row_temperature, float* out_logprob,
+                            float* out_entropy, float* out_lse, float* out_sum_p2,
+                            struct CUstream_st* stream);
+
+/*
+ * Forward from host memory: copies hidden, weight and labels from host
+ * buffers into the caller's device buffers and runs lmhead_logprob_fwd on
+ * them, with the host-to-device copies overlapped with the tensor-core work.
+ * The weight is copied in vocabulary slices (whole 1024-column chunks; the
+ * first small, later ones up to a quarter of V) on a copy stream, and the
+ * forward GEMM runs as one launch per slice, each after its slice has landed,
+ * so only the copy of hidden and of the first slice is exposed. An addition of
+ * this library for callers whose inputs live in host memory (an offloaded LM
+ * head, a host-side data loader); the pages have no counterpart.
+ *   hidden_host  bf16 [T, H], weight_host bf16 [V, H], labels_host int32 [T]:
+ *                host memory, page-locked for the copies to overlap (pageable
+ *                memory works but is copied synchronously by the driver)
+ *   hidden, weight, labels  device buffers of the same shapes, written by the
+ *                call (the backward can then run on them)
+ *   out_logprob_host, out_entropy_host  f32 [T] host buffers or NULL: filled
+ *                after the forward, in `stream` order (out_entropy_host needs
+ *                out_entropy)
+ *   copy_stream  stream for the host-to-device copies, or NULL for one the
+ *                library creates per device on first use
+ * Results are bit-identical to lmhead_logprob_fwd on the same data: every tile
+ * is computed as in the single launch. Ordering: the copies start after the
+ * work already enqueued on `stream` (an event recorded on `stream` at entry),
+ * and `stream` waits for every copy before the kernels that read it, so all of
+ * the call is ordered on `stream` as if it ran there. Nothing is allocated on
+ * the device; the library keeps a copy stream and a few events per device.
+ * Everything else (workspace, sizes, errors) as lmhead_logprob_fwd.
+ */
+int lmhead_logprob_fwd_host(const uint16_t* hidden_host, const uint16_t* weight_host,
+                            const int32_t* labels_host, int64_t T, int64_t H, int64_t V,
+                            float inv_temperature, uint16_t* hidden, uint16_t* weight,
+                            int32_t* labels, float* out_logprob, float* out_entropy,
+                            float* out_lse, float* out_logprob_host, float* out_entropy_host,
+                            void* workspace, size_t workspace_bytes, struct CUstream_st* stream,
+                            struct CUstream_st* copy_stream);
+
+/*
  * Forward without a workspace, for callers that cannot allocate device memory
  * (a plugin whose host framework owns all device memory and hands out no
  * workspace, or code that must not call cudaMalloc because it can block and
@@ -234,6 +291,16 @@ int lmhead_device_status(struct CUstream_st* stream, unsigned* bits);
  * No fault, trap or hang is involved.
  */
 int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
+
+/*
+ * Self-test of the division that logprob_from_logits_div applies: for every
+ * one of the 65536 bf16 bit patterns x, compares its quotient x / temperature
+ * with IEEE fp32 division (round to nearest) and stores in *mismatches the
+ * number of inputs whose result bits differ (NaN counts as equal to NaN);
+ * 0 means the division form is bit-exact for this temperature. Synchronises
+ * `stream`. Any temperature may be given, including 0, negative, inf or NaN.
+ */
+int lmhead_selftest_division(float temperature, int* mismatches, struct CUstream_st* stream);
 
 /*
  * The tensor-core engine alone, for engine tests: D[M, N] = sum_k A[m, k] B[n, k]

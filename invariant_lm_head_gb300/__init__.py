@@ -52,6 +52,9 @@ SIGNATURES = {
     "lmhead_logprob_fwd_stats": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P,
                                   ctypes.c_size_t, _P], ctypes.c_int),
     "logprob_from_logits_stats": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P, _P], ctypes.c_int),
+    "logprob_from_logits_div": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "lmhead_logprob_fwd_host": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 _P, ctypes.c_size_t, _P, _P], ctypes.c_int),
     "lmhead_last_error_string": ([], ctypes.c_char_p),
     "lmhead_abi_version": ([], ctypes.c_int),
     "lmhead_kernel_launches": ([], ctypes.c_ulonglong),
@@ -61,6 +64,7 @@ SIGNATURES = {
     "lmhead_timing_kind_name": ([ctypes.c_int], ctypes.c_char_p),
     "lmhead_device_status": ([_P, ctypes.POINTER(ctypes.c_uint)], ctypes.c_int),
     "lmhead_selftest_wait_timeout": ([ctypes.c_uint64, _P], ctypes.c_int),
+    "lmhead_selftest_division": ([_F, ctypes.POINTER(ctypes.c_int), _P], ctypes.c_int),
     "lmhead_engine_gemm": ([_P, _P, _I64, _I64, _I64, ctypes.c_int, _P, _P], ctypes.c_int),
     "lmhead_logprob_entropy_bwd": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P,
                                     ctypes.c_size_t, _P], ctypes.c_int),
@@ -159,6 +163,54 @@ def lmhead_logprob_fwd_stats(hidden, weight, labels, inv_temperature: float = 1.
     """Fused forward with sum_pi_squared. Returns (logprob, entropy, lse, sum_p2)."""
     return _fwd("lmhead_logprob_fwd_stats", hidden, weight, labels, inv_temperature, out_logprob,
                 out_entropy, out_lse, out_sum_p2, want_entropy, want_lse, True, workspace, stream)
+
+
+def lmhead_logprob_fwd_host(hidden_host, weight_host, labels_host, inv_temperature: float = 1.0,
+                            *, hidden, weight, labels, out_logprob=None, out_entropy=None,
+                            out_lse=None, out_logprob_host=None, out_entropy_host=None,
+                            want_entropy: bool = True, want_lse: bool = True, workspace=None,
+                            stream=None, copy_stream=None):
+    """Fused forward from host inputs, copies overlapped with the forward.
+
+    hidden_host, weight_host, labels_host are CPU tensors (page-locked for the
+    copies to overlap); hidden, weight, labels are device tensors of the same
+    shapes that the call fills. out_logprob_host / out_entropy_host (CPU f32
+    [T] or None) receive the results in stream order. copy_stream is a
+    torch.cuda.Stream or None (the library's own). Returns (logprob, entropy
+    or None, lse or None) on the device.
+    """
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight, "weight", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    cpu = torch.device("cpu")
+    _need(hidden_host, "hidden_host", torch.bfloat16, cpu, 2)
+    _need(weight_host, "weight_host", torch.bfloat16, cpu, 2)
+    _need(labels_host, "labels_host", torch.int32, cpu, 1)
+    T, H = hidden.shape
+    V = weight.shape[0]
+    if (tuple(hidden_host.shape) != (T, H) or tuple(weight_host.shape) != (V, H)
+            or weight.shape[1] != H or labels.shape[0] != T or labels_host.shape[0] != T):
+        raise ValueError("shape mismatch between the host and device inputs")
+    for t, n in ((out_logprob_host, "out_logprob_host"), (out_entropy_host, "out_entropy_host")):
+        if t is not None:
+            _need(t, n, torch.float32, cpu, 1)
+    if out_logprob is None:
+        out_logprob = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_entropy is None and (want_entropy or out_entropy_host is not None):
+        out_entropy = torch.empty(T, dtype=torch.float32, device=dev)
+    if out_lse is None and want_lse:
+        out_lse = torch.empty(T, dtype=torch.float32, device=dev)
+    ws, ws_bytes = _workspace(LMH_OP_FWD, T, H, V, workspace, dev)
+    cs = None if copy_stream is None else ctypes.c_void_p(copy_stream.cuda_stream)
+    rc = library().lmhead_logprob_fwd_host(
+        _ptr(hidden_host), _ptr(weight_host), _ptr(labels_host), T, H, V, float(inv_temperature),
+        _ptr(hidden), _ptr(weight), _ptr(labels), _ptr(out_logprob), _ptr(out_entropy),
+        _ptr(out_lse), _ptr(out_logprob_host), _ptr(out_entropy_host), _ptr(ws), ws_bytes,
+        _stream_ptr(stream), cs)
+    _check("lmhead_logprob_fwd_host", rc)
+    return out_logprob, out_entropy, out_lse
 
 
 def _fwd(name, hidden, weight, labels, inv_temperature, out_logprob, out_entropy, out_lse,
@@ -260,8 +312,32 @@ def logprob_from_logits_stats(logits, labels, inv_temperature: float = 1.0, *, o
                    out_entropy, out_lse, out_sum_p2, want_entropy, want_lse, True, stream)
 
 
+def logprob_from_logits_div(logits, labels, temperature=1.0, *, out_logprob=None,
+                            out_entropy=None, out_lse=None, out_sum_p2=None,
+                            want_entropy: bool = True, want_lse: bool = False,
+                            want_sum_p2: bool = False, stream=None):
+    """Sampler formula with the temperature as an fp32 division, z = logits / t.
+
+    temperature is a float (one t for every row) or an f32 tensor [T] of
+    per-row temperatures on the logits' device. Returns (logprob, entropy,
+    lse, sum_p2), the ones not asked for None.
+    """
+    torch = _torch()
+    row_t = None
+    t = 1.0
+    if isinstance(temperature, torch.Tensor):
+        _need(temperature, "temperature", torch.float32, logits.device, 1)
+        if temperature.shape[0] != logits.shape[0]:
+            raise ValueError("temperature must have one value per row")
+        row_t = temperature
+    else:
+        t = float(temperature)
+    return _logits("logprob_from_logits_div", logits, labels, t, out_logprob, out_entropy,
+                   out_lse, out_sum_p2, want_entropy, want_lse, want_sum_p2, stream, row_t=row_t)
+
+
 def _logits(name, logits, labels, inv_temperature, out_logprob, out_entropy, out_lse, out_sum_p2,
-            want_entropy, want_lse, want_sum_p2, stream):
+            want_entropy, want_lse, want_sum_p2, stream, row_t=None):
     torch = _torch()
     dev = logits.device
     _need(logits, "logits", torch.bfloat16, dev, 2)
@@ -275,9 +351,11 @@ def _logits(name, logits, labels, inv_temperature, out_logprob, out_entropy, out
         out_lse = torch.empty(T, dtype=torch.float32, device=dev)
     if out_sum_p2 is None and want_sum_p2:
         out_sum_p2 = torch.empty(T, dtype=torch.float32, device=dev)
-    args = [_ptr(logits), _ptr(labels), T, V, float(inv_temperature), _ptr(out_logprob),
-            _ptr(out_entropy), _ptr(out_lse)]
-    if name == "logprob_from_logits_stats":
+    args = [_ptr(logits), _ptr(labels), T, V, float(inv_temperature)]
+    if name == "logprob_from_logits_div":
+        args.append(_ptr(row_t))
+    args += [_ptr(out_logprob), _ptr(out_entropy), _ptr(out_lse)]
+    if name in ("logprob_from_logits_stats", "logprob_from_logits_div"):
         args.append(_ptr(out_sum_p2))
     rc = getattr(library(), name)(*args, _stream_ptr(stream))
     _check(name, rc)
@@ -315,6 +393,16 @@ def lmhead_device_status(stream=None) -> int:
 def lmhead_selftest_wait_timeout(limit_ns: int = 1_000_000, stream=None) -> int:
     """Run the bounded-wait self-test; returns the library's status code (6 expected)."""
     return library().lmhead_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
+
+
+def lmhead_selftest_division(temperature: float, stream=None) -> int:
+    """Number of bf16 inputs whose quotient in the division form differs from
+    IEEE fp32 division by ``temperature`` (0 = bit-exact)."""
+    n = ctypes.c_int(-1)
+    _check("lmhead_selftest_division",
+           library().lmhead_selftest_division(float(temperature), ctypes.byref(n),
+                                              _stream_ptr(stream)))
+    return int(n.value)
 
 
 def lmhead_engine_gemm(A, B, out=None, a_kmajor: bool = True, b_kmajor: bool = True,

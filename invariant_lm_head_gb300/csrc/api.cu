@@ -1,6 +1,7 @@
 // C ABI of liblmhead.so: argument checks, workspace layout, TMA descriptors
 // and the launch sequence of each entry point. Declarations and contracts are
 // in include/lmhead.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -249,11 +250,12 @@ enum Kind : int {
   K_LOGITS_ROWWISE,
   K_ENGINE_GEMM,
   K_SELFTEST,
+  K_LOGITS_ROWWISE_DIV,
   K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {
-    "fused_fwd_gemm",   "fwd_merge",      "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm",
-    "logits_rowwise",   "engine_gemm",    "selftest_wait"};
+    "fused_fwd_gemm", "fwd_merge",   "dlogits_gemm",  "grad_hidden_gemm",  "grad_weight_gemm",
+    "logits_rowwise", "engine_gemm", "selftest_wait", "logits_rowwise_div"};
 
 struct TimingRec {
   int kind;
@@ -302,11 +304,20 @@ struct KernelTimer {
     if (_rc != LMH_OK) return _rc;                        \
   } while (0)
 
+// A run of vocab units [begin, end) of the forward GEMM; `ready` (or NULL) is
+// an event the launch waits for first.
+struct FwdSlice {
+  int begin, end;
+  cudaEvent_t ready;
+};
+
 // Forward statistics into `w`, merged into the outputs. out_sum_p2 may be NULL.
+// With `slices`, the forward GEMM runs as one launch per slice, each after its
+// event; every tile is computed exactly as in the single launch.
 int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* weight,
                 const int32_t* labels, int64_t T, int64_t H, int64_t V, float s, float* out_lp,
                 float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st,
-                float* out_sum_p2 = nullptr) {
+                float* out_sum_p2 = nullptr, const std::vector<FwdSlice>* slices = nullptr) {
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
   LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
@@ -324,9 +335,25 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_q = out_sum_p2 ? w.pq : nullptr;
   p.part_zl = w.pzl;
   p.part_ld = T;
-  LMH_LAUNCH(K_FWD_GEMM, st,
-             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
-             "fused forward");
+  if (!slices) {
+    LMH_LAUNCH(K_FWD_GEMM, st,
+               lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
+               "fused forward");
+  } else {
+    for (const FwdSlice& sl : *slices) {
+      if (sl.ready) {
+        const cudaError_t e = cudaStreamWaitEvent(st, sl.ready, 0);
+        if (e != cudaSuccess)
+          return fail(LMH_ERR_LAUNCH, "cudaStreamWaitEvent: %s", cudaGetErrorString(e));
+      }
+      p.vunit_begin = sl.begin;
+      p.vunit_end = sl.end;
+      LMH_LAUNCH(K_FWD_GEMM, st,
+                 lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms,
+                                  st),
+                 "fused forward (vocab slice)");
+    }
+  }
   LMH_LAUNCH(K_FWD_MERGE, st,
              lmh::launch_fwd_merge(w.pm, w.ps, w.pu, out_sum_p2 ? w.pq : nullptr, w.pzl, labels, T,
                                    n_fwd_chunks(V), V, out_lp, out_ent, out_lse, out_sum_p2, st),
@@ -362,12 +389,21 @@ int fwd_entry(const uint16_t* hidden, const uint16_t* weight, const int32_t* lab
   return ok();
 }
 
+// divide == false: temp_value is the inverse temperature s (z = x * s).
+// divide == true: temp_value is the temperature t (z = x / t), or each row's
+// t comes from row_temperature when that is not NULL.
 int logits_entry(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
-                 float inv_temperature, float* out_logprob, float* out_entropy, float* out_lse,
-                 float* out_sum_p2, struct CUstream_st* stream) {
+                 float temp_value, bool divide, const float* row_temperature, float* out_logprob,
+                 float* out_entropy, float* out_lse, float* out_sum_p2,
+                 struct CUstream_st* stream) {
   LMH_TRY(check_dims(T, 8, V, false));
-  LMH_TRY(check_temperature(inv_temperature));
+  if (!row_temperature) {
+    if (!std::isfinite(temp_value) || !(temp_value > 0.f))
+      return fail(LMH_ERR_INVALID_ARG, "%s must be finite and > 0",
+                  divide ? "temperature" : "inv_temperature");
+  }
   if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
+  LMH_TRY(check_ptr(row_temperature, 4, "row_temperature", true));
   LMH_TRY(check_ptr(logits, (V % 8 == 0) ? 16 : 2, "logits"));
   LMH_TRY(check_ptr(labels, 4, "labels"));
   LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
@@ -377,12 +413,63 @@ int logits_entry(const uint16_t* logits, const int32_t* labels, int64_t T, int64
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_LOGITS_ROWWISE, st,
-             lmh::launch_logits_logprob(logits, labels, T, V, inv_temperature, out_logprob,
-                                        out_entropy, out_lse, out_sum_p2, dev->sms, dev->status,
-                                        st),
+  LMH_LAUNCH(divide ? K_LOGITS_ROWWISE_DIV : K_LOGITS_ROWWISE, st,
+             lmh::launch_logits_logprob(logits, labels, T, V, temp_value, divide,
+                                        row_temperature, out_logprob, out_entropy, out_lse,
+                                        out_sum_p2, dev->sms, dev->status, st),
              "logits log-prob");
   return ok();
+}
+
+// ------------------------------------------------------------ host-staged forward
+// Per device: a copy stream of the library's own (non-blocking, created on
+// first use) and a pool of events. Events are reused from call to call: a
+// stream wait takes the record that is current when it is enqueued, so a later
+// record cannot disturb an earlier wait. The mutex keeps one call's records and
+// waits together when several host threads call at once.
+struct Staging {
+  cudaStream_t copy = nullptr;
+  std::vector<cudaEvent_t> events;
+  std::mutex mu;
+};
+Staging g_staging[kMaxDevices];
+
+int staging_events(Staging& sg, size_t n) {
+  while (sg.events.size() < n) {
+    cudaEvent_t e = nullptr;
+    const cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (r != cudaSuccess) return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(r));
+    sg.events.push_back(e);
+  }
+  return LMH_OK;
+}
+
+// Vocab slices of the staged forward, in 1024-column units: the first small,
+// so the tensor cores start soon after the first copies land, then doubling up
+// to a quarter of the vocabulary; a tail shorter than the first slice joins
+// the slice before it. Copies run several times faster than the forward
+// consumes the weight, so only the first slice's copy is exposed.
+std::vector<FwdSlice> staged_slices(int n_vunits) {
+  std::vector<FwdSlice> out;
+  const int first = n_vunits < 16 ? 1 : (n_vunits + 15) / 16;
+  const int cap = std::max(first, (n_vunits + 3) / 4);
+  int b = 0, size = first;
+  while (b < n_vunits) {
+    int e = std::min(n_vunits, b + size);
+    if (n_vunits - e > 0 && n_vunits - e < first) e = n_vunits;
+    out.push_back(FwdSlice{b, e, nullptr});
+    b = e;
+    size = std::min(cap, size * 2);
+  }
+  return out;
+}
+
+int copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t st,
+               const char* what) {
+  if (bytes == 0) return LMH_OK;
+  const cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, st);
+  if (e != cudaSuccess) return fail(LMH_ERR_LAUNCH, "copy of %s: %s", what, cudaGetErrorString(e));
+  return LMH_OK;
 }
 
 // Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
@@ -621,15 +708,93 @@ int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
 int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
                         float inv_temperature, float* out_logprob, float* out_entropy,
                         float* out_lse, struct CUstream_st* stream) {
-  return logits_entry(logits, labels, T, V, inv_temperature, out_logprob, out_entropy, out_lse,
-                      nullptr, stream);
+  return logits_entry(logits, labels, T, V, inv_temperature, false, nullptr, out_logprob,
+                      out_entropy, out_lse, nullptr, stream);
 }
 
 int logprob_from_logits_stats(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
                               float inv_temperature, float* out_logprob, float* out_entropy,
                               float* out_lse, float* out_sum_p2, struct CUstream_st* stream) {
-  return logits_entry(logits, labels, T, V, inv_temperature, out_logprob, out_entropy, out_lse,
-                      out_sum_p2, stream);
+  return logits_entry(logits, labels, T, V, inv_temperature, false, nullptr, out_logprob,
+                      out_entropy, out_lse, out_sum_p2, stream);
+}
+
+int logprob_from_logits_div(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                            float temperature, const float* row_temperature, float* out_logprob,
+                            float* out_entropy, float* out_lse, float* out_sum_p2,
+                            struct CUstream_st* stream) {
+  return logits_entry(logits, labels, T, V, temperature, true, row_temperature, out_logprob,
+                      out_entropy, out_lse, out_sum_p2, stream);
+}
+
+int lmhead_logprob_fwd_host(const uint16_t* hidden_host, const uint16_t* weight_host,
+                            const int32_t* labels_host, int64_t T, int64_t H, int64_t V,
+                            float inv_temperature, uint16_t* hidden, uint16_t* weight,
+                            int32_t* labels, float* out_logprob, float* out_entropy,
+                            float* out_lse, float* out_logprob_host, float* out_entropy_host,
+                            void* workspace, size_t workspace_bytes, struct CUstream_st* stream,
+                            struct CUstream_st* copy_stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(inv_temperature));
+  if (T == 0) return ok();  // nothing to copy, read or write; pointers may be NULL
+  if (!hidden_host || !weight_host || !labels_host)
+    return fail(LMH_ERR_INVALID_ARG, "a host input pointer is NULL");
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  if (out_entropy_host && !out_entropy)
+    return fail(LMH_ERR_INVALID_ARG, "out_entropy_host needs out_entropy");
+  const size_t need = lmhead_workspace_size(LMH_OP_FWD, T, H, V);
+  if (!workspace || workspace_bytes < need)
+    return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
+  LMH_TRY(check_ptr(workspace, 16, "workspace"));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  Staging& sg = g_staging[dev_id];
+  std::lock_guard<std::mutex> lk(sg.mu);
+  cudaError_t e;
+  if (!sg.copy && (e = cudaStreamCreateWithFlags(&sg.copy, cudaStreamNonBlocking)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaStreamCreate: %s", cudaGetErrorString(e));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t cs = copy_stream ? reinterpret_cast<cudaStream_t>(copy_stream) : sg.copy;
+
+  std::vector<FwdSlice> slices = staged_slices(n_fwd_chunks(V));
+  LMH_TRY(staging_events(sg, slices.size() + 1));
+  // The copies may overwrite the device inputs only after the caller's
+  // earlier work on `stream` is done with them.
+  if ((e = cudaEventRecord(sg.events[0], st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(cs, sg.events[0], 0)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "stream ordering: %s", cudaGetErrorString(e));
+  LMH_TRY(copy_async(hidden, hidden_host, static_cast<size_t>(T * H) * 2, cudaMemcpyHostToDevice,
+                     cs, "hidden"));
+  LMH_TRY(copy_async(labels, labels_host, static_cast<size_t>(T) * 4, cudaMemcpyHostToDevice, cs,
+                     "labels"));
+  const int64_t unit_cols = static_cast<int64_t>(lmh::kBN) * lmh::kFwdTilesPerChunk;
+  for (size_t i = 0; i < slices.size(); ++i) {
+    const int64_t r0 = slices[i].begin * unit_cols;
+    const int64_t r1 = std::min<int64_t>(V, slices[i].end * unit_cols);
+    LMH_TRY(copy_async(weight + r0 * H, weight_host + r0 * H, static_cast<size_t>((r1 - r0) * H) * 2,
+                       cudaMemcpyHostToDevice, cs, "weight"));
+    slices[i].ready = sg.events[1 + i];
+    if ((e = cudaEventRecord(slices[i].ready, cs)) != cudaSuccess)
+      return fail(LMH_ERR_LAUNCH, "cudaEventRecord: %s", cudaGetErrorString(e));
+  }
+  Carver c{static_cast<char*>(workspace)};
+  const FwdWs w = carve_fwd(c, T, V);
+  LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, inv_temperature, out_logprob,
+                      out_entropy, out_lse, w, st, nullptr, &slices));
+  if (out_logprob_host)
+    LMH_TRY(copy_async(out_logprob_host, out_logprob, static_cast<size_t>(T) * 4,
+                       cudaMemcpyDeviceToHost, st, "logprob"));
+  if (out_entropy_host)
+    LMH_TRY(copy_async(out_entropy_host, out_entropy, static_cast<size_t>(T) * 4,
+                       cudaMemcpyDeviceToHost, st, "entropy"));
+  return ok();
 }
 
 int lmhead_device_status(struct CUstream_st* stream, unsigned* bits) {
@@ -665,6 +830,25 @@ int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) 
     return fail(LMH_ERR_LAUNCH, "wait self-test: %s", cudaGetErrorString(e));
   if (result == 0) return fail(LMH_ERR_DEVICE_TIMEOUT, "bounded wait gave up as expected");
   return fail(LMH_ERR_LAUNCH, "bounded wait self-test: unexpected result %d", result);
+}
+
+int lmhead_selftest_division(float temperature, int* mismatches, struct CUstream_st* stream) {
+  if (!mismatches) return fail(LMH_ERR_INVALID_ARG, "mismatches is NULL");
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(dev->selftest, 0, sizeof(int), st)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "division self-test: %s", cudaGetErrorString(e));
+  LMH_LAUNCH(K_SELFTEST, st, lmh::launch_division_selftest(temperature, dev->selftest, st),
+             "division self-test");
+  int count = -1;
+  if ((e = cudaMemcpyAsync(&count, dev->selftest, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "division self-test: %s", cudaGetErrorString(e));
+  *mismatches = count;
+  return ok();
 }
 
 int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t N, int64_t K,

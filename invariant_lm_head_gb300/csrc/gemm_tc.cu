@@ -34,12 +34,14 @@
 //              accumulated over row chunks in ascending order. Taking the
 //              small hidden operand as A keeps it resident in L2 while dl
 //              streams through once.
-//   StoreF32   D = A * B^T in fp32 (the bare engine GEMM; A = dl and B = hidden read
-//              MN-major) in fp32, accumulated over row chunks in ascending order.
+//   StoreF32   D = A * B^T in fp32, row-major (the bare engine GEMM).
 //
-// Batch invariance: K is walked in the same order for every tile, the work
-// split depends only on N (vocab) and never on M (rows), each row is reduced
-// by one thread in a fixed column order, and there are no atomics.
+// Batch invariance: the work split depends only on N (vocab) and never on M
+// (rows), each row is reduced by one thread in a fixed column order, there are
+// no atomics, and the forward, dlogits and grad_hidden contractions walk K in
+// ascending order for every tile. grad_weight, a sum over rows that no row's
+// output depends on, walks K downwards on a CTA's odd waves for L2 reuse; its
+// bits are fixed by the inputs, the row chunking and the SM count.
 #include <cfloat>
 #include <cstdint>
 
@@ -76,8 +78,9 @@ __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_t
   const int first_m = g * p.group_m;
   const int gm = min(p.group_m, p.n_m_tiles - first_m);
   const int r = u - g * per_group;
-  vunit = r / gm;
-  m_tile = first_m + (r - vunit * gm);
+  const int vu = r / gm;
+  m_tile = first_m + (r - vu * gm);
+  vunit = p.vunit_begin + vu;
   n_first = vunit * p.tiles_per_unit;
   n_count = min(p.tiles_per_unit, p.n_n_tiles - n_first);
 }
@@ -460,7 +463,10 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   p.n_m_tiles = (p.M + kBM - 1) / kBM;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
   p.tiles_per_unit = tiles_per_unit;
-  p.n_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
+  const int all_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
+  const int vu_end = (p.vunit_end > 0 && p.vunit_end < all_vunits) ? p.vunit_end : all_vunits;
+  if (p.vunit_begin < 0 || p.vunit_begin > vu_end) return cudaErrorInvalidValue;
+  p.n_vunits = vu_end - p.vunit_begin;
   p.n_units = p.n_m_tiles * p.n_vunits;
   // m tiles per raster group, per contraction (same-session sweep of 4/8/16/32
   // on the Qwen-like step): the N = V contractions (forward, dlogits) share W

@@ -36,6 +36,10 @@ struct GemmParams {
   int M, N, K;  // D[M, N] = sum_k A[m, k] * B[n, k]
   int a_mn, b_mn;  // 1 = operand stored MN-major ([K][M] / [K][N])
   int n_m_tiles, n_n_tiles, tiles_per_unit, n_vunits, n_units, group_m;
+  // Vocab units [vunit_begin, vunit_end) of N taken by this launch (vunit_end
+  // 0 = to the end); launch_gemm turns them into n_vunits, and a unit's vocab
+  // unit index stays global, so partials land in their usual planes.
+  int vunit_begin, vunit_end;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -82,12 +86,20 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
                         const CUtensorMap* c = nullptr);
 
 // out_sum_p2 may be NULL; when it is not, sum_v p^2 is accumulated too.
+// temp_value is the inverse temperature (divide == false: z = x * s) or the
+// temperature (divide == true: z = x / t, IEEE fp32 division); with divide,
+// row_temperature (f32 [T] or NULL) gives each row its own t.
 cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
-                                  int64_t V, float inv_temperature, float* out_logprob,
+                                  int64_t V, float temp_value, bool divide,
+                                  const float* row_temperature, float* out_logprob,
                                   float* out_entropy, float* out_lse, float* out_sum_p2,
                                   int num_sms, unsigned* status, cudaStream_t stream);
 
 // pq and out_sum_p2 may be NULL (both or neither).
+// Counts (into *mismatches, which the caller zeroes) the bf16 inputs x whose
+// quotient x / t in the logits path differs from IEEE fp32 division.
+cudaError_t launch_division_selftest(float t, int* mismatches, cudaStream_t stream);
+
 cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pq,
                              const float* pzl, const int32_t* labels, int64_t T, int n_vunits,
                              int64_t V, float* out_logprob, float* out_entropy, float* out_lse,

@@ -86,18 +86,134 @@ __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], i
   st.m = mn;
 }
 
-// Fold 32 bf16 values, given as 4 x 16-byte words (8 values each, of which
-// the first nv words are valid), scaled by c > 0, into the state. Same
-// statistics as stat_fold on y = x * c, in fewer instructions: the max is taken
-// on the raw bf16 pairs (exact, and max commutes with the positive scale), and
-// the scale and the max shift are one FMA, d = x * c - m. Every operation is
-// still an explicit round-to-nearest intrinsic in a fixed order.
+// How a bf16 logit x becomes y = z * log2(e), z the temperature-scaled logit.
+// ScaleMul multiplies by the inverse temperature s, folded with log2(e) into one
+// factor c = s * log2(e): y = x * c, and the shifted value y - m is one FMA.
+// ScaleDiv divides by the temperature t, z = x / t rounded to nearest exactly
+// as IEEE fp32 division rounds it, then y = z * log2(e): the fp32 logits
+// divided by an fp32 temperature, as the verl page's temperature-order table
+// requires and as a sampler that divides by a per-request temperature tensor
+// computes it. Both maps are non-decreasing in x (t, c > 0), so the maximum of
+// y is the map of the maximum of x.
 __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <bool kQ>
+struct ScaleMul {
+  float c;
+  __device__ __forceinline__ float y(float x) const { return __fmul_rn(x, c); }
+  // Every group takes the one-FMA path.
+  __device__ __forceinline__ bool group_fast(const uint4 (&)[4], int) const { return true; }
+  // d[2i], d[2i+1] = the shifted values y - m of the low and high bf16 of
+  // word i (8 values per 16-byte word, words of w in order).
+  __device__ __forceinline__ void shift_fast(const uint4 (&w)[4], float neg_m,
+                                             float (&d)[32]) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        d[8 * k + 2 * q] = __fmaf_rn(bf16_lo_f(ws[q]), c, neg_m);
+        d[8 * k + 2 * q + 1] = __fmaf_rn(bf16_hi_f(ws[q]), c, neg_m);
+      }
+    }
+  }
+  __device__ __forceinline__ void shift_exact(const uint4 (&w)[4], int, float neg_m,
+                                              float (&d)[32]) const {
+    shift_fast(w, neg_m, d);
+  }
+};
+
+// IEEE fp32 division, kept out of line so the rare callers add no code to the
+// unrolled folds.
+static __device__ __noinline__ float div_ieee(float x, float t) { return __fdiv_rn(x, t); }
+
+// The quotient uses Markstein's correction of a reciprocal product (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with r = 1/t rounded to nearest,
+// q0 = x * r rounded, the remainder q0 * t - x is exact in one FMA, and
+// q0 - rem * r rounded once is the correctly rounded quotient. Taking the
+// remainder with this sign also gives -0 for x = -0. The fast path holds for
+// t in [2^-20, 2^20] and x = 0 or |x| in [2^-100, 2^100], where every
+// intermediate is exact or a normal fp32 number, so the result scales exactly
+// with the exponents of x and t. It was checked by exact arithmetic for every
+// bf16 significand against every fp32 temperature significand and for every
+// bf16 input in that range at 2000 temperatures, and on the GPU against IEEE
+// division for every bf16 input (the library's lmhead_selftest_division).
+// Other inputs (tiny or huge |x|, inf, extreme t) take the IEEE division.
+struct ScaleDiv {
+  float t;
+  float r;  // 1/t rounded to nearest, or 0 when t is outside [2^-20, 2^20]
+  __device__ __forceinline__ static ScaleDiv make(float temperature) {
+    ScaleDiv d;
+    d.t = temperature;
+    d.r = (temperature >= 0x1p-20f && temperature <= 0x1p20f) ? __frcp_rn(temperature) : 0.f;
+    return d;
+  }
+  __device__ __forceinline__ float fast_quotient(float x) const {
+    const float q0 = __fmul_rn(x, r);
+    const float nrem = __fmaf_rn(q0, t, -x);
+    return __fmaf_rn(-nrem, r, q0);
+  }
+  __device__ __forceinline__ float quotient(float x) const {
+    const float ax = fabsf(x);
+    if (r != 0.f && (ax == 0.f || (ax >= 0x1p-100f && ax <= 0x1p100f))) return fast_quotient(x);
+    return div_ieee(x, t);
+  }
+  __device__ __forceinline__ float y(float x) const { return __fmul_rn(quotient(x), kLog2e); }
+  // True when every value of the first nv words is in the fast path's range
+  // (a group holding a zero is sent to shift_exact too, which is exact for it).
+  __device__ __forceinline__ bool group_fast(const uint4 (&w)[4], int nv) const {
+    if (r == 0.f) return false;
+    __nv_bfloat162 amax = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0].x));
+    __nv_bfloat162 amin = amax;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < nv) {
+        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const __nv_bfloat162 a = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&ws[q]));
+          amax = __hmax2(amax, a);
+          amin = __hmin2(amin, a);
+        }
+      }
+    }
+    const float lo = fminf(__low2float(amin), __high2float(amin));
+    const float hi = fmaxf(__low2float(amax), __high2float(amax));
+    return lo >= 0x1p-100f && hi <= 0x1p100f;
+  }
+  // d = z * log2(e) - m in one FMA, z = x / t.
+  __device__ __forceinline__ void shift_fast(const uint4 (&w)[4], float neg_m,
+                                             float (&d)[32]) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        d[8 * k + 2 * q] = __fmaf_rn(fast_quotient(bf16_lo_f(ws[q])), kLog2e, neg_m);
+        d[8 * k + 2 * q + 1] = __fmaf_rn(fast_quotient(bf16_hi_f(ws[q])), kLog2e, neg_m);
+      }
+    }
+  }
+  __device__ __forceinline__ void shift_exact(const uint4 (&w)[4], int nv, float neg_m,
+                                              float (&d)[32]) const {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < nv) {
+        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          d[8 * k + 2 * q] = __fmaf_rn(quotient(bf16_lo_f(ws[q])), kLog2e, neg_m);
+          d[8 * k + 2 * q + 1] = __fmaf_rn(quotient(bf16_hi_f(ws[q])), kLog2e, neg_m);
+        }
+      }
+    }
+  }
+};
+
+template <bool kQ, class S>
 __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&w)[4], int nv,
-                                                  float c) {
+                                                  const S& sc) {
   __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0].x);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -109,25 +225,28 @@ __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&
     }
   }
   const float gmax = fmaxf(__low2float(m2), __high2float(m2));
-  const float mn = fmaxf(st.m, __fmul_rn(gmax, c));
+  const float mn = fmaxf(st.m, sc.y(gmax));
   const float d0 = __fsub_rn(st.m, mn);
   const float a = ex2(d0);
   const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
   const float s = __fmul_rn(st.s, a);
-  const float nmn = -mn;
+  float d[32];
+  if (sc.group_fast(w, nv))
+    sc.shift_fast(w, -mn, d);
+  else
+    sc.shift_exact(w, nv, -mn, d);
   float s0 = 0.f, s1 = 0.f, u0 = 0.f, u1 = 0.f, q0 = 0.f, q1 = 0.f;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k < nv) {
-      const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float da = __fmaf_rn(bf16_lo_f(ws[q]), c, nmn);
+        const float da = d[8 * k + 2 * q];
         const float ea = ex2(da);
         s0 = __fadd_rn(s0, ea);
         u0 = __fmaf_rn(ea, da, u0);
         if (kQ) q0 = __fmaf_rn(ea, ea, q0);
-        const float db = __fmaf_rn(bf16_hi_f(ws[q]), c, nmn);
+        const float db = d[8 * k + 2 * q + 1];
         const float eb = ex2(db);
         s1 = __fadd_rn(s1, eb);
         u1 = __fmaf_rn(eb, db, u1);

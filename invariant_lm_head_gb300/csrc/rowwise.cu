@@ -1,7 +1,8 @@
 // Memory-bound kernels of the LM-head library (sm_103a):
 //   * the sampler formula on materialised bf16 logits (one streaming pass per
-//     row: fp32 scale by the temperature factor, online max / sum-exp /
-//     entropy accumulator, optionally sum p^2, label gather),
+//     row: fp32 scale by the inverse temperature, or fp32 division by a
+//     scalar or per-row temperature; online max / sum-exp / entropy
+//     accumulator, optionally sum p^2; label gather),
 //   * the fixed-order merge of the fused forward's per-vocab-chunk partials,
 //   * a self-test of the bounded wait (a barrier that nothing completes).
 //
@@ -55,6 +56,24 @@ __device__ __forceinline__ OnlineStat cta_reduce(OnlineStat st, OnlineStat* sh) 
   return r;
 }
 
+// The temperature map of one row: ScaleMul from the folded factor, ScaleDiv
+// from the row's own temperature when a per-row array is given. A row
+// temperature that is not finite and > 0 becomes NaN, so that row's outputs
+// are NaN and no other row is affected.
+template <class S>
+__device__ __forceinline__ S row_scale(float tparam, const float* row_t, int64_t row);
+template <>
+__device__ __forceinline__ ScaleMul row_scale<ScaleMul>(float tparam, const float*, int64_t) {
+  return ScaleMul{tparam};
+}
+template <>
+__device__ __forceinline__ ScaleDiv row_scale<ScaleDiv>(float tparam, const float* row_t,
+                                                        int64_t row) {
+  float t = row_t ? row_t[row] : tparam;
+  if (!(t > 0.f && t <= 3.402823466e38f)) t = __int_as_float(0x7fffffff);
+  return ScaleDiv::make(t);
+}
+
 __device__ __forceinline__ void write_row_outputs(int64_t row, const OnlineStat& st, float y_label,
                                                   bool label_ok, float* out_lp, float* out_ent,
                                                   float* out_lse, float* out_sum_p2) {
@@ -81,11 +100,12 @@ static_assert(kLVecPerThread == 4, "stat_fold_bf16x32 folds four 16-byte words p
 constexpr int kLStages = 6;
 constexpr int kLSmemBytes = kLStages * kLChunkBytes + 1024;
 
-template <bool kQ>
+template <bool kQ, class S>
 __global__ void __launch_bounds__(kLThreads, 2)
     logits_logprob_tma_kernel(const uint16_t* __restrict__ logits,
                               const int32_t* __restrict__ labels, int64_t T, int64_t V,
-                              float scale2, float* __restrict__ out_lp,
+                              float tparam, const float* __restrict__ row_t,
+                              float* __restrict__ out_lp,
                               float* __restrict__ out_ent, float* __restrict__ out_lse,
                               float* __restrict__ out_sum_p2, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -162,6 +182,7 @@ __global__ void __launch_bounds__(kLThreads, 2)
     uint32_t stage = 0, phase = 0, parity = 0;
     bool ok = true;
     for (int64_t row = blockIdx.x; row < T; row += gridDim.x, parity ^= 1u) {
+      const S sc = row_scale<S>(tparam, row_t, row);
       OnlineStat st = stat_empty();
       for (int64_t c = 0; c < n_chunks; ++c) {
         if (ok) ok = mbar_wait(full_bar(stage), phase, abort_flag, status);
@@ -182,7 +203,7 @@ __global__ void __launch_bounds__(kLThreads, 2)
               w[k] = make_uint4(0, 0, 0, 0);
             }
           }
-          if (nv > 0) stat_fold_bf16x32<kQ>(st, w, nv, scale2);
+          if (nv > 0) stat_fold_bf16x32<kQ>(st, w, nv, sc);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(stage));  // this warp is done with the chunk
@@ -209,8 +230,7 @@ __global__ void __launch_bounds__(kLThreads, 2)
         const int lab = labels[row];
         const bool lab_ok = lab >= 0 && (int64_t)lab < V;
         float yl = 0.f;
-        if (lab_ok)
-          yl = __fmul_rn(__uint_as_float(static_cast<uint32_t>(logits[row * V + lab]) << 16), scale2);
+        if (lab_ok) yl = sc.y(__uint_as_float(static_cast<uint32_t>(logits[row * V + lab]) << 16));
         write_row_outputs(row, r, yl, lab_ok, out_lp, out_ent, out_lse, out_sum_p2);
       }
     }
@@ -218,17 +238,19 @@ __global__ void __launch_bounds__(kLThreads, 2)
 }
 
 // Any V: element-wise loads, 8 values per fold.
-template <bool kQ>
+template <bool kQ, class S>
 __global__ void __launch_bounds__(kRowThreads)
     logits_logprob_scalar_kernel(const uint16_t* __restrict__ logits,
                                  const int32_t* __restrict__ labels, int64_t T, int64_t V,
-                                 float scale2, float* __restrict__ out_lp,
+                                 float tparam, const float* __restrict__ row_t,
+                                 float* __restrict__ out_lp,
                                  float* __restrict__ out_ent, float* __restrict__ out_lse,
                                  float* __restrict__ out_sum_p2) {
   __shared__ OnlineStat sh[kRowWarps];
   constexpr int kGroup = 8;
   for (int64_t row = blockIdx.x; row < T; row += gridDim.x) {
     const uint16_t* rp = logits + row * V;
+    const S sc = row_scale<S>(tparam, row_t, row);
     OnlineStat st = stat_empty();
     for (int64_t base = threadIdx.x; base < V; base += (int64_t)kGroup * kRowThreads) {
       float y[kGroup];
@@ -237,7 +259,7 @@ __global__ void __launch_bounds__(kRowThreads)
       for (int k = 0; k < kGroup; ++k) {
         const int64_t idx = base + (int64_t)k * kRowThreads;
         if (idx < V) {
-          y[k] = __fmul_rn(__uint_as_float(static_cast<uint32_t>(rp[idx]) << 16), scale2);
+          y[k] = sc.y(__uint_as_float(static_cast<uint32_t>(rp[idx]) << 16));
           n = k + 1;
         } else {
           y[k] = 0.f;
@@ -250,7 +272,7 @@ __global__ void __launch_bounds__(kRowThreads)
       const int lab = labels[row];
       const bool ok = lab >= 0 && (int64_t)lab < V;
       float yl = 0.f;
-      if (ok) yl = __fmul_rn(__uint_as_float(static_cast<uint32_t>(rp[lab]) << 16), scale2);
+      if (ok) yl = sc.y(__uint_as_float(static_cast<uint32_t>(rp[lab]) << 16));
       write_row_outputs(row, r, yl, ok, out_lp, out_ent, out_lse, out_sum_p2);
     }
   }
@@ -294,41 +316,67 @@ __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_
   }
 }
 
-}  // namespace
+// Every bf16 bit pattern x: the library's quotient x / t against IEEE fp32
+// division; counts the inputs whose result bits differ (NaN equals NaN).
+__global__ void division_selftest_kernel(float t, int* mismatches) {
+  const uint32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= 65536u) return;
+  const float x = __uint_as_float(i << 16);
+  const float a = ScaleDiv::make(t).quotient(x);
+  const float b = __fdiv_rn(x, t);
+  const bool same = (__float_as_uint(a) == __float_as_uint(b)) || (a != a && b != b);
+  if (!same) atomicAdd(mismatches, 1);
+}
 
-cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
-                                  int64_t V, float inv_temperature, float* out_lp, float* out_ent,
-                                  float* out_lse, float* out_sum_p2, int num_sms, unsigned* status,
-                                  cudaStream_t stream) {
-  if (T <= 0) return cudaSuccess;
-  const float scale2 = inv_temperature * kLog2e;
-  const int64_t max_grid = (int64_t)num_sms * 4;
-  const int grid = (int)(T < max_grid ? T : max_grid);
+template <bool kQ, class S>
+cudaError_t launch_logits_t(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,
+                            float tparam, const float* row_t, float* out_lp, float* out_ent,
+                            float* out_lse, float* out_sum_p2, int num_sms, unsigned* status,
+                            cudaStream_t stream) {
   const bool vec = (V & 7) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
   if (vec) {
     const int64_t tgrid = (int64_t)num_sms * 2;
-    const int g2 = (int)(T < tgrid ? T : tgrid);
-    cudaError_t e;
-    if (out_sum_p2) {
-      e = cudaFuncSetAttribute(logits_logprob_tma_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
-      if (e != cudaSuccess) return e;
-      logits_logprob_tma_kernel<true><<<g2, kLThreads, kLSmemBytes, stream>>>(
-          logits, labels, T, V, scale2, out_lp, out_ent, out_lse, out_sum_p2, status);
-    } else {
-      e = cudaFuncSetAttribute(logits_logprob_tma_kernel<false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kLSmemBytes);
-      if (e != cudaSuccess) return e;
-      logits_logprob_tma_kernel<false><<<g2, kLThreads, kLSmemBytes, stream>>>(
-          logits, labels, T, V, scale2, out_lp, out_ent, out_lse, nullptr, status);
-    }
-  } else if (out_sum_p2)
-    logits_logprob_scalar_kernel<true><<<grid, kRowThreads, 0, stream>>>(
-        logits, labels, T, V, scale2, out_lp, out_ent, out_lse, out_sum_p2);
-  else
-    logits_logprob_scalar_kernel<false><<<grid, kRowThreads, 0, stream>>>(
-        logits, labels, T, V, scale2, out_lp, out_ent, out_lse, nullptr);
-  const cudaError_t e = cudaGetLastError();
+    const int grid = (int)(T < tgrid ? T : tgrid);
+    const cudaError_t e = cudaFuncSetAttribute(logits_logprob_tma_kernel<kQ, S>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kLSmemBytes);
+    if (e != cudaSuccess) return e;
+    logits_logprob_tma_kernel<kQ, S><<<grid, kLThreads, kLSmemBytes, stream>>>(
+        logits, labels, T, V, tparam, row_t, out_lp, out_ent, out_lse, out_sum_p2, status);
+  } else {
+    const int64_t max_grid = (int64_t)num_sms * 4;
+    const int grid = (int)(T < max_grid ? T : max_grid);
+    logits_logprob_scalar_kernel<kQ, S><<<grid, kRowThreads, 0, stream>>>(
+        logits, labels, T, V, tparam, row_t, out_lp, out_ent, out_lse, out_sum_p2);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels, int64_t T,
+                                  int64_t V, float temp_value, bool divide,
+                                  const float* row_temperature, float* out_lp, float* out_ent,
+                                  float* out_lse, float* out_sum_p2, int num_sms, unsigned* status,
+                                  cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  cudaError_t e;
+  if (divide) {
+    e = out_sum_p2 ? launch_logits_t<true, ScaleDiv>(logits, labels, T, V, temp_value,
+                                                     row_temperature, out_lp, out_ent, out_lse,
+                                                     out_sum_p2, num_sms, status, stream)
+                   : launch_logits_t<false, ScaleDiv>(logits, labels, T, V, temp_value,
+                                                      row_temperature, out_lp, out_ent, out_lse,
+                                                      nullptr, num_sms, status, stream);
+  } else {
+    const float scale2 = temp_value * kLog2e;  // inverse temperature folded with log2(e)
+    e = out_sum_p2 ? launch_logits_t<true, ScaleMul>(logits, labels, T, V, scale2, nullptr,
+                                                     out_lp, out_ent, out_lse, out_sum_p2,
+                                                     num_sms, status, stream)
+                   : launch_logits_t<false, ScaleMul>(logits, labels, T, V, scale2, nullptr,
+                                                      out_lp, out_ent, out_lse, nullptr, num_sms,
+                                                      status, stream);
+  }
   if (e == cudaSuccess) note_launch();
   return e;
 }
@@ -346,6 +394,13 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
   else
     fwd_merge_kernel<false><<<(unsigned)blocks, threads, 0, stream>>>(
         pm, ps, pu, nullptr, pzl, labels, T, n_vunits, V, out_lp, out_ent, out_lse, nullptr);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+cudaError_t launch_division_selftest(float t, int* mismatches, cudaStream_t stream) {
+  division_selftest_kernel<<<256, 256, 0, stream>>>(t, mismatches);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

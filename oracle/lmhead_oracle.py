@@ -19,9 +19,10 @@ stored, each step written out as the pages define it):
   function below works row by row; no quantity mixes rows.
 * Temperature (same page, the temperature-order comment and its table): the
   logits are scaled in fp32 precision by the fp32 temperature, never by a
-  bf16-rounded one. The library's entry points take ``inv_temperature`` as an
-  fp32 scalar, so ``z = s * logits`` with ``s`` the fp32 value widened to
-  float64.
+  bf16-rounded one. Most entry points take ``inv_temperature`` as an fp32
+  scalar, so ``z = s * logits`` with ``s`` the fp32 value widened to float64.
+  The sampler-parity form divides instead: ``z = fp32(logits) / fp32(t)``,
+  the quotient rounded to fp32 as the table's "cast first, then divide" fixes.
 * The fused projection, from the SkyRL pull request "Triton backend for fused
   LM-head log-prob" (summary: the vocab projection folded into the chunked
   log-prob, fp32 softmax math): ``logits[t, v] = sum_h hidden[t, h] *
@@ -65,6 +66,8 @@ __all__ = [
     "fused_sum_p2",
     "fused_forward",
     "logprob_from_logits",
+    "divided_logits",
+    "logprob_from_logits_div",
     "dlogits",
     "dlogits_entropy",
     "fused_backward",
@@ -139,6 +142,32 @@ def fused_sum_p2(hidden, weight, inv_temperature: float) -> np.ndarray:
 def logprob_from_logits(logits, labels, inv_temperature: float = 1.0):
     """(logprob, entropy, lse) of the sampler formula on given logits, z = s * logits."""
     return sampler_logprob(fp32_scalar(inv_temperature) * _f64(logits), labels)
+
+
+def divided_logits(logits, temperature) -> np.ndarray:
+    """z = fp32(logits) / fp32(t), the quotient rounded to fp32, as float64 [T, V].
+
+    The verl page's temperature-order table fixes this step's precision: the
+    logits are cast to fp32 first and then divided by the fp32 temperature.
+    numpy's float32 division is the IEEE round-to-nearest quotient, so ``z``
+    holds exactly the fp32 values a sampler that divides by the temperature
+    sees. ``temperature`` is a scalar or one value per row.
+    """
+    x = np.asarray(logits, dtype=np.float32)
+    t = np.asarray(temperature, dtype=np.float32)
+    if t.ndim == 1:
+        t = t[:, None]
+    return (x / t).astype(np.float64)
+
+
+def logprob_from_logits_div(logits, labels, temperature):
+    """(logprob, entropy, lse) of the sampler formula on z = fp32(logits) / fp32(t).
+
+    The log-softmax and everything after it are float64, as in
+    ``sampler_logprob``; only the division is taken at the fp32 precision the
+    pages fix for it.
+    """
+    return sampler_logprob(divided_logits(logits, temperature), labels)
 
 
 def dlogits(z, labels, grad, inv_temperature: float, lse=None) -> np.ndarray:

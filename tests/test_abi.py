@@ -105,6 +105,23 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     rc = lib.lmhead_logprob_entropy_bwd(16, 16, 16, None, None, None, None, 4, 256, 4096, 1.0, 16,
                                         16, 256, 1 << 30, None)
     assert rc == lmh.LMH_ERR_INVALID_ARG  # both upstream grads missing
+    div = lib.logprob_from_logits_div
+    assert div(16, 16, 4, 4096, 0.0, None, 16, None, None, None, None) == lmh.LMH_ERR_INVALID_ARG
+    assert div(16, 16, 4, 4096, float("nan"), None, 16, None, None, None, None) == \
+        lmh.LMH_ERR_INVALID_ARG
+    assert b"temperature" in lib.lmhead_last_error_string()
+    assert div(16, 16, 4, 4096, 0.7, 18, 16, None, None, None, None) == lmh.LMH_ERR_ALIGNMENT
+    assert div(24, 16, 4, 4096, 0.7, None, 16, None, None, None, None) == lmh.LMH_ERR_ALIGNMENT
+    assert div(None, None, 0, 4096, 0.7, None, None, None, None, None, None) == lmh.LMH_OK
+    fh = lib.lmhead_logprob_fwd_host
+    args = [16, 16, 16, 4, 256, 4096, 1.0, 16, 16, 16, 16, None, None, None, None, 256, 1 << 30,
+            None, None]
+    assert fh(*args[:2], None, *args[3:]) == lmh.LMH_ERR_INVALID_ARG  # host labels missing
+    assert fh(*args[:7], 24, *args[8:]) == lmh.LMH_ERR_ALIGNMENT  # device hidden
+    assert fh(*args[:14], 16, *args[15:]) == lmh.LMH_ERR_INVALID_ARG  # entropy host w/o device
+    assert fh(*args[:15], None, *args[16:]) == lmh.LMH_ERR_WORKSPACE
+    assert fh(*args[:6], 0.0, *args[7:]) == lmh.LMH_ERR_INVALID_ARG
+    assert fh(None, None, None, 0, 256, 4096, 1.0, *([None] * 9), 0, None, None) == lmh.LMH_OK
     assert lib.lmhead_engine_gemm(16, 16, 8, 8, 8, 4, 16, None) == lmh.LMH_ERR_INVALID_ARG
     assert lib.lmhead_selftest_wait_timeout(10, None) == lmh.LMH_ERR_INVALID_ARG
 

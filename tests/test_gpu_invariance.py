@@ -152,3 +152,25 @@ def test_grad_hidden_rows_invariant_across_row_chunk_boundary(lmh):
         gh, _ = lmh.lmhead_logprob_bwd(h[r0:r1], w, lab[r0:r1], g[r0:r1], 1.0)
         assert torch.equal(gh, gh_full[r0:r1]), (r0, r1)
     torch.cuda.synchronize()
+
+
+def test_logits_division_form_sub_batches_and_shuffles(lmh):
+    import torch
+
+    T, V = 300, 5000
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    x, lab = to_dev_bf16(inp["logits"]), to_dev(inp["labels"])
+    full = lmh.logprob_from_logits_div(x, lab, 0.7, want_lse=True, want_sum_p2=True)
+    for bs in (1, 7, 256):
+        for r0 in range(0, T, bs):
+            r1 = min(T, r0 + bs)
+            part = lmh.logprob_from_logits_div(x[r0:r1], lab[r0:r1], 0.7, want_lse=True,
+                                               want_sum_p2=True)
+            for a, b in zip(part, full):
+                assert _mismatch(a, b[r0:r1]) == 0
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(4)).to(x.device)
+    part = lmh.logprob_from_logits_div(x[perm].contiguous(), lab[perm].contiguous(), 0.7,
+                                       want_lse=True, want_sum_p2=True)
+    for a, b in zip(part, full):
+        assert _mismatch(a, b[perm]) == 0
+    torch.cuda.synchronize()

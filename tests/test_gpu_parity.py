@@ -314,3 +314,139 @@ def test_bounded_wait_selftest_reports_timeout(lmh):
     assert lmh.lmhead_device_status() == 0  # cleared by the read
     # the context is still usable
     test_engine_gemm_matches_fp64(lmh, 128, 256, 64, 3)
+
+
+# ----------------------------------------------------------------- sampler-parity (division) form
+@pytest.mark.parametrize("T,V", [(300, 5000), (64, 152064), (5, 4999), (3, 1), (130, 8)])
+def test_logits_division_form_matches_oracle(lmh, T, V):
+    import torch
+
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    logits, labels = inp["logits"], inp["labels"]
+    if T > 2:
+        labels[0] = -100
+        labels[1] = V - 1
+    temps = np.random.default_rng(T + V).uniform(0.4, 1.6, size=T).astype(np.float32)
+    for t in (0.7, temps):
+        t_dev = to_dev(temps) if isinstance(t, np.ndarray) else t
+        lp, ent, lse, q = lmh.logprob_from_logits_div(to_dev_bf16(logits), to_dev(labels), t_dev,
+                                                      want_lse=True, want_sum_p2=True)
+        torch.cuda.synchronize()
+        rlp, rent, rlse = oracle.logprob_from_logits_div(f64(logits), labels, t)
+        assert max_abs(lp.cpu().numpy(), rlp) < ATOL_LOGPROB
+        assert max_abs(ent.cpu().numpy(), rent) < ATOL_LOGPROB
+        assert max_abs(lse.cpu().numpy(), rlse) < ATOL_LOGPROB
+        rq = oracle.row_sum_p2(oracle.divided_logits(f64(logits), t))
+        assert max_abs(q.cpu().numpy(), rq) < 1e-5
+
+
+def test_logits_division_per_row_temperature_equals_scalar_calls(lmh):
+    """A row's outputs with a per-row temperature array are bit-identical to a
+    call with that row's temperature as the scalar, and the optional outputs
+    change nothing else."""
+    import torch
+
+    T, V = 12, 5000
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    x, lab = to_dev_bf16(inp["logits"]), to_dev(inp["labels"])
+    temps = np.random.default_rng(5).uniform(0.3, 2.0, size=T).astype(np.float32)
+    full = lmh.logprob_from_logits_div(x, lab, to_dev(temps), want_lse=True, want_sum_p2=True)
+    plain = lmh.logprob_from_logits_div(x, lab, to_dev(temps), want_lse=True)
+    for r in range(T):
+        one = lmh.logprob_from_logits_div(x[r:r + 1], lab[r:r + 1], float(temps[r]), want_lse=True,
+                                          want_sum_p2=True)
+        for a, b in zip(one, full):
+            assert torch.equal(a.view(torch.int32), b[r:r + 1].view(torch.int32))
+    for a, b in zip(plain[:3], full[:3]):
+        assert torch.equal(a, b)
+    torch.cuda.synchronize()
+
+
+def test_logits_division_bad_row_temperature_is_nan_in_that_row_only(lmh):
+    import torch
+
+    T, V = 6, 4096
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    x, lab = to_dev_bf16(inp["logits"]), to_dev(inp["labels"])
+    temps = np.array([0.7, 0.0, 0.9, -1.0, float("inf"), 1.1], dtype=np.float32)
+    lp, ent, _, _ = lmh.logprob_from_logits_div(x, lab, to_dev(temps))
+    torch.cuda.synchronize()
+    lp, ent = lp.cpu().numpy(), ent.cpu().numpy()
+    bad = np.array([False, True, False, True, True, False])
+    assert np.all(np.isnan(lp[bad])) and np.all(np.isnan(ent[bad]))
+    assert np.all(np.isfinite(lp[~bad])) and np.all(np.isfinite(ent[~bad]))
+    rlp, _, _ = oracle.logprob_from_logits_div(f64(inp["logits"][~bad]), inp["labels"][~bad],
+                                               temps[~bad])
+    assert max_abs(lp[~bad], rlp) < ATOL_LOGPROB
+
+
+def test_logits_division_against_torch_sampler_formula(lmh):
+    """Against torch's own fp32 sampler formula on the GPU (log_softmax of the
+    fp32 logits divided by a per-row temperature tensor, then gather): the
+    same z, reduced in another order, so equal to within a few fp32 ulps of
+    the log-probs, not bit for bit."""
+    import torch
+
+    T, V = 64, 152064
+    inp = W.logits_inputs(W.LOGITS, T=T, V=V)
+    x, lab = to_dev_bf16(inp["logits"]), to_dev(inp["labels"])
+    temps = torch.full((T,), 0.7, dtype=torch.float32, device=x.device)
+    lp, _, _, _ = lmh.logprob_from_logits_div(x, lab, temps)
+    ref = torch.log_softmax(x.float() / temps[:, None], dim=-1).gather(1, lab.long()[:, None])[:, 0]
+    torch.cuda.synchronize()
+    assert float((lp - ref).abs().max()) < 1e-4
+
+
+# ----------------------------------------------------------------- forward from host memory
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (64, 128, 152064), (7, 64, 1000), (5, 8, 1)])
+def test_forward_from_host_is_bitwise_the_device_forward(lmh, T, H, V):
+    """The staged forward (host copies overlapped with per-slice launches)
+    fills the device inputs and gives the device forward's exact bits."""
+    import torch
+
+    hidden, weight, labels, _ = fused_case(41, T, H, V, w_std=0.2, oov=((0, -100),) if T > 1 else ())
+    h_host = W.as_torch_bf16(hidden).pin_memory()
+    w_host = W.as_torch_bf16(weight).pin_memory()
+    l_host = torch.from_numpy(labels).pin_memory()
+    dev = torch.device("cuda:0")
+    h = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    w = torch.empty(V, H, dtype=torch.bfloat16, device=dev)
+    lab = torch.empty(T, dtype=torch.int32, device=dev)
+    lp_host = torch.empty(T, dtype=torch.float32).pin_memory()
+    ent_host = torch.empty(T, dtype=torch.float32).pin_memory()
+    for copy_stream in (None, torch.cuda.Stream()):
+        lp, ent, lse = lmh.lmhead_logprob_fwd_host(h_host, w_host, l_host, S07, hidden=h, weight=w,
+                                                   labels=lab, out_logprob_host=lp_host,
+                                                   out_entropy_host=ent_host,
+                                                   copy_stream=copy_stream)
+        torch.cuda.synchronize()
+        assert torch.equal(h.cpu(), h_host) and torch.equal(w.cpu(), w_host)
+        assert torch.equal(lab.cpu(), l_host)
+        rlp, rent, rlse = lmh.lmhead_logprob_fwd(to_dev_bf16(hidden), to_dev_bf16(weight),
+                                                 to_dev(labels), S07, want_lse=True)
+        torch.cuda.synchronize()
+        for a, b in ((lp, rlp), (ent, rent), (lse, rlse)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+        assert torch.equal(lp_host, lp.cpu()) and torch.equal(ent_host, ent.cpu())
+        lmh.lmhead_device_status()
+        h.zero_(), w.zero_(), lab.zero_()
+
+
+def test_division_form_is_ieee_division_for_every_bf16_input(lmh):
+    """The quotient the division form uses, for all 65536 bf16 inputs, equals
+    IEEE fp32 division bit for bit: at the pages' temperatures, at temperatures
+    whose significand is all ones or a power of two, at random ones across
+    the fast path's range, and at extreme or invalid ones (IEEE path)."""
+    rng = np.random.default_rng(123)
+    ts = [0.7, 0.9, 0.6, 1.0, 0.8984375, 0.69921875, 0.6015625, 2.0, 0.5,
+          float(np.nextafter(np.float32(1.0), np.float32(2.0))),
+          float(np.nextafter(np.float32(2.0), np.float32(1.0))),
+          float(np.nextafter(np.float32(1.0), np.float32(0.0))),
+          2.0 ** -20, 2.0 ** 20, 2.0 ** -21, 3.0e6, 1e-30, 1e30, 0.0, -1.0,
+          float("inf"), float("nan")]
+    ts += [float(np.float32(v)) for v in np.exp(rng.uniform(np.log(2.0 ** -20), np.log(2.0 ** 20),
+                                                            size=300))]
+    ts += [float(np.uint32((127 << 23) | int(m)).view(np.float32)) for m in
+           rng.integers(0, 1 << 23, size=300)]
+    bad = {t: n for t in ts if (n := lmh.lmhead_selftest_division(t)) != 0}
+    assert not bad, bad

@@ -8,6 +8,7 @@ copy and show that it fails.
 import json
 import math
 import os
+from fractions import Fraction
 
 import numpy as np
 import pytest
@@ -382,6 +383,93 @@ def test_temperature_order_policy():
 
 
 # ---------------------------------------------------------------------------
+# sampler-parity form: z = fp32(logits) / fp32(t)
+# ---------------------------------------------------------------------------
+
+def check_division_rounding(divide, seed, n=300):
+    """Number of quotients that are not the round-to-nearest fp32 value of x / t.
+
+    Exact rational arithmetic: z is the nearest fp32 value to the rational
+    x / t when neither fp32 neighbour of z is strictly closer to it.
+    """
+    rng = np.random.default_rng(seed)
+    x = _bf(4.0 * rng.standard_normal((1, n)))
+    t = np.float32(rng.uniform(0.3, 1.7))
+    z = np.asarray(divide(x, t), dtype=np.float64)[0]
+    bad = 0
+    for xi, zi in zip(x[0], z):
+        zf = np.float32(zi)
+        if float(zf) != zi:
+            bad += 1
+            continue
+        exact = Fraction(float(xi)) / Fraction(float(t))
+        d = abs(Fraction(float(zf)) - exact)
+        for nb in (np.nextafter(zf, np.float32(-np.inf)), np.nextafter(zf, np.float32(np.inf))):
+            if abs(Fraction(float(nb)) - exact) < d:
+                bad += 1
+                break
+    return bad
+
+
+def test_division_is_round_to_nearest_fp32():
+    for seed in range(3):
+        assert check_division_rounding(oracle.divided_logits, seed) == 0
+
+
+def test_division_form_matches_torch_fp32_division_and_log_softmax():
+    rng = np.random.default_rng(71)
+    rows, V = 6, 3000
+    logits = _bf(2.0 * rng.standard_normal((rows, V)))
+    lab = rng.integers(0, V, size=rows)
+    lab[2] = -100
+    temps = rng.uniform(0.5, 1.5, size=rows).astype(np.float32)
+    # torch's fp32 tensor division, then the sampler formula in float64
+    zt = torch.from_numpy(logits.astype(np.float32)) / torch.from_numpy(temps)[:, None]
+    assert np.array_equal(zt.numpy().astype(np.float64), oracle.divided_logits(logits, temps))
+    lsm = torch.log_softmax(zt.double(), dim=-1)
+    want = lsm.gather(1, torch.from_numpy(np.where(lab < 0, 0, lab))[:, None])[:, 0].numpy()
+    want[2] = 0.0
+    lp, ent, lse = oracle.logprob_from_logits_div(logits, lab, temps)
+    assert np.max(np.abs(lp - want)) < 1e-12
+    assert np.max(np.abs(lse - torch.logsumexp(zt.double(), dim=-1).numpy())) < 1e-12
+    # per-row temperatures are row-by-row scalar calls
+    for r in range(rows):
+        lp_r, ent_r, _ = oracle.logprob_from_logits_div(logits[r:r + 1], lab[r:r + 1], temps[r])
+        assert lp_r[0] == lp[r] and ent_r[0] == ent[r]
+    # t = 1 divides exactly: the same as the multiplied form with s = 1
+    lp1, ent1, _ = oracle.logprob_from_logits_div(logits, lab, 1.0)
+    lp1m, ent1m, _ = oracle.logprob_from_logits(logits, lab, 1.0)
+    assert np.array_equal(lp1, lp1m) and np.array_equal(ent1, ent1m)
+    # the two forms differ only by the last-bit rounding of z
+    lpm, _, _ = oracle.logprob_from_logits(logits, lab, 1.0 / 0.7)
+    lpd, _, _ = oracle.logprob_from_logits_div(logits, lab, 0.7)
+    assert 0 < np.max(np.abs(lpm - lpd)) < 1e-5
+
+
+def test_temperature_order_policy_division_form():
+    """The table's claim for the fp32 division inside a chunk: a row's value
+    does not depend on the chunk it is taken in, and the bf16-temperature path
+    mismatches every row unless t = 1."""
+    with open(os.path.join(GOLDEN, "temperature_order.json")) as f:
+        gold = json.load(f)
+    rng = np.random.default_rng(62)
+    rows, V = 64, 32000
+    logits = _bf(2.0 * rng.standard_normal((rows, V)) + rng.standard_normal((rows, 1)))
+    lab = rng.integers(0, V, size=rows)
+    for c in gold["cases"]:
+        T = c["temperature"]
+        tb = c["bf16_temperature"]
+        z_bf16 = _bf(logits.astype(np.float32) / np.float32(tb))
+        lp_bf16, _, _ = oracle.logprob_from_logits(z_bf16, lab, 1.0)
+        lp_div, _, _ = oracle.logprob_from_logits_div(logits, lab, T)
+        chunks = [oracle.logprob_from_logits_div(logits[i:i + 8], lab[i:i + 8], T)[0]
+                  for i in range(0, rows, 8)]
+        assert np.array_equal(np.concatenate(chunks), lp_div)
+        expected = rows if c["mismatched_rows"] == gold["rows"] else 0
+        assert int(np.sum(lp_bf16 != lp_div)) == expected, T
+
+
+# ---------------------------------------------------------------------------
 # planted mistakes: each pin must reject a plausible error in the oracle
 # ---------------------------------------------------------------------------
 
@@ -444,7 +532,18 @@ def _sum_p2_unnormalised(z):
     return (e * e).sum(axis=1) / e.sum(axis=1)  # divides by s instead of s^2
 
 
+def _divide_by_reciprocal(x, t):
+    return np.asarray(x, np.float32) * np.float32(1.0 / np.float32(t))  # x * RN(1/t)
+
+
+def _divide_in_bf16(x, t):
+    tb = W.bf16_bits_to_f32(W.f32_to_bf16_bits(np.array([t], np.float32)))[0]
+    return np.asarray(x, np.float32) / tb
+
+
 def test_planted_mistakes_are_caught():
+    assert check_division_rounding(_divide_by_reciprocal, 0) > 0
+    assert check_division_rounding(_divide_in_bf16, 0) > 0
     assert check_scipy_lse_entropy(_sampler_entropy_missing_lse, 0) > 1e-3
     assert check_two_value(_sampler_entropy_missing_lse, 4096, 7, 5.5, 0.25) > 1e-3
     with np.errstate(over="ignore", invalid="ignore"):
