@@ -55,6 +55,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 GEMM_KINDS = ("fused_fwd_gemm", "dlogits_gemm", "grad_hidden_gemm", "grad_weight_gemm")
 
 
+def n_fwd_chunks(V: int) -> int:
+    """1024-column vocabulary chunks of the forward's partials."""
+    return (V + 1023) // 1024
+
+
 def inv_temperature() -> float:
     import numpy as np
 
@@ -470,9 +475,15 @@ def run_gpu(args):
         "grad_hidden_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
         "grad_weight_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
     }
+    bytes_per_launch = {  # HBM-bound helpers of the step
+        "fwd_merge": (16.0 * n_fwd_chunks(V) + 4.0 + 12.0) * T,
+        "hidden_transpose": 4.0 * min(T, rows_per_chunk) * H,
+    }
     for k, info in kernels.items():
         if k in flops_per_launch:
             info["tflops"] = flops_per_launch[k] / (info["avg_ms"] * 1e-3) / 1e12
+        if k in bytes_per_launch:
+            info["gbs"] = bytes_per_launch[k] / (info["avg_ms"] * 1e-3) / 1e9
     dominant = max(kernels, key=lambda k: kernels[k]["total_ms"]) if kernels else None
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     roofline = None

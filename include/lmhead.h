@@ -70,7 +70,8 @@ struct CUstream_st; /* cudaStream_t */
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
  * Returns SIZE_MAX for invalid arguments. The forward needs 16 bytes per row
  * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
- * row and a bf16 dlogits buffer of min(T, 16384) x V.
+ * row, a bf16 dlogits buffer of min(T, 16384) x V and a bf16 transpose of one
+ * 16384-row chunk of hidden (H x min(T, 16384)).
  */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 

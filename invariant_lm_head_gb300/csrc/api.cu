@@ -186,11 +186,11 @@ struct BwdWs {
   float* lp;
   float* ent;
   uint16_t* dl;  // [Tc][Vpad] bf16 dlogits of one row chunk
-  int64_t vpad, tc;
+  uint16_t* ht;  // [H][Tcpad] bf16 transpose of one row chunk of hidden
+  int64_t vpad, tc, tcpad;
 };
 
 BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
-  (void)H;
   BwdWs w;
   w.vpad = round_up(V, 8);
   w.tc = T < lmh::kBwdRowChunk ? T : lmh::kBwdRowChunk;
@@ -199,6 +199,8 @@ BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
   w.lp = c.take<float>(T);
   w.ent = c.take<float>(T);
   w.dl = c.take<uint16_t>(w.tc * w.vpad);
+  w.tcpad = round_up(w.tc, 8);
+  w.ht = c.take<uint16_t>(H * w.tcpad);
   return w;
 }
 
@@ -251,11 +253,13 @@ enum Kind : int {
   K_ENGINE_GEMM,
   K_SELFTEST,
   K_LOGITS_ROWWISE_DIV,
+  K_HIDDEN_TRANSPOSE,
   K_COUNT
 };
 const char* const kKindNames[K_COUNT] = {
     "fused_fwd_gemm", "fwd_merge",   "dlogits_gemm",  "grad_hidden_gemm",  "grad_weight_gemm",
-    "logits_rowwise", "engine_gemm", "selftest_wait", "logits_rowwise_div"};
+    "logits_rowwise", "engine_gemm", "selftest_wait", "logits_rowwise_div",
+    "hidden_transpose"};
 
 struct TimingRec {
   int kind;
@@ -476,7 +480,8 @@ int copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cu
 // chunk of kBwdRowChunk rows, in ascending order:
 //   dl   = recomputed logits -> dlogits (bf16 [rows][Vpad])
 //   dH   = dl * W          (A = dl K-major, B = W MN-major)
-//   dW  (+)= dl^T * hidden (A = dl MN-major, B = hidden MN-major)
+//   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
+//   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
 int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                  const float* grad_lp, const float* grad_ent, const float* lse, const float* ent,
                  int64_t T, int64_t H, int64_t V, float s, uint16_t* grad_hidden,
@@ -523,10 +528,10 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
-    CUtensorMap t_w, t_h, t_h_mn, t_dl, t_dl_mn;
+    CUtensorMap t_w, t_h, t_ht, t_dl, t_dl_mn;
     LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));        // [V][K=H]
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
-    LMH_TRY(make_tmap(&t_h_mn, h_c, H, rows, H * 2, 64, lmh::kBK));           // [K=rows][M=H]
+    LMH_TRY(make_tmap(&t_ht, w.ht, rows, H, w.tcpad * 2, lmh::kBK, lmh::kBM)); // [M=H][K=rows]
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
     LMH_TRY(make_tmap(&t_dl_mn, w.dl, V, rows, w.vpad * 2, 64, lmh::kBK));    // [K=rows][N=V]
 
@@ -560,17 +565,21 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
                lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
                "grad_hidden");
 
+    // hidden^T of the chunk, so grad_weight reads its A operand K-major
+    LMH_LAUNCH(K_HIDDEN_TRANSPOSE, st,
+               lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st), "hidden transpose");
+
     lmh::GemmParams r{};
     r.status = dev->status;
     // grad_weight^T [H][V] = hidden^T * dl, stored transposed into grad_weight [V][H]
     r.M = static_cast<int>(H);
     r.N = static_cast<int>(V);
     r.K = static_cast<int>(rows);
-    r.a_mn = 1;
+    r.a_mn = 0;
     r.b_mn = 1;
     r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
     LMH_LAUNCH(K_DWEIGHT_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreF32T, t_h_mn, t_dl_mn, r, 1, dev->sms, st, &o_gw),
+               lmh::launch_gemm(lmh::Epi::StoreF32T, t_ht, t_dl_mn, r, 1, dev->sms, st, &o_gw),
                "grad_weight");
   }
   return ok();

@@ -29,11 +29,11 @@
 //              for an out-of-vocab label (same page, out-of-vocab gradient
 //              fix); written as bf16 dl [rows][V].
 //   StoreBf16  grad_hidden = dl * W (B = W read MN-major), rounded once to bf16.
-//   StoreF32T  grad_weight^T = hidden^T * dl (A = hidden and B = dl read
-//              MN-major), written transposed as grad_weight [V][H] in fp32,
-//              accumulated over row chunks in ascending order. Taking the
-//              small hidden operand as A keeps it resident in L2 while dl
-//              streams through once.
+//   StoreF32T  grad_weight^T = hidden^T * dl (A = the chunk's hidden^T read
+//              K-major, B = dl read MN-major), written transposed as
+//              grad_weight [V][H] in fp32, accumulated over row chunks in
+//              ascending order. Taking the small hidden operand as A keeps it
+//              close to L2 while dl streams through once.
 //   StoreF32   D = A * B^T in fp32, row-major (the bare engine GEMM).
 //
 // Batch invariance: the work split depends only on N (vocab) and never on M

@@ -100,6 +100,11 @@ cudaError_t launch_logits_logprob(const uint16_t* logits, const int32_t* labels,
 // quotient x / t in the logits path differs from IEEE fp32 division.
 cudaError_t launch_division_selftest(float t, int* mismatches, cudaStream_t stream);
 
+// out[c][r] = in[r][c] for a rows x cols bf16 matrix; cols % 8 == 0 and
+// `in` rows 16-byte aligned (in_ld % 8 == 0).
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t in_ld,
+                                  uint16_t* out, int64_t out_ld, cudaStream_t stream);
+
 cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, const float* pq,
                              const float* pzl, const int32_t* labels, int64_t T, int n_vunits,
                              int64_t V, float* out_logprob, float* out_entropy, float* out_lse,

@@ -316,6 +316,49 @@ __global__ void wait_selftest_kernel(unsigned* status, unsigned long long limit_
   }
 }
 
+// out[c][r] = in[r][c] for a rows x cols bf16 matrix (cols % 8 == 0, rows of
+// `in` 16-byte aligned): 64 x 64 tiles through shared memory, 16-byte loads,
+// and 16-byte stores where the output row allows them. Each warp stores
+// 4 output rows x 128 contiguous bytes.
+__global__ void __launch_bounds__(256)
+    transpose_bf16_kernel(const uint16_t* __restrict__ in, int64_t rows, int64_t cols,
+                          int64_t in_ld, uint16_t* __restrict__ out, int64_t out_ld) {
+  __shared__ uint16_t tile[64][64 + 2];
+  const int64_t r0 = (int64_t)blockIdx.y * 64;
+  const int64_t c0 = (int64_t)blockIdx.x * 64;
+  for (int i = threadIdx.x; i < 512; i += 256) {
+    const int r = i >> 3, cw = i & 7;
+    const int64_t gr = r0 + r, gc = c0 + cw * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (gr < rows && gc < cols) v = *reinterpret_cast<const uint4*>(in + gr * in_ld + gc);
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tile[r][cw * 8 + 2 * j] = static_cast<uint16_t>(ws[j] & 0xffffu);
+      tile[r][cw * 8 + 2 * j + 1] = static_cast<uint16_t>(ws[j] >> 16);
+    }
+  }
+  __syncthreads();
+  const bool vec_out = (out_ld & 7) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
+  for (int i = threadIdx.x; i < 512; i += 256) {
+    const int c = i >> 3, rw = i & 7;
+    const int64_t gc = c0 + c, gr = r0 + rw * 8;
+    if (gc >= cols || gr >= rows) continue;
+    uint32_t ws[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      ws[j] = static_cast<uint32_t>(tile[rw * 8 + 2 * j][c]) |
+              (static_cast<uint32_t>(tile[rw * 8 + 2 * j + 1][c]) << 16);
+    uint16_t* dst = out + gc * out_ld + gr;
+    if (vec_out && gr + 8 <= rows) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(ws[0], ws[1], ws[2], ws[3]);
+    } else {
+      for (int j = 0; j < 8 && gr + j < rows; ++j)
+        dst[j] = static_cast<uint16_t>(ws[j >> 1] >> (16 * (j & 1)));
+    }
+  }
+}
+
 // Every bf16 bit pattern x: the library's quotient x / t against IEEE fp32
 // division; counts the inputs whose result bits differ (NaN equals NaN).
 __global__ void division_selftest_kernel(float t, int* mismatches) {
@@ -401,6 +444,16 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
 
 cudaError_t launch_division_selftest(float t, int* mismatches, cudaStream_t stream) {
   division_selftest_kernel<<<256, 256, 0, stream>>>(t, mismatches);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols, int64_t in_ld,
+                                  uint16_t* out, int64_t out_ld, cudaStream_t stream) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+  transpose_bf16_kernel<<<grid, 256, 0, stream>>>(in, rows, cols, in_ld, out, out_ld);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
