@@ -476,7 +476,7 @@ def run_gpu(args):
         "grad_weight_gemm": 2.0 * min(T, rows_per_chunk) * H * V,
     }
     bytes_per_launch = {  # HBM-bound helpers of the step
-        "fwd_merge": (16.0 * n_fwd_chunks(V) + 4.0 + 12.0) * T,
+        "fwd_merge": (12.0 * n_fwd_chunks(V) + 20.0) * T,  # m, s, u; zl, label; 3 outputs
         "hidden_transpose": 4.0 * min(T, rows_per_chunk) * H,
     }
     for k, info in kernels.items():
