@@ -97,28 +97,28 @@ __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], i
 // y is the map of the maximum of x.
 __device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// The two bf16 of a 32-bit word as an fp32 pair (low half first).
+__device__ __forceinline__ f32x2 bf16x2_f2(uint32_t w) { return f2_pack(bf16_lo_f(w), bf16_hi_f(w)); }
 
 struct ScaleMul {
   float c;
   __device__ __forceinline__ float y(float x) const { return __fmul_rn(x, c); }
   // Every group takes the one-FMA path.
   __device__ __forceinline__ bool group_fast(const uint4 (&)[4], int) const { return true; }
-  // d[2i], d[2i+1] = the shifted values y - m of the low and high bf16 of
-  // word i (8 values per 16-byte word, words of w in order).
+  // d[i] = the shifted pair y - m of the two bf16 of word i (words of w in
+  // order, 4 per 16-byte vector).
   __device__ __forceinline__ void shift_fast(const uint4 (&w)[4], float neg_m,
-                                             float (&d)[32]) const {
+                                             f32x2 (&d)[16]) const {
+    const f32x2 c2 = f2_pack(c, c), nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        d[8 * k + 2 * q] = __fmaf_rn(bf16_lo_f(ws[q]), c, neg_m);
-        d[8 * k + 2 * q + 1] = __fmaf_rn(bf16_hi_f(ws[q]), c, neg_m);
-      }
+      for (int q = 0; q < 4; ++q) d[4 * k + q] = f2_fma(bf16x2_f2(ws[q]), c2, nm2);
     }
   }
   __device__ __forceinline__ void shift_exact(const uint4 (&w)[4], int, float neg_m,
-                                              float (&d)[32]) const {
+                                              f32x2 (&d)[16]) const {
     shift_fast(w, neg_m, d);
   }
 };
@@ -130,16 +130,16 @@ static __device__ __noinline__ float div_ieee(float x, float t) { return __fdiv_
 // The quotient uses Markstein's correction of a reciprocal product (P.
 // Markstein, "Computation of elementary functions on the IBM RISC System/6000
 // processor", IBM J. Res. Dev. 34(1), 1990): with r = 1/t rounded to nearest,
-// q0 = x * r rounded, the remainder q0 * t - x is exact in one FMA, and
-// q0 - rem * r rounded once is the correctly rounded quotient. Taking the
-// remainder with this sign also gives -0 for x = -0. The fast path holds for
-// t in [2^-20, 2^20] and x = 0 or |x| in [2^-100, 2^100], where every
+// q0 = x * r rounded, the remainder x - q0 * t is exact in one FMA, and
+// q0 + rem * r rounded once is the correctly rounded quotient. The fast path
+// holds for t in [2^-20, 2^20] and |x| in [2^-100, 2^100], where every
 // intermediate is exact or a normal fp32 number, so the result scales exactly
 // with the exponents of x and t. It was checked by exact arithmetic for every
 // bf16 significand against every fp32 temperature significand and for every
 // bf16 input in that range at 2000 temperatures, and on the GPU against IEEE
-// division for every bf16 input (the library's lmhead_selftest_division).
-// Other inputs (tiny or huge |x|, inf, extreme t) take the IEEE division.
+// division for every bf16 input (the library's lmhead_selftest_division,
+// which runs this same packed routine). Other inputs (zero, tiny or huge |x|,
+// inf, extreme t) take the IEEE division.
 struct ScaleDiv {
   float t;
   float r;  // 1/t rounded to nearest, or 0 when t is outside [2^-20, 2^20]
@@ -149,19 +149,26 @@ struct ScaleDiv {
     d.r = (temperature >= 0x1p-20f && temperature <= 0x1p20f) ? __frcp_rn(temperature) : 0.f;
     return d;
   }
-  __device__ __forceinline__ float fast_quotient(float x) const {
-    const float q0 = __fmul_rn(x, r);
-    const float nrem = __fmaf_rn(q0, t, -x);
-    return __fmaf_rn(-nrem, r, q0);
+  // Both halves of x2 through the fast path (no range check).
+  __device__ __forceinline__ f32x2 fast_quotient2(f32x2 x2) const {
+    const f32x2 r2 = f2_pack(r, r);
+    const f32x2 q0 = f2_mul(x2, r2);
+    const f32x2 rem = f2_fma(q0, f2_pack(-t, -t), x2);
+    return f2_fma(rem, r2, q0);
+  }
+  __device__ __forceinline__ static bool in_fast_range(float ax) {
+    return ax >= 0x1p-100f && ax <= 0x1p100f;
   }
   __device__ __forceinline__ float quotient(float x) const {
-    const float ax = fabsf(x);
-    if (r != 0.f && (ax == 0.f || (ax >= 0x1p-100f && ax <= 0x1p100f))) return fast_quotient(x);
+    if (r != 0.f && in_fast_range(fabsf(x))) {
+      float lo, hi;
+      f2_unpack(fast_quotient2(f2_pack(x, x)), lo, hi);
+      return lo;
+    }
     return div_ieee(x, t);
   }
   __device__ __forceinline__ float y(float x) const { return __fmul_rn(quotient(x), kLog2e); }
-  // True when every value of the first nv words is in the fast path's range
-  // (a group holding a zero is sent to shift_exact too, which is exact for it).
+  // True when every value of the first nv vectors is in the fast path's range.
   __device__ __forceinline__ bool group_fast(const uint4 (&w)[4], int nv) const {
     if (r == 0.f) return false;
     __nv_bfloat162 amax = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0].x));
@@ -178,39 +185,44 @@ struct ScaleDiv {
         }
       }
     }
-    const float lo = fminf(__low2float(amin), __high2float(amin));
-    const float hi = fmaxf(__low2float(amax), __high2float(amax));
-    return lo >= 0x1p-100f && hi <= 0x1p100f;
+    return in_fast_range(fminf(__low2float(amin), __high2float(amin))) &&
+           in_fast_range(fmaxf(__low2float(amax), __high2float(amax)));
   }
   // d = z * log2(e) - m in one FMA, z = x / t.
   __device__ __forceinline__ void shift_fast(const uint4 (&w)[4], float neg_m,
-                                             float (&d)[32]) const {
+                                             f32x2 (&d)[16]) const {
+    const f32x2 l2 = f2_pack(kLog2e, kLog2e), nm2 = f2_pack(neg_m, neg_m);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        d[8 * k + 2 * q] = __fmaf_rn(fast_quotient(bf16_lo_f(ws[q])), kLog2e, neg_m);
-        d[8 * k + 2 * q + 1] = __fmaf_rn(fast_quotient(bf16_hi_f(ws[q])), kLog2e, neg_m);
-      }
+      for (int q = 0; q < 4; ++q) d[4 * k + q] = f2_fma(fast_quotient2(bf16x2_f2(ws[q])), l2, nm2);
     }
   }
   __device__ __forceinline__ void shift_exact(const uint4 (&w)[4], int nv, float neg_m,
-                                              float (&d)[32]) const {
+                                              f32x2 (&d)[16]) const {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       if (k < nv) {
         const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          d[8 * k + 2 * q] = __fmaf_rn(quotient(bf16_lo_f(ws[q])), kLog2e, neg_m);
-          d[8 * k + 2 * q + 1] = __fmaf_rn(quotient(bf16_hi_f(ws[q])), kLog2e, neg_m);
-        }
+        for (int q = 0; q < 4; ++q)
+          d[4 * k + q] = f2_pack(__fmaf_rn(quotient(bf16_lo_f(ws[q])), kLog2e, neg_m),
+                                 __fmaf_rn(quotient(bf16_hi_f(ws[q])), kLog2e, neg_m));
       }
     }
   }
 };
 
+// Fold 32 bf16 values, given as 4 x 16-byte words (8 values each, of which
+// the first nv words are valid), into the state; sc maps a value to y. Same
+// statistics as stat_fold on the mapped values, in fewer instructions: the max
+// is taken on the raw bf16 pairs (exact, and max commutes with the
+// non-decreasing map); the final scale and the max shift are one FMA,
+// d = x * c - m (ScaleMul) or d = z * log2(e) - m (ScaleDiv); and the two bf16
+// of each 32-bit word go through every fp32 step as one packed pair, the low
+// halves feeding one partial sum and the high halves the other. Every
+// operation is still an explicit round-to-nearest operation in a fixed order.
 template <bool kQ, class S>
 __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&w)[4], int nv,
                                                   const S& sc) {
@@ -230,30 +242,30 @@ __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&
   const float a = ex2(d0);
   const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
   const float s = __fmul_rn(st.s, a);
-  float d[32];
+  f32x2 d[16];
   if (sc.group_fast(w, nv))
     sc.shift_fast(w, -mn, d);
   else
     sc.shift_exact(w, nv, -mn, d);
-  float s0 = 0.f, s1 = 0.f, u0 = 0.f, u1 = 0.f, q0 = 0.f, q1 = 0.f;
+  f32x2 s2 = f2_pack(0.f, 0.f), u2 = s2, q2 = s2;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k < nv) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float da = d[8 * k + 2 * q];
-        const float ea = ex2(da);
-        s0 = __fadd_rn(s0, ea);
-        u0 = __fmaf_rn(ea, da, u0);
-        if (kQ) q0 = __fmaf_rn(ea, ea, q0);
-        const float db = d[8 * k + 2 * q + 1];
-        const float eb = ex2(db);
-        s1 = __fadd_rn(s1, eb);
-        u1 = __fmaf_rn(eb, db, u1);
-        if (kQ) q1 = __fmaf_rn(eb, eb, q1);
+        float da, db;
+        f2_unpack(d[4 * k + q], da, db);
+        const f32x2 e2 = f2_pack(ex2(da), ex2(db));
+        s2 = f2_add(s2, e2);
+        u2 = f2_fma(e2, d[4 * k + q], u2);
+        if (kQ) q2 = f2_fma(e2, e2, q2);
       }
     }
   }
+  float s0, s1, u0, u1, q0, q1;
+  f2_unpack(s2, s0, s1);
+  f2_unpack(u2, u0, u1);
+  f2_unpack(q2, q0, q1);
   if (kQ) st.q = __fmaf_rn(st.q, __fmul_rn(a, a), __fadd_rn(q0, q1));
   st.s = __fadd_rn(s, __fadd_rn(s0, s1));
   st.u = __fadd_rn(u, __fadd_rn(u0, u1));
