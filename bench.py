@@ -76,14 +76,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "of fallback"
 
 
-def file_sha(path: str) -> str:
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def sources_sha(paths) -> str | None:
+    """sha256 prefix of the named repository files, concatenated in order."""
+    h = hashlib.sha256()
+    for rel in paths:
+        full = os.path.join(ROOT, rel)
+        if not os.path.exists(full):
+            return None
+        with open(full, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_for(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source has changed since the counters were taken."""
+    """DRAM bytes per launch from the committed ncu summary, or None when a
+    source file that shapes the kernel's memory traffic has changed since the
+    counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -92,8 +100,8 @@ def traffic_for(kernel: str):
     k = d.get("kernels", {}).get(kernel)
     if not k:
         return None
-    src = os.path.join(ROOT, k.get("source_file", ""))
-    if not os.path.exists(src) or file_sha(src) != k.get("source_sha"):
+    files = k.get("source_files") or []
+    if not files or sources_sha(files) != k.get("source_sha"):
         return None
     return k.get("dram_bytes_per_full_launch")
 

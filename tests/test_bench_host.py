@@ -4,6 +4,8 @@ max-over-ranks timing and the whole-job throughput aggregate."""
 import os
 import socket
 
+import json
+
 import pytest
 import torch.multiprocessing as mp
 
@@ -51,3 +53,16 @@ def test_single_rank_aggregate_and_defaults():
 
 def test_traffic_lookup_ignores_stale_counters(tmp_path, monkeypatch):
     assert bench.traffic_for("no_such_kernel") is None
+    # a fake repository: the entry counts only while its sources are unchanged
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "a.cu").write_text("one")
+    (tmp_path / "b.cu").write_text("two")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.sources_sha(["a.cu", "b.cu"])
+    entry = {"source_files": ["a.cu", "b.cu"], "source_sha": sha,
+             "dram_bytes_per_full_launch": 1234}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"kernels": {"k": entry}}))
+    assert bench.traffic_for("k") == 1234
+    (tmp_path / "b.cu").write_text("changed")
+    assert bench.traffic_for("k") is None
+    assert bench.sources_sha(["a.cu", "missing.cu"]) is None
