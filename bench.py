@@ -557,6 +557,19 @@ def run_gpu(args):
         extras = {"fwd_only": {"T=16384 H=3584 V=152064": {
             "tokens_per_s": T / (f_ms * 1e-3), "ms_per_call": f_ms, "ms_kernels": fk,
             "tflops_kernels": 2.0 * T * H * V / (fk * 1e-3) / 1e12}}}
+        # small batches of the same head: the forward then reads W (1.09 GB)
+        # once per call and is bound by HBM, not by the tensor cores
+        small = {}
+        for Ts in (1, 64, 512):
+            fs = lambda: lmh.lmhead_logprob_fwd(hidden[:Ts], weight, labels[:Ts], s,  # noqa: E731
+                                                out_logprob=lp[:Ts], out_entropy=ent[:Ts],
+                                                workspace=ws_f)
+            ks = kernel_ms(lmh, fs, args.steps, 3, fwd_kernels)
+            small[f"T={Ts}"] = {"ms_kernels": ks, "tokens_per_s": Ts / (ks * 1e-3),
+                                "weight_gbs": V * H * 2 / (ks * 1e-3) / 1e9,
+                                "weight_frac_of_hbm": V * H * 2 / (ks * 1e-3) / 1e9
+                                / peaks["hbm_gbs"]}
+        extras["fwd_only"]["small_batches H=3584 V=152064"] = small
         gh = gw = ws_b = hidden = weight = None  # free before the next legs
         torch.cuda.empty_cache()
         # forward only, Llama-like shape

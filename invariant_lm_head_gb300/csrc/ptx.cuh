@@ -1,5 +1,6 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA tile loads, tcgen05 (TMEM
-// allocation, MMA, commit, loads) and bounded waits.
+// allocation, MMA, commit, loads), bounded waits, and packed fp32-pair
+// arithmetic.
 //
 // Every wait in this library is bounded: it polls, and after a time limit it
 // records LMH_DEVSTAT_TIMEOUT in the caller-visible status word, raises the

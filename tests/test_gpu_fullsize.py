@@ -4,9 +4,9 @@ sampled vocabulary rows of grad_weight) and properties that hold at any size.
 
 Workloads (seeded inputs from workloads.py):
   tiny fused forward      T=64    H=256  V=4096   (whole output, plus 1/7-row batches)
-  logits path             T=8192         V=152064
+  logits path             T=8192         V=152064 (also its division form)
   Llama-like forward      T=4096  H=4096 V=32000
-  Qwen-like fwd+bwd       T=16384 H=3584 V=152064 inv_T=1/0.7
+  Qwen-like fwd+bwd       T=16384 H=3584 V=152064 inv_T=1/0.7 (also from host memory)
   packed varlen fwd+bwd   32 sequences, lengths U[128, 4096], H=5120 V=152064
 """
 
@@ -90,6 +90,28 @@ def test_logits_config_sampled_rows_and_properties(lmh):
     assert np.all(lse >= row_max - 1e-4)
 
 
+def test_logits_config_division_form_sampled_rows(lmh):
+    """The sampler-parity form on the full logits workload, per-row
+    temperatures, against the oracle's fp32-division form on sampled rows."""
+    import torch
+
+    wl = W.LOGITS
+    inp = W.logits_inputs(wl)
+    x, lab = to_dev_bf16(inp["logits"]), to_dev(inp["labels"])
+    temps = np.random.default_rng(8).uniform(0.5, 1.5, size=wl.T).astype(np.float32)
+    lp, ent, lse, q = lmh.logprob_from_logits_div(x, lab, to_dev(temps), want_lse=True,
+                                                  want_sum_p2=True)
+    torch.cuda.synchronize()
+    rows = _sample_rows(wl.T, 128, 9)
+    rlp, rent, rlse = oracle.logprob_from_logits_div(f64(inp["logits"][rows]), inp["labels"][rows],
+                                                     temps[rows])
+    assert max_abs(lp.cpu().numpy()[rows], rlp) < ATOL_LOGPROB
+    assert max_abs(ent.cpu().numpy()[rows], rent) < ATOL_LOGPROB
+    assert max_abs(lse.cpu().numpy()[rows], rlse) < ATOL_LOGPROB
+    rq = oracle.row_sum_p2(oracle.divided_logits(f64(inp["logits"][rows]), temps[rows]))
+    assert max_abs(q.cpu().numpy()[rows], rq) < 1e-5
+
+
 def test_llama_config_forward_sampled_rows(lmh):
     import torch
 
@@ -139,6 +161,32 @@ def test_qwen_config_forward_backward_sampled(lmh, qwen):
     lhs = float(torch.sum(gw.double() * w.double()).item())
     rhs = float(torch.sum(gh.double() * h.double()).item())
     assert abs(lhs - rhs) < RTOL_FROB_GRAD * max(abs(lhs), abs(rhs))
+
+
+def test_qwen_config_forward_from_host_is_bitwise_the_device_forward(lmh, qwen):
+    """The host-staged forward (the benchmark's end-to-end path: weight copied
+    in vocab slices, one launch per slice) gives the device forward's bits."""
+    import torch
+
+    wl, inp, _ = qwen
+    s = wl.inv_temperature
+    h_host = W.as_torch_bf16(inp["hidden"]).pin_memory()
+    w_host = W.as_torch_bf16(inp["weight"]).pin_memory()
+    l_host = torch.from_numpy(inp["labels"]).pin_memory()
+    dev = torch.device("cuda:0")
+    h = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    w = torch.empty(wl.V, wl.H, dtype=torch.bfloat16, device=dev)
+    lab = torch.empty(wl.T, dtype=torch.int32, device=dev)
+    lp_host = torch.empty(wl.T, dtype=torch.float32).pin_memory()
+    lp, ent, lse = lmh.lmhead_logprob_fwd_host(h_host, w_host, l_host, s, hidden=h, weight=w,
+                                               labels=lab, out_logprob_host=lp_host)
+    ref = lmh.lmhead_logprob_fwd(h, w, lab, s, want_lse=True)
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    assert torch.equal(w.cpu(), w_host) and torch.equal(h.cpu(), h_host)
+    for a, b in zip((lp, ent, lse), ref):
+        assert _bits_equal(a, b)
+    assert torch.equal(lp_host, lp.cpu())
 
 
 def test_qwen_config_grad_weight_with_sparse_upstream_grad(lmh, qwen):
