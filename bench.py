@@ -18,6 +18,8 @@ Prints ONE JSON line (rank 0). Besides the contract keys it carries:
                  and its division (sampler-parity) form
   sampler_parity fp32-bit mismatch counts against torch's fp32 sampler
                  formula on [4096, 152064] logits
+  next_rows      the entropy-gradient step and the sum_pi_squared variants of
+                 the forward and of the logits path, on the same workloads
   cpu_baseline   the fp64 CPU oracle timed on a bounded sample on host cores
   e2e            the same step from pinned host inputs: the host-staged
                  forward (copies overlapped with the forward) and the
@@ -570,6 +572,30 @@ def run_gpu(args):
                                 "weight_frac_of_hbm": V * H * 2 / (ks * 1e-3) / 1e9
                                 / peaks["hbm_gbs"]}
         extras["fwd_only"]["small_batches H=3584 V=152064"] = small
+        # the next rows on the same workload: the backward with an entropy
+        # gradient, and the forward that also returns sum_pi_squared
+        g_ent = torch.randn(T, generator=torch.Generator(device=dev).manual_seed(11), device=dev)
+
+        def ent_step():
+            lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp, out_entropy=ent,
+                                   out_lse=lse, workspace=ws_f)
+            lmh.lmhead_logprob_entropy_bwd(hidden, weight, labels, grad, g_ent, s, lse=lse,
+                                           entropy=ent, grad_hidden=gh, grad_weight=gw,
+                                           workspace=ws_b)
+
+        step_kernels = ("fused_fwd_gemm", "fwd_merge", "dlogits_gemm", "grad_hidden_gemm",
+                        "hidden_transpose", "grad_weight_gemm")
+        e_ms = kernel_ms(lmh, ent_step, args.steps, 2, step_kernels)
+        q2 = torch.empty(T, device=dev)
+        fq = lambda: lmh.lmhead_logprob_fwd_stats(hidden, weight, labels, s,  # noqa: E731
+                                                  out_logprob=lp, out_entropy=ent, out_lse=lse,
+                                                  out_sum_p2=q2, workspace=ws_f)
+        q_ms = kernel_ms(lmh, fq, args.steps, 2, fwd_kernels)
+        extras["next_rows"] = {
+            "entropy_grad_fwd_bwd": {"ms_kernels_per_step": e_ms, "tokens_per_s": T / (e_ms * 1e-3),
+                                     "tflops_as_executed": 8.0 * T * H * V / (e_ms * 1e-3) / 1e12},
+            "fwd_with_sum_p2": {"ms_kernels": q_ms, "tokens_per_s": T / (q_ms * 1e-3),
+                                "tflops": 2.0 * T * H * V / (q_ms * 1e-3) / 1e12}}
         gh = gw = ws_b = hidden = weight = None  # free before the next legs
         torch.cuda.empty_cache()
         # forward only, Llama-like shape
@@ -623,6 +649,13 @@ def run_gpu(args):
         lmh.lmhead_timing_enable(False)
         dk_ms = sum(drec) / len(drec)
         dgbs = T3 * V3 * 2 / (dk_ms * 1e-3) / 1e9
+        q3 = torch.empty(T3, device=dev)
+        sq = lambda: lmh.logprob_from_logits_stats(x, l3, 1.0, out_logprob=lp3,  # noqa: E731
+                                                   out_entropy=ent3, out_sum_p2=q3)
+        sq_ms = kernel_ms(lmh, sq, args.steps, 3, ("logits_rowwise",))
+        extras["next_rows"]["logits_with_sum_p2"] = {
+            "kernel_ms": sq_ms, "achieved_gbs": round(T3 * V3 * 2 / (sq_ms * 1e-3) / 1e9, 1),
+            "frac": round(T3 * V3 * 2 / (sq_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         extras["logits_path"]["division_form"] = {
             "tokens_per_s": T3 / (d_ms * 1e-3), "ms": d_ms, "kernel_ms": dk_ms,
             "achieved_gbs": round(dgbs, 1), "frac": round(dgbs / peaks["hbm_gbs"], 4)}

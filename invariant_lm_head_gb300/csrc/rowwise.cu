@@ -289,9 +289,21 @@ __global__ void fwd_merge_kernel(const float* __restrict__ pm, const float* __re
   const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= T) return;
   OnlineStat st = stat_empty();
-  for (int c = 0; c < n_vunits; ++c) {
-    const int64_t o = (int64_t)c * T + row;
-    stat_merge<kQ>(st, OnlineStat{pm[o], ps[o], pu[o], kQ ? pq[o] : 0.f});
+  // Loads of kBatch chunks are issued before their merges, so a thread keeps
+  // several loads in flight; the merge order stays ascending.
+  constexpr int kBatch = 8;
+  for (int c0 = 0; c0 < n_vunits; c0 += kBatch) {
+    OnlineStat b[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (c0 + j < n_vunits) {
+        const int64_t o = (int64_t)(c0 + j) * T + row;
+        b[j] = OnlineStat{pm[o], ps[o], pu[o], kQ ? pq[o] : 0.f};
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (c0 + j < n_vunits) stat_merge<kQ>(st, b[j]);
   }
   const int lab = labels[row];
   const bool ok = lab >= 0 && (int64_t)lab < V;
@@ -429,7 +441,7 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
                              int64_t V, float* out_lp, float* out_ent, float* out_lse,
                              float* out_sum_p2, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  const int threads = 128;
+  const int threads = 64;  // T = 16384 gives 256 blocks: every SM gets rows
   const int64_t blocks = (T + threads - 1) / threads;
   if (pq && out_sum_p2)
     fwd_merge_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(
