@@ -319,10 +319,20 @@ def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
                                       s, want_lse=True)
         out["cases"].append({"batch": int(rows.numel()), "shift": shift,
                              "mismatched": compare(rows, part)})
-    perm = torch.randperm(T, generator=torch.Generator().manual_seed(11)).to(dev)
-    part = lmh.lmhead_logprob_fwd(hidden[perm].contiguous(), weight, labels[perm].contiguous(), s,
+    for seed in (11, 12, 13):  # three shuffled packings of the whole batch
+        perm = torch.randperm(T, generator=torch.Generator().manual_seed(seed)).to(dev)
+        part = lmh.lmhead_logprob_fwd(hidden[perm].contiguous(), weight,
+                                      labels[perm].contiguous(), s, want_lse=True)
+        out["cases"].append({"batch": T, "shuffled": seed, "mismatched": compare(perm, part)})
+    # the batch as T rows of a larger one: one more copy of the first 4096 rows after it
+    extra = torch.arange(0, min(T, 4096), device=dev)
+    rows = torch.cat([torch.arange(T, device=dev), extra])
+    part = lmh.lmhead_logprob_fwd(hidden[rows].contiguous(), weight, labels[rows].contiguous(), s,
                                   want_lse=True)
-    out["cases"].append({"batch": T, "shuffled": True, "mismatched": compare(perm, part)})
+    n = sum(int((bits(a[:T]) != bits(b)).sum().item()) for a, b in zip(part, full))
+    out["rows_compared"] += T
+    out["mismatched_values"] += n
+    out["cases"].append({"batch": int(rows.numel()), "embedded_rows": T, "mismatched": n})
     torch.cuda.synchronize()
     return out
 
