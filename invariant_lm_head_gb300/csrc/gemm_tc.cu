@@ -467,7 +467,11 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   const int vu_end = (p.vunit_end > 0 && p.vunit_end < all_vunits) ? p.vunit_end : all_vunits;
   if (p.vunit_begin < 0 || p.vunit_begin > vu_end) return cudaErrorInvalidValue;
   p.n_vunits = vu_end - p.vunit_begin;
-  p.n_units = p.n_m_tiles * p.n_vunits;
+  // Unit indices are int on the device; sizes whose unit count does not fit
+  // are refused (they would need terabytes of workspace anyway).
+  const long long units = static_cast<long long>(p.n_m_tiles) * p.n_vunits;
+  if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+  p.n_units = static_cast<int>(units);
   // m tiles per raster group, per contraction (same-session sweep of 4/8/16/32
   // on the Qwen-like step): the N = V contractions (forward, dlogits) share W
   // tiles across more m tiles, the K = V grad_hidden prefers small groups.
