@@ -113,3 +113,56 @@ def test_logits_paths_replay_from_a_graph(lmh):
     torch.cuda.synchronize()
     for a, b in zip(out, eager):
         assert torch.equal(_bits(a), _bits(b))
+
+
+def test_forward_from_host_replays_from_a_graph(lmh):
+    """The staged forward forks its copies onto a second stream through
+    events; captured, the fork and join become graph edges and a replay
+    copies the current host inputs."""
+    import torch
+
+    T, H, V = 200, 128, 5000
+    hidden, weight, labels, _ = fused_case(53, T, H, V, w_std=0.2)
+    h_host = W.as_torch_bf16(hidden).pin_memory()
+    w_host = W.as_torch_bf16(weight).pin_memory()
+    l_host = torch.from_numpy(labels).pin_memory()
+    dev = torch.device("cuda:0")
+    h = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    w = torch.empty(V, H, dtype=torch.bfloat16, device=dev)
+    lab = torch.empty(T, dtype=torch.int32, device=dev)
+    lp = torch.empty(T, device=dev)
+    ent = torch.empty(T, device=dev)
+    lse = torch.empty(T, device=dev)
+    ws = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, T, H, V), dtype=torch.uint8,
+                     device=dev)
+    copy_stream = torch.cuda.Stream()
+
+    def run():
+        lmh.lmhead_logprob_fwd_host(h_host, w_host, l_host, S07, hidden=h, weight=w, labels=lab,
+                                    out_logprob=lp, out_entropy=ent, out_lse=lse, workspace=ws,
+                                    copy_stream=copy_stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (lp, ent, lse)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    h.zero_(), w.zero_(), lp.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(w.cpu(), w_host)
+    for a, b in zip((lp, ent, lse), eager):
+        assert torch.equal(_bits(a), _bits(b))
+    # new host contents are copied by the next replay
+    h_host.copy_(W.as_torch_bf16(W.random_bf16(54, (T, H), 1.0)))
+    graph.replay()
+    torch.cuda.synchronize()
+    ref = lmh.lmhead_logprob_fwd(h, w, lab, S07, want_lse=True)
+    assert torch.equal(h.cpu(), h_host)
+    for a, b in zip((lp, ent, lse), ref):
+        assert torch.equal(_bits(a), _bits(b))
