@@ -151,7 +151,8 @@ def _bwd(lmh, hidden, weight, labels, grad, s, pass_lse=True):
 
 @pytest.mark.parametrize("pass_lse", [True, False])
 @pytest.mark.parametrize("s", [1.0, S07])
-@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (64, 256, 4096), (3, 8, 16)])
+@pytest.mark.parametrize("T,H,V", [(300, 264, 5000), (64, 256, 4096), (3, 8, 16), (5, 8, 1),
+                                   (9, 16, 7), (130, 24, 1031)])
 def test_fused_backward_matches_oracle(lmh, T, H, V, s, pass_lse):
     hidden, weight, labels, grad = fused_case(31, T, H, V, w_std=0.05, oov=[(T - 1, -100)])
     gh, gw = _bwd(lmh, hidden, weight, labels, grad, s, pass_lse)
