@@ -552,13 +552,22 @@ def run_gpu(args):
         grad.copy_(g_host, non_blocking=True)
         bwd()
 
+    # the host-to-device copy rate these inputs see (pinned memory, one stream)
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    weight.copy_(w_host, non_blocking=True)
+    c0.record()
+    weight.copy_(w_host, non_blocking=True)
+    c1.record()
+    torch.cuda.synchronize()
+    h2d_gbs = w_host.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     barrier(ws)
     e2e_ms = reduce_max(timed(e2e_step, args.steps, 2) * args.steps, ws, dev)
     h2d = sum(t.numel() * t.element_size() for t in (h_host, w_host, l_host, g_host))
     line["e2e"] = {"value": aggregate_tokens_per_s(T, ws, args.steps, e2e_ms), "unit": "tokens/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 2 * T * 4,
                    "path": "lmhead_logprob_fwd_host (pinned host inputs, copies overlapped with "
-                           "the forward) + lmhead_logprob_bwd; logprob and entropy to host"}
+                           "the forward) + lmhead_logprob_bwd; logprob and entropy to host",
+                   "h2d_copy_gbs": round(h2d_gbs, 1)}
     del h_host, w_host
 
     if ws == 1 and not args.no_extras:
