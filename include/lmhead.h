@@ -3,7 +3,8 @@
  * GPU (sm_103a). C ABI of liblmhead.so.
  *
  * What is computed (the "sampler formula"): for each token row t,
- *   z[t, v]     = s * logits[t, v]                 (s = inv_temperature, fp32)
+ *   z[t, v]     = s * logits[t, v]                 (s = inv_temperature, fp32;
+ *                 logprob_from_logits_div: logits[t, v] / t, fp32 division)
  *   logprob[t]  = z[t, label[t]] - logsumexp_v z[t, v]
  *   entropy[t]  = -sum_v p[t, v] * log p[t, v],     p = softmax(z[t, :])
  * i.e. an fp32 log_softmax over the full vocabulary followed by a gather of
@@ -18,7 +19,8 @@
  * Batch invariance: every reduction runs in an order fixed by V and H alone.
  * A row's logprob, entropy, lse and grad_hidden row are bit-identical whatever
  * batch, chunk, offset or packing the row arrives in. grad_weight sums over
- * rows: it is deterministic run to run for identical inputs, not invariant to
+ * rows: it is deterministic run to run for identical inputs on the same GPU
+ * model (its summation order also depends on the SM count), not invariant to
  * the order of rows.
  *
  * Conventions shared by all entry points
@@ -28,9 +30,12 @@
  *    backward keeps the -softmax * g term and drops the one-hot term (SkyRL
  *    page, out-of-vocab gradient fix). To ignore a padding row entirely, pass
  *    g = 0 for it.
- *  - All pointers are device pointers owned by the caller. The library never
- *    allocates, never synchronises and never reads results back: everything is
- *    enqueued on `stream` (NULL = legacy default stream) of the current device.
+ *  - All pointers are device pointers owned by the caller, except the host
+ *    buffers of lmhead_logprob_fwd_host. The library never allocates device
+ *    memory, and outside the diagnostics that say so it never synchronises or
+ *    reads results back: everything is enqueued on `stream` (NULL = legacy
+ *    default stream) of the current device. A whole step can therefore be
+ *    captured into a CUDA graph once a first call has set up the device.
  *  - Return value: LMH_OK, or an error code with nothing launched (argument
  *    errors) or with the launch failing (LMH_ERR_LAUNCH). The message of the
  *    last error of the calling thread is lmhead_last_error_string().
