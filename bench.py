@@ -642,10 +642,23 @@ def run_gpu(args):
         l3 = torch.randint(0, V3, (T3,), generator=g3, device=dev, dtype=torch.int32)
         lp3 = torch.empty(T3, device=dev)
         ent3 = torch.empty(T3, device=dev)
+        # The legs before this one keep the tensor cores at the power cap for
+        # seconds; an idle second lets the clocks settle before a leg whose
+        # issue rate matters, and this leg's own clocks are reported with it.
+        torch.cuda.synchronize()
+        time.sleep(1.0)
+        l_clocks = ClockSampler(uuid)
+        l_clocks.start()
+        t_end = time.time() + 0.6  # keep the leg loaded long enough for a few clock samples
+        while time.time() < t_end:
+            for _ in range(50):
+                lmh.logprob_from_logits(x, l3, 1.0, out_logprob=lp3, out_entropy=ent3)
+            torch.cuda.synchronize()
         lmh.lmhead_timing_enable(True)
         l_ms = timed(lambda: lmh.logprob_from_logits(x, l3, 1.0, out_logprob=lp3,
                                                      out_entropy=ent3), args.steps, 3)
         krec = [ms for name, ms in lmh.lmhead_timing_read() if name == "logits_rowwise"]
+        l_clk = l_clocks.stop()
         lmh.lmhead_timing_enable(False)
         k_ms = sum(krec) / len(krec)
         gbs = T3 * V3 * 2 / (k_ms * 1e-3) / 1e9
@@ -657,7 +670,8 @@ def run_gpu(args):
                          "frac": round(gbs / peaks["hbm_gbs"], 4),
                          "peak_source": f"hbm_gbs {peak_src}",
                          "traffic": traffic_for("logits_rowwise"),
-                         "algorithmic_bytes_per_launch": T3 * V3 * 2}}
+                         "algorithmic_bytes_per_launch": T3 * V3 * 2},
+            "clocks": l_clk}
         # sampler-parity (division) form on the same logits, and the mismatch
         # counts against torch's own fp32 sampler formula on the GPU
         temps = torch.full((T3,), 0.7, dtype=torch.float32, device=dev)
