@@ -215,6 +215,43 @@ def test_qwen_config_grad_weight_with_sparse_upstream_grad(lmh, qwen):
     assert rel_frob(got[lab_rows], ref[lab_rows]) < RTOL_FROB_GRAD
 
 
+def test_qwen_config_entropy_backward_sampled(lmh, qwen):
+    """The backward with an entropy gradient (the next row after the hot
+    path) at the full workload: grad_hidden on sampled rows, and grad_weight
+    on sampled vocabulary rows with both upstream grads zero outside 32 rows."""
+    import torch
+
+    wl, inp, w64 = qwen
+    s = wl.inv_temperature
+    h, w = to_dev_bf16(inp["hidden"]), to_dev_bf16(inp["weight"])
+    lab = to_dev(inp["labels"])
+    g_ent = np.random.default_rng(12).standard_normal(wl.T).astype(np.float32)
+    lp, ent, lse = lmh.lmhead_logprob_fwd(h, w, lab, s, want_lse=True)
+    gh, _ = lmh.lmhead_logprob_entropy_bwd(h, w, lab, to_dev(inp["grad"]), to_dev(g_ent), s,
+                                           lse=lse, entropy=ent)
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    rows = _sample_rows(wl.T, 32, 13, extra=(8191, 8192))
+    rgh = oracle.fused_grad_hidden_rows(f64(inp["hidden"][rows]), w64, inp["labels"][rows],
+                                        inp["grad"][rows], s, np.arange(len(rows)),
+                                        grad_entropy=g_ent[rows])
+    assert rel_frob(gh.float().cpu().numpy()[rows], rgh) < RTOL_FROB_GRAD
+    active = _sample_rows(wl.T, 32, 14)
+    g = np.zeros(wl.T, dtype=np.float32)
+    ge = np.zeros(wl.T, dtype=np.float32)
+    g[active] = inp["grad"][active]
+    ge[active] = g_ent[active]
+    _, gw = lmh.lmhead_logprob_entropy_bwd(h, w, lab, to_dev(g), to_dev(ge), s)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(15)
+    vrows = np.unique(np.concatenate([inp["labels"][active], rng.choice(wl.V, 100, replace=False)]))
+    ref = oracle.grad_weight_from_rows(f64(inp["hidden"][active]), w64, inp["labels"][active],
+                                       g[active], s, np.arange(len(active)), vocab_rows=vrows,
+                                       grad_entropy=ge[active])
+    got = gw[to_dev(vrows.astype(np.int64))].cpu().numpy()
+    assert rel_frob(got, ref) < RTOL_FROB_GRAD
+
+
 def test_packed_varlen_rows_identical_alone_and_shuffled(lmh):
     import torch
 
