@@ -709,7 +709,8 @@ def run_gpu(args):
 
 
 def run_case(args):
-    """One kernel family on one shape, for profiling: --case fwd|bwd|logits|logits_div --shape ..."""
+    """One kernel family on one shape, for profiling: --case fwd|bwd|logits|logits_div|logits_stats
+    --shape ..."""
     import torch
 
     import invariant_lm_head_gb300 as lmh
@@ -719,7 +720,7 @@ def run_case(args):
     lmh.build()
     dims = [int(x) for x in args.shape.split(",")]
     s = inv_temperature()
-    if args.case in ("logits", "logits_div"):
+    if args.case in ("logits", "logits_div", "logits_stats"):
         T, V = dims
         g = torch.Generator(device=dev)
         g.manual_seed(7)
@@ -731,6 +732,10 @@ def run_case(args):
         if args.case == "logits":
             fn = lambda: lmh.logprob_from_logits(x, lab, s, out_logprob=lp,  # noqa: E731
                                                  out_entropy=ent)
+        elif args.case == "logits_stats":
+            q = torch.empty(T, device=dev)
+            fn = lambda: lmh.logprob_from_logits_stats(x, lab, s, out_logprob=lp,  # noqa: E731
+                                                       out_entropy=ent, out_sum_p2=q)
         else:
             temps = torch.full((T,), 0.7, dtype=torch.float32, device=dev)
             fn = lambda: lmh.logprob_from_logits_div(x, lab, temps, out_logprob=lp,  # noqa: E731
@@ -784,7 +789,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip fwd-only and logits-path legs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_div"], default=None,
+    ap.add_argument("--case", choices=["fwd", "bwd", "logits", "logits_div", "logits_stats"],
+                    default=None,
                     help="time one entry point on --shape only (profiling aid; no contract line)")
     ap.add_argument("--shape", default="4096,4096,32000", help="T,H,V (fwd/bwd) or T,V (logits)")
     args = ap.parse_args(argv)
