@@ -362,6 +362,60 @@ def _logits(name, logits, labels, inv_temperature, out_logprob, out_entropy, out
     return out_logprob, out_entropy, out_lse, out_sum_p2
 
 
+_LOGPROB_FN = None
+
+
+def _logprob_function():
+    """The autograd Function behind lmhead_logprob, built on first use (torch
+    is imported lazily so that the module loads without it)."""
+    global _LOGPROB_FN
+    if _LOGPROB_FN is not None:
+        return _LOGPROB_FN
+    torch = _torch()
+
+    class _LMHeadLogprob(torch.autograd.Function):
+        @staticmethod
+        def forward(ctx, hidden, weight, labels, inv_temperature):
+            lp, ent, lse = lmhead_logprob_fwd(hidden, weight, labels, inv_temperature,
+                                              want_lse=True)
+            ctx.save_for_backward(hidden, weight, labels, lse, ent)
+            ctx.inv_temperature = inv_temperature
+            ctx.set_materialize_grads(False)
+            return lp, ent
+
+        @staticmethod
+        def backward(ctx, grad_logprob, grad_entropy):
+            hidden, weight, labels, lse, ent = ctx.saved_tensors
+            if grad_logprob is None and grad_entropy is None:
+                return None, None, None, None
+            s = ctx.inv_temperature
+            g = None if grad_logprob is None else grad_logprob.float().contiguous()
+            if grad_entropy is None:
+                gh, gw = lmhead_logprob_bwd(hidden, weight, labels, g, s, lse=lse)
+            else:
+                gh, gw = lmhead_logprob_entropy_bwd(hidden, weight, labels, g,
+                                                    grad_entropy.float().contiguous(), s,
+                                                    lse=lse, entropy=ent)
+            return (gh if ctx.needs_input_grad[0] else None,
+                    gw.to(weight.dtype) if ctx.needs_input_grad[1] else None, None, None)
+
+    _LOGPROB_FN = _LMHeadLogprob
+    return _LOGPROB_FN
+
+
+def lmhead_logprob(hidden, weight, labels, inv_temperature: float = 1.0):
+    """Differentiable fused LM-head log-probs: (logprob, entropy), f32 [T].
+
+    Forward is lmhead_logprob_fwd; backward is lmhead_logprob_bwd, or
+    lmhead_logprob_entropy_bwd when the entropy output also receives a
+    gradient. hidden bf16 [T, H] and weight bf16 [V, H] get bf16 gradients
+    (grad_weight is accumulated in fp32 by the library and rounded once to
+    the weight's dtype; call lmhead_logprob_bwd directly to keep it in fp32).
+    labels int32 [T] get none.
+    """
+    return _logprob_function().apply(hidden, weight, labels, float(inv_temperature))
+
+
 def lmhead_kernel_launches() -> int:
     """Kernels launched by the library in this process so far."""
     return int(library().lmhead_kernel_launches())

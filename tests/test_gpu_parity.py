@@ -451,3 +451,37 @@ def test_division_form_is_ieee_division_for_every_bf16_input(lmh):
            rng.integers(0, 1 << 23, size=300)]
     bad = {t: n for t in ts if (n := lmh.lmhead_selftest_division(t)) != 0}
     assert not bad, bad
+
+
+# ----------------------------------------------------------------- autograd wrapper
+@pytest.mark.parametrize("use_entropy", [False, True])
+def test_autograd_wrapper_matches_the_direct_calls(lmh, use_entropy):
+    """loss.backward() through lmhead_logprob runs the library's backward:
+    the same bits as calling it directly, and within tolerance of the oracle."""
+    import torch
+
+    T, H, V = 300, 264, 5000
+    hidden, weight, labels, grad = fused_case(61, T, H, V, w_std=0.2, oov=((2, -100),))
+    g_ent = W.random_f32(62, T)
+    h = to_dev_bf16(hidden).requires_grad_(True)
+    w = to_dev_bf16(weight).requires_grad_(True)
+    lab, g, ge = to_dev(labels), to_dev(grad), to_dev(g_ent)
+    lp, ent = lmh.lmhead_logprob(h, w, lab, S07)
+    loss = (lp * g).sum() + ((ent * ge).sum() if use_entropy else 0.0)
+    loss.backward()
+    torch.cuda.synchronize()
+    with torch.no_grad():
+        lp0, ent0, lse0 = lmh.lmhead_logprob_fwd(h.detach(), w.detach(), lab, S07, want_lse=True)
+        if use_entropy:
+            gh0, gw0 = lmh.lmhead_logprob_entropy_bwd(h.detach(), w.detach(), lab, g, ge, S07,
+                                                      lse=lse0, entropy=ent0)
+        else:
+            gh0, gw0 = lmh.lmhead_logprob_bwd(h.detach(), w.detach(), lab, g, S07, lse=lse0)
+    torch.cuda.synchronize()
+    assert torch.equal(lp.detach(), lp0) and torch.equal(ent.detach(), ent0)
+    assert torch.equal(h.grad, gh0)
+    assert torch.equal(w.grad, gw0.to(torch.bfloat16))
+    rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, S07,
+                                     grad_entropy=g_ent if use_entropy else None)
+    assert rel_frob(h.grad.float().cpu().numpy(), rgh) < RTOL_FROB_GRAD
+    assert rel_frob(w.grad.float().cpu().numpy(), rgw) < RTOL_FROB_GRAD
