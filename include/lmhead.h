@@ -81,8 +81,8 @@ struct CUstream_st; /* cudaStream_t */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 
 /*
- * Fused forward (spec entry point; SkyRL page summary for the fusion,
- * verl page for the formula).
+ * Fused forward: the vocab projection folded into the log-prob pass (SkyRL
+ * page, summary) computing the sampler formula (verl page).
  *   hidden   bf16 [T, H], 16-byte aligned, H % 8 == 0
  *   weight   bf16 [V, H] (nn.Linear layout), 16-byte aligned
  *   labels   int32 [T]
