@@ -29,7 +29,7 @@ Multi-GPU (torchrun): every rank runs its own replica of the workload on its
 own GPU (weak scaling, no data-path collective); the step time is the max over
 ranks and `value` sums the tokens of all ranks.
 
---impl reference times the fp64 CPU oracle (the reference arm of this build)
+--impl reference times the fp64 CPU oracle (the reference arm)
 on host cores, on a bounded row sample of the same workload per step.
 """
 
