@@ -240,6 +240,36 @@ def cpu_baseline(target_s: float = 15.0, rows: int = 128):
                       f"incl. grad_weight over the sampled rows, repeated {n}x in {dt:.1f} s"}
 
 
+def cpu_oracle_logits(target_s: float = 3.0, rows: int = 64, divide: bool = False):
+    """fp64 oracle of the sampler formula (or its division form) on a row
+    sample of the logits workload, repeated for about target_s seconds."""
+    import oracle
+    import workloads as W
+
+    inp = W.logits_inputs(W.LOGITS, T=rows)
+    x = W.bf16_bits_to_f32(inp["logits"])
+    lab = inp["labels"]
+
+    def step():
+        if divide:
+            oracle.logprob_from_logits_div(x, lab, 0.7)
+        else:
+            oracle.logprob_from_logits(x, lab, 1.0)
+
+    step()
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        step()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= target_s or n >= 100:
+            break
+    return {"value": rows * n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{rows} rows of the logits workload (V={W.LOGITS.V}), fp64, "
+                      f"repeated {n}x in {dt:.1f} s"}
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -693,6 +723,9 @@ def run_gpu(args):
             "tokens_per_s": T3 / (d_ms * 1e-3), "ms": d_ms, "kernel_ms": dk_ms,
             "achieved_gbs": round(dgbs, 1), "frac": round(dgbs / peaks["hbm_gbs"], 4)}
         extras["sampler_parity"] = sampler_parity(lmh, x[:4096], l3[:4096])
+        if rank == 0 and not args.no_cpu_baseline:
+            extras["logits_path"]["cpu_oracle"] = cpu_oracle_logits()
+            extras["logits_path"]["division_form"]["cpu_oracle"] = cpu_oracle_logits(divide=True)
         del x
         torch.cuda.empty_cache()
         line.update(extras)
