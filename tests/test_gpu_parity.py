@@ -485,3 +485,50 @@ def test_autograd_wrapper_matches_the_direct_calls(lmh, use_entropy):
                                      grad_entropy=g_ent if use_entropy else None)
     assert rel_frob(h.grad.float().cpu().numpy(), rgh) < RTOL_FROB_GRAD
     assert rel_frob(w.grad.float().cpu().numpy(), rgw) < RTOL_FROB_GRAD
+
+
+# ----------------------------------------------------------------- chunk coverage, poisoned outputs
+@pytest.mark.parametrize("T", [127, 128, 129, 257, 16383, 16385])
+def test_every_output_element_is_written(lmh, T):
+    """Output buffers filled with NaN beforehand: every element of every output
+    must be written (finite) and match the oracle, for T at and around
+    multiples of the 128-row tile and the 16384-row backward chunk, and prime T."""
+    import torch
+
+    H, V = 64, 1000
+    hidden, weight, labels, grad = fused_case(71, T, H, V, w_std=0.2, oov=((T // 2, -100),))
+    h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
+    dev = h.device
+    nan = float("nan")
+    lp, ent, lse, q = (torch.full((T,), nan, device=dev) for _ in range(4))
+    gh = torch.full((T, H), nan, dtype=torch.bfloat16, device=dev)
+    gw = torch.full((V, H), nan, device=dev)
+    lmh.lmhead_logprob_fwd_stats(h, w, lab, S07, out_logprob=lp, out_entropy=ent, out_lse=lse,
+                                 out_sum_p2=q)
+    lmh.lmhead_logprob_bwd(h, w, lab, g, S07, lse=lse, grad_hidden=gh, grad_weight=gw)
+    torch.cuda.synchronize()
+    lmh.lmhead_device_status()
+    for t in (lp, ent, lse, q, gh.float(), gw):
+        assert bool(torch.isfinite(t).all())
+    rlp, rent, rlse = oracle.fused_forward(f64(hidden), f64(weight), labels, S07)
+    assert max_abs(lp.cpu().numpy(), rlp) < ATOL_LOGPROB
+    assert max_abs(ent.cpu().numpy(), rent) < ATOL_LOGPROB
+    rgh, rgw = oracle.fused_backward(f64(hidden), f64(weight), labels, grad, S07)
+    assert rel_frob(gh.float().cpu().numpy(), rgh) < RTOL_FROB_GRAD
+    assert rel_frob(gw.cpu().numpy(), rgw) < RTOL_FROB_GRAD
+    # the logits path and its division form into poisoned buffers
+    x = to_dev_bf16(W.f32_to_bf16_bits((f64(hidden) @ f64(weight).T).astype(np.float32)))
+    for fill in (lp, ent, lse, q):
+        fill.fill_(nan)
+    lmh.logprob_from_logits_stats(x, lab, S07, out_logprob=lp, out_entropy=ent, out_lse=lse,
+                                  out_sum_p2=q)
+    torch.cuda.synchronize()
+    for t in (lp, ent, lse, q):
+        assert bool(torch.isfinite(t).all())
+    for fill in (lp, ent, lse, q):
+        fill.fill_(nan)
+    lmh.logprob_from_logits_div(x, lab, 0.7, out_logprob=lp, out_entropy=ent, out_lse=lse,
+                                out_sum_p2=q)
+    torch.cuda.synchronize()
+    for t in (lp, ent, lse, q):
+        assert bool(torch.isfinite(t).all())
