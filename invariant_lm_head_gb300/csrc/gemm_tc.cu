@@ -357,8 +357,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld32(taddr + c * 32, v);
 
           if constexpr (E == (int)Epi::FwdStats) {
+            const f32x2 sc2 = f2_pack(p.scale2, p.scale2);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], p.scale2);
+            for (int i = 0; i < 32; i += 2) {
+              const f32x2 y2 = f2_mul(f2_pack(v[i], v[i + 1]), sc2);
+              f2_unpack(y2, v[i], v[i + 1]);
+            }
             if (nvalid == 32)
               stat_fold<32, true>(st, v);
             else
@@ -370,14 +374,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           } else {
             if constexpr (E == (int)Epi::DLogits) {
+              // per value: t = y - lse2, p = 2^t, dl = -p * (c1 * t + c0) (+ gs
+              // at the label); pairs of values share each packed operation,
+              // and -(p * coef) is p * (-c1 * t - c0) exactly.
               const int rel = lab - col0;
+              const f32x2 sc2 = f2_pack(p.scale2, p.scale2), nl2 = f2_pack(-lse2, -lse2);
+              const f32x2 nc1 = f2_pack(-c1, -c1), nc0 = f2_pack(-c0, -c0);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float t = __fmaf_rn(v[i], p.scale2, -lse2);
-                const float pr = ex2(t);
-                float d = -__fmul_rn(pr, __fmaf_rn(c1, t, c0));
-                if (i == rel) d = __fadd_rn(d, gs);
-                v[i] = d;
+              for (int i = 0; i < 32; i += 2) {
+                const f32x2 t2 = f2_fma(f2_pack(v[i], v[i + 1]), sc2, nl2);
+                float ta, tb;
+                f2_unpack(t2, ta, tb);
+                const f32x2 d2 = f2_mul(f2_pack(ex2(ta), ex2(tb)), f2_fma(nc1, t2, nc0));
+                f2_unpack(d2, v[i], v[i + 1]);
+                if (i == rel) v[i] = __fadd_rn(v[i], gs);
+                if (i + 1 == rel) v[i + 1] = __fadd_rn(v[i + 1], gs);
               }
             }
             // Stage the 128 x 32 chunk and store it with one TMA bulk store

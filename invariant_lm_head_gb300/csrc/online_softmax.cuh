@@ -65,19 +65,40 @@ __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], i
   const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
   const float s = __fmul_rn(st.s, a);
   float s0 = 0.f, s1 = 0.f, u0 = 0.f, u1 = 0.f, q0 = 0.f, q1 = 0.f;
+  if constexpr (N % 2 == 0) {
+    // the two partial sums as one packed pair: even values in the low half,
+    // odd values in the high half (y - m is y + (-m) exactly)
+    const f32x2 nm2 = f2_pack(-mn, -mn);
+    f32x2 s2 = f2_pack(0.f, 0.f), u2 = s2, q2 = s2;
 #pragma unroll
-  for (int j = 0; j < N; j += 2) {
-    const float da = (j < n) ? __fsub_rn(y[j], mn) : 0.f;
-    const float ea = (j < n) ? ex2(da) : 0.f;
-    s0 = __fadd_rn(s0, ea);
-    u0 = __fmaf_rn(ea, da, u0);
-    if (kQ) q0 = __fmaf_rn(ea, ea, q0);
-    if (j + 1 < N) {
-      const float db = (j + 1 < n) ? __fsub_rn(y[j + 1], mn) : 0.f;
-      const float eb = (j + 1 < n) ? ex2(db) : 0.f;
-      s1 = __fadd_rn(s1, eb);
-      u1 = __fmaf_rn(eb, db, u1);
-      if (kQ) q1 = __fmaf_rn(eb, eb, q1);
+    for (int j = 0; j < N; j += 2) {
+      float da, db;
+      f2_unpack(f2_add(f2_pack(y[j], y[j + 1]), nm2), da, db);
+      da = (j < n) ? da : 0.f;
+      db = (j + 1 < n) ? db : 0.f;
+      const f32x2 e2 = f2_pack((j < n) ? ex2(da) : 0.f, (j + 1 < n) ? ex2(db) : 0.f);
+      s2 = f2_add(s2, e2);
+      u2 = f2_fma(e2, f2_pack(da, db), u2);
+      if (kQ) q2 = f2_fma(e2, e2, q2);
+    }
+    f2_unpack(s2, s0, s1);
+    f2_unpack(u2, u0, u1);
+    f2_unpack(q2, q0, q1);
+  } else {
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      const float da = (j < n) ? __fsub_rn(y[j], mn) : 0.f;
+      const float ea = (j < n) ? ex2(da) : 0.f;
+      s0 = __fadd_rn(s0, ea);
+      u0 = __fmaf_rn(ea, da, u0);
+      if (kQ) q0 = __fmaf_rn(ea, ea, q0);
+      if (j + 1 < N) {
+        const float db = (j + 1 < n) ? __fsub_rn(y[j + 1], mn) : 0.f;
+        const float eb = (j + 1 < n) ? ex2(db) : 0.f;
+        s1 = __fadd_rn(s1, eb);
+        u1 = __fmaf_rn(eb, db, u1);
+        if (kQ) q1 = __fmaf_rn(eb, eb, q1);
+      }
     }
   }
   if (kQ) st.q = __fmaf_rn(st.q, __fmul_rn(a, a), __fadd_rn(q0, q1));
