@@ -57,8 +57,17 @@ __device__ __forceinline__ void stat_merge(OnlineStat& a, const OnlineStat& b) {
 template <int N, bool kQ = false>
 __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], int n = N) {
   float gmax = y[0];
+  if (n == N && N % 2 == 1) {
 #pragma unroll
-  for (int j = 1; j < N; ++j) gmax = (j < n) ? fmaxf(gmax, y[j]) : gmax;
+    for (int j = 1; j + 1 < N; j += 2) gmax = fmax3(gmax, y[j], y[j + 1]);
+  } else if (n == N) {
+#pragma unroll
+    for (int j = 1; j + 1 < N; j += 2) gmax = fmax3(gmax, y[j], y[j + 1]);
+    gmax = fmaxf(gmax, y[N - 1]);
+  } else {
+#pragma unroll
+    for (int j = 1; j < N; ++j) gmax = (j < n) ? fmaxf(gmax, y[j]) : gmax;
+  }
   const float mn = fmaxf(st.m, gmax);
   const float d0 = __fsub_rn(st.m, mn);
   const float a = ex2(d0);
