@@ -387,8 +387,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 f2_unpack(t2, ta, tb);
                 const f32x2 d2 = f2_mul(f2_pack(ex2(ta), ex2(tb)), f2_fma(nc1, t2, nc0));
                 f2_unpack(d2, v[i], v[i + 1]);
-                if (i == rel) v[i] = __fadd_rn(v[i], gs);
-                if (i + 1 == rel) v[i + 1] = __fadd_rn(v[i + 1], gs);
+              }
+              // the one-hot term, in the rare chunks that hold some row's label
+              if (__any_sync(0xffffffffu, static_cast<unsigned>(rel) < 32u)) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (i == rel) v[i] = __fadd_rn(v[i], gs);
               }
             }
             // Stage the 128 x 32 chunk and store it with one TMA bulk store
