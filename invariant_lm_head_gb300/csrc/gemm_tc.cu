@@ -357,20 +357,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld32(taddr + c * 32, v);
 
           if constexpr (E == (int)Epi::FwdStats) {
-            const f32x2 sc2 = f2_pack(p.scale2, p.scale2);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const f32x2 y2 = f2_mul(f2_pack(v[i], v[i + 1]), sc2);
-              f2_unpack(y2, v[i], v[i + 1]);
-            }
+            // y = acc * scale2 (the temperature and log2(e)), folded into
+            // the statistics' shift; the label's y is formed on its own
             if (nvalid == 32)
-              stat_fold<32, true>(st, v);
+              stat_fold_scaled<32, true>(st, v, p.scale2);
             else
-              stat_fold<32, true>(st, v, nvalid);
+              stat_fold_scaled<32, true>(st, v, p.scale2, nvalid);
             const int rel = lab - col0;
             if (__any_sync(0xffffffffu, rel >= 0 && rel < nvalid)) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) zl = (i == rel) ? v[i] : zl;
+              for (int i = 0; i < 32; ++i) zl = (i == rel) ? __fmul_rn(v[i], p.scale2) : zl;
             }
           } else {
             if constexpr (E == (int)Epi::DLogits) {

@@ -116,6 +116,51 @@ __device__ __forceinline__ void stat_fold(OnlineStat& st, const float (&y)[N], i
   st.m = mn;
 }
 
+// As stat_fold on y = x * c (c > 0), with the scale folded into the shift:
+// the max is taken on the raw values (max commutes with the positive scale),
+// m = max y is that max times c, and each d = x * c - m is one FMA. The values
+// go through the fp32 steps as packed pairs, even indices in the low half.
+template <int N, bool kQ = false>
+__device__ __forceinline__ void stat_fold_scaled(OnlineStat& st, const float (&x)[N], float c,
+                                                 int n = N) {
+  static_assert(N % 2 == 0, "pairs of values");
+  float gmax = x[0];
+  if (n == N) {
+#pragma unroll
+    for (int j = 1; j + 1 < N; j += 2) gmax = fmax3(gmax, x[j], x[j + 1]);
+    gmax = fmaxf(gmax, x[N - 1]);
+  } else {
+#pragma unroll
+    for (int j = 1; j < N; ++j) gmax = (j < n) ? fmaxf(gmax, x[j]) : gmax;
+  }
+  const float mn = fmaxf(st.m, __fmul_rn(gmax, c));
+  const float d0 = __fsub_rn(st.m, mn);
+  const float a = ex2(d0);
+  const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
+  const float s = __fmul_rn(st.s, a);
+  const f32x2 c2 = f2_pack(c, c), nm2 = f2_pack(-mn, -mn);
+  f32x2 s2 = f2_pack(0.f, 0.f), u2 = s2, q2 = s2;
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    float da, db;
+    f2_unpack(f2_fma(f2_pack(x[j], x[j + 1]), c2, nm2), da, db);
+    da = (j < n) ? da : 0.f;
+    db = (j + 1 < n) ? db : 0.f;
+    const f32x2 e2 = f2_pack((j < n) ? ex2(da) : 0.f, (j + 1 < n) ? ex2(db) : 0.f);
+    s2 = f2_add(s2, e2);
+    u2 = f2_fma(e2, f2_pack(da, db), u2);
+    if (kQ) q2 = f2_fma(e2, e2, q2);
+  }
+  float s0, s1, u0, u1, q0, q1;
+  f2_unpack(s2, s0, s1);
+  f2_unpack(u2, u0, u1);
+  f2_unpack(q2, q0, q1);
+  if (kQ) st.q = __fmaf_rn(st.q, __fmul_rn(a, a), __fadd_rn(q0, q1));
+  st.s = __fadd_rn(s, __fadd_rn(s0, s1));
+  st.u = __fadd_rn(u, __fadd_rn(u0, u1));
+  st.m = mn;
+}
+
 // How a bf16 logit x becomes y = z * log2(e), z the temperature-scaled logit.
 // ScaleMul multiplies by the inverse temperature s, folded with log2(e) into one
 // factor c = s * log2(e): y = x * c, and the shifted value y - m is one FMA.
