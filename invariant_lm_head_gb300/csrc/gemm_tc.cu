@@ -206,21 +206,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             const uint32_t sA = smem_base + stage * kStageBytes;
             mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-            if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
+            auto load_a = [&]() {
+              if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
 #pragma unroll
-              for (int j = 0; j < kBM / 64; ++j)
-                tma_load_2d(sA + j * kMnBoxBytes, &tmA, full_bar(stage), m_tile * kBM + 64 * j,
-                            kb * kBK);
-            } else {
-              tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
-            }
-            if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
+                for (int j = 0; j < kBM / 64; ++j)
+                  tma_load_2d(sA + j * kMnBoxBytes, &tmA, full_bar(stage),
+                              m_tile * kBM + 64 * j, kb * kBK);
+              } else {
+                tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+              }
+            };
+            auto load_b = [&]() {
+              if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
 #pragma unroll
-              for (int j = 0; j < kBN / 64; ++j)
-                tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
-                            n_tile * kBN + 64 * j, kb * kBK);
+                for (int j = 0; j < kBN / 64; ++j)
+                  tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
+                              n_tile * kBN + 64 * j, kb * kBK);
+              } else {
+                tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+              }
+            };
+            // The forward and dlogits stream W as B: B first, so the DRAM
+            // loads start before A's (small, L2-resident, or for short batches
+            // mostly out-of-bounds zero fill). The other contractions stream
+            // A and measured faster with A first.
+            if (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
+              load_b();
+              load_a();
             } else {
-              tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+              load_a();
+              load_b();
             }
             ++issued;
             if (++stage == kStages) {
