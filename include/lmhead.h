@@ -232,6 +232,45 @@ int lmhead_logprob_fwd_host(const uint16_t* hidden_host, const uint16_t* weight_
                             struct CUstream_st* copy_stream);
 
 /*
+ * The forward split by vocabulary shards, for a vocab-parallel (tensor-
+ * parallel) LM head whose ranks each hold rows [v_offset, v_offset + V) of
+ * the weight. The pages' vocab-parallel log-softmax (SkyRL page, the chunked
+ * distributed log-prob) exchanges per-row max / sum-exp / label-logit
+ * statistics between ranks; here the statistics are the forward's own
+ * per-1024-column partials, so the merged result is bit-identical to
+ * lmhead_logprob_fwd on the whole weight, whatever the number of shards.
+ *
+ * lmhead_logprob_fwd_partials: this shard's statistics.
+ *   hidden bf16 [T, H], weight bf16 [V, H] (the shard), labels int32 [T] as
+ *   indices into the whole vocabulary.
+ *   v_offset  the shard's first row, a multiple of 1024 (LMH_ERR_ALIGNMENT
+ *             otherwise); every shard but the last should hold a multiple
+ *             of 1024 rows so that the shards' chunks tile the vocabulary
+ *   part_m, part_s, part_u  f32 planes [ceil(V / 1024)][T] receiving the
+ *             chunks' base-2 max, sum and entropy accumulators. Point them at
+ *             chunk v_offset / 1024 of the whole-vocabulary planes
+ *             [ceil(V_total / 1024)][T].
+ *   label_logit f32 [T]: the scaled label logit (base 2) of rows whose label
+ *             is in this shard, 0 for every other row. Summing the shards'
+ *             buffers gives every row its value: exactly one term is nonzero.
+ * lmhead_logprob_merge: the fixed-order merge of the whole-vocabulary planes
+ *   (V = V_total) and the summed label_logit, into logprob, entropy and lse
+ *   as lmhead_logprob_fwd returns them.
+ * The exchange between ranks is the caller's: all-gather each plane's slice
+ * in rank order, and sum label_logit. On one GPU, several shards of one weight
+ * write into one set of planes directly.
+ */
+int lmhead_logprob_fwd_partials(const uint16_t* hidden, const uint16_t* weight,
+                                const int32_t* labels, int64_t T, int64_t H, int64_t V,
+                                int64_t v_offset, float inv_temperature, float* part_m,
+                                float* part_s, float* part_u, float* label_logit,
+                                struct CUstream_st* stream);
+int lmhead_logprob_merge(const float* part_m, const float* part_s, const float* part_u,
+                         const float* label_logit, const int32_t* labels, int64_t T, int64_t V,
+                         float* out_logprob, float* out_entropy, float* out_lse,
+                         struct CUstream_st* stream);
+
+/*
  * Forward without a workspace, for callers that cannot allocate device memory
  * (a plugin whose host framework owns all device memory and hands out no
  * workspace, or code that must not call cudaMalloc because it can block and

@@ -53,6 +53,9 @@ SIGNATURES = {
                                   ctypes.c_size_t, _P], ctypes.c_int),
     "logprob_from_logits_stats": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P, _P], ctypes.c_int),
     "logprob_from_logits_div": ([_P, _P, _I64, _I64, _F, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "lmhead_logprob_fwd_partials": ([_P, _P, _P, _I64, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P],
+                                    ctypes.c_int),
+    "lmhead_logprob_merge": ([_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _P], ctypes.c_int),
     "lmhead_logprob_fwd_host": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P, _P, _P, _P, _P,
                                  _P, ctypes.c_size_t, _P, _P], ctypes.c_int),
     "lmhead_last_error_string": ([], ctypes.c_char_p),
@@ -360,6 +363,55 @@ def _logits(name, logits, labels, inv_temperature, out_logprob, out_entropy, out
     rc = getattr(library(), name)(*args, _stream_ptr(stream))
     _check(name, rc)
     return out_logprob, out_entropy, out_lse, out_sum_p2
+
+
+def lmhead_logprob_fwd_partials(hidden, weight_shard, labels, v_offset: int,
+                                inv_temperature: float = 1.0, *, part_m, part_s, part_u,
+                                label_logit, stream=None):
+    """One vocab shard's forward statistics (see include/lmhead.h).
+
+    part_m, part_s, part_u: f32 [ceil(V_shard / 1024), T] views into the
+    whole-vocabulary planes at chunk v_offset / 1024; label_logit f32 [T].
+    """
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight_shard, "weight_shard", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    T, H = hidden.shape
+    V = weight_shard.shape[0]
+    n = -(-V // 1024)
+    for t, nm in ((part_m, "part_m"), (part_s, "part_s"), (part_u, "part_u")):
+        _need(t, nm, torch.float32, dev, 2)
+        if tuple(t.shape) != (n, T):
+            raise ValueError(f"{nm} must be [{n}, {T}]")
+    _need(label_logit, "label_logit", torch.float32, dev, 1)
+    rc = library().lmhead_logprob_fwd_partials(
+        _ptr(hidden), _ptr(weight_shard), _ptr(labels), T, H, V, int(v_offset),
+        float(inv_temperature), _ptr(part_m), _ptr(part_s), _ptr(part_u), _ptr(label_logit),
+        _stream_ptr(stream))
+    _check("lmhead_logprob_fwd_partials", rc)
+
+
+def lmhead_logprob_merge(part_m, part_s, part_u, label_logit, labels, V: int, *,
+                         out_logprob=None, out_entropy=None, out_lse=None, stream=None):
+    """Merge whole-vocabulary planes into (logprob, entropy, lse), f32 [T]."""
+    torch = _torch()
+    dev = labels.device
+    T = labels.shape[0]
+    out_logprob = torch.empty(T, device=dev) if out_logprob is None else out_logprob
+    out_entropy = torch.empty(T, device=dev) if out_entropy is None else out_entropy
+    out_lse = torch.empty(T, device=dev) if out_lse is None else out_lse
+    n = -(-int(V) // 1024)
+    for t, nm in ((part_m, "part_m"), (part_s, "part_s"), (part_u, "part_u")):
+        _need(t, nm, torch.float32, dev, 2)
+        if tuple(t.shape) != (n, T):
+            raise ValueError(f"{nm} must be [{n}, {T}]")
+    rc = library().lmhead_logprob_merge(
+        _ptr(part_m), _ptr(part_s), _ptr(part_u), _ptr(label_logit), _ptr(labels), T, int(V),
+        _ptr(out_logprob), _ptr(out_entropy), _ptr(out_lse), _stream_ptr(stream))
+    _check("lmhead_logprob_merge", rc)
+    return out_logprob, out_entropy, out_lse
 
 
 _LOGPROB_FN = None

@@ -736,6 +736,82 @@ int logprob_from_logits_div(const uint16_t* logits, const int32_t* labels, int64
                       out_entropy, out_lse, out_sum_p2, stream);
 }
 
+int lmhead_logprob_fwd_partials(const uint16_t* hidden, const uint16_t* weight,
+                                const int32_t* labels, int64_t T, int64_t H, int64_t V,
+                                int64_t v_offset, float inv_temperature, float* part_m,
+                                float* part_s, float* part_u, float* label_logit,
+                                struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, H, V, true));
+  LMH_TRY(check_temperature(inv_temperature));
+  const int64_t unit_cols = static_cast<int64_t>(lmh::kBN) * lmh::kFwdTilesPerChunk;
+  if (v_offset < 0 || v_offset > LMH_MAX_DIM - V)
+    return fail(LMH_ERR_INVALID_ARG, "v_offset=%lld out of range", (long long)v_offset);
+  if (v_offset % unit_cols != 0)
+    return fail(LMH_ERR_ALIGNMENT, "v_offset must be a multiple of %lld", (long long)unit_cols);
+  if (T == 0) return ok();  // nothing to read or write; pointers may be NULL
+  LMH_TRY(check_ptr(hidden, 16, "hidden"));
+  LMH_TRY(check_ptr(weight, 16, "weight"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(part_m, 4, "part_m"));
+  LMH_TRY(check_ptr(part_s, 4, "part_s"));
+  LMH_TRY(check_ptr(part_u, 4, "part_u"));
+  LMH_TRY(check_ptr(label_logit, 4, "label_logit"));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // rows whose label lies in another shard keep 0, so the shards' buffers
+  // can be summed
+  LMH_TRY(launch_status(cudaMemsetAsync(label_logit, 0, static_cast<size_t>(T) * 4, st),
+                        "zero label_logit"));
+  CUtensorMap ta, tb;
+  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  lmh::GemmParams p{};
+  p.M = static_cast<int>(T);
+  p.N = static_cast<int>(V);
+  p.K = static_cast<int>(H);
+  p.status = dev->status;
+  p.scale2 = inv_temperature * lmh::kLog2e;
+  p.inv_temp = inv_temperature;
+  p.labels = labels;
+  p.label_base = v_offset;
+  p.part_m = part_m;
+  p.part_s = part_s;
+  p.part_u = part_u;
+  p.part_q = nullptr;
+  p.part_zl = label_logit;
+  p.part_ld = T;
+  LMH_LAUNCH(K_FWD_GEMM, st,
+             lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev->sms, st),
+             "forward partials");
+  return ok();
+}
+
+int lmhead_logprob_merge(const float* part_m, const float* part_s, const float* part_u,
+                         const float* label_logit, const int32_t* labels, int64_t T, int64_t V,
+                         float* out_logprob, float* out_entropy, float* out_lse,
+                         struct CUstream_st* stream) {
+  LMH_TRY(check_dims(T, 8, V, false));
+  if (T == 0) return ok();
+  LMH_TRY(check_ptr(part_m, 4, "part_m"));
+  LMH_TRY(check_ptr(part_s, 4, "part_s"));
+  LMH_TRY(check_ptr(part_u, 4, "part_u"));
+  LMH_TRY(check_ptr(label_logit, 4, "label_logit"));
+  LMH_TRY(check_ptr(labels, 4, "labels"));
+  LMH_TRY(check_ptr(out_logprob, 4, "out_logprob"));
+  LMH_TRY(check_ptr(out_entropy, 4, "out_entropy", true));
+  LMH_TRY(check_ptr(out_lse, 4, "out_lse", true));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_LAUNCH(K_FWD_MERGE, st,
+             lmh::launch_fwd_merge(part_m, part_s, part_u, nullptr, label_logit, labels, T,
+                                   n_fwd_chunks(V), V, out_logprob, out_entropy, out_lse, nullptr,
+                                   st),
+             "partials merge");
+  return ok();
+}
+
 int lmhead_logprob_fwd_host(const uint16_t* hidden_host, const uint16_t* weight_host,
                             const int32_t* labels_host, int64_t T, int64_t H, int64_t V,
                             float inv_temperature, uint16_t* hidden, uint16_t* weight,

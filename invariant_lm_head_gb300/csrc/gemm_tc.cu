@@ -334,7 +334,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int lab = -1;
       float lse2 = 0.f, gs = 0.f, c0 = 0.f, c1 = 0.f;
       if constexpr (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
-        if (row_ok) lab = p.labels[row];
+        if (row_ok) {
+          // the label as a column of this launch (a vocab shard starts at
+          // label_base); anything outside [0, N) is out of vocabulary here
+          const int64_t l = static_cast<int64_t>(p.labels[row]) - p.label_base;
+          lab = (l >= 0 && l < p.N) ? static_cast<int>(l) : -1;
+        }
       }
       if constexpr (E == (int)Epi::DLogits) {
         if (row_ok) {

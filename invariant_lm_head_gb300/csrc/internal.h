@@ -45,6 +45,7 @@ struct GemmParams {
   float scale2;    // inv_temperature * log2(e)
   float inv_temp;  // inv_temperature
   const int32_t* labels;
+  int64_t label_base;      // FwdStats / DLogits: labels are global, columns start here
   const float* grad;       // DLogits: upstream grad of logprob [M] (may be NULL = 0)
   const float* grad_ent;   // DLogits: upstream grad of entropy [M] (NULL = none)
   const float* lse;        // DLogits: natural-log lse [M]

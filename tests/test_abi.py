@@ -122,6 +122,16 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     assert fh(*args[:15], None, *args[16:]) == lmh.LMH_ERR_WORKSPACE
     assert fh(*args[:6], 0.0, *args[7:]) == lmh.LMH_ERR_INVALID_ARG
     assert fh(None, None, None, 0, 256, 4096, 1.0, *([None] * 9), 0, None, None) == lmh.LMH_OK
+    fp = lib.lmhead_logprob_fwd_partials
+    pa = [16, 16, 16, 4, 256, 4096, 0, 1.0, 16, 16, 16, 16, None]
+    assert fp(*pa[:6], 512, *pa[7:]) == lmh.LMH_ERR_ALIGNMENT  # v_offset not a chunk start
+    assert fp(*pa[:6], -1024, *pa[7:]) == lmh.LMH_ERR_INVALID_ARG
+    assert fp(*pa[:11], None, None) == lmh.LMH_ERR_INVALID_ARG  # label_logit missing
+    assert fp(None, None, None, 0, 256, 4096, 2048, 1.0, None, None, None, None, None) == lmh.LMH_OK
+    assert lib.lmhead_logprob_merge(16, 16, 16, 16, 16, 4, 4096, None, None, None, None) == \
+        lmh.LMH_ERR_INVALID_ARG  # out_logprob missing
+    assert lib.lmhead_logprob_merge(None, None, None, None, None, 0, 4096, None, None, None,
+                                    None) == lmh.LMH_OK
     assert lib.lmhead_engine_gemm(16, 16, 8, 8, 8, 4, 16, None) == lmh.LMH_ERR_INVALID_ARG
     assert lib.lmhead_selftest_wait_timeout(10, None) == lmh.LMH_ERR_INVALID_ARG
 

@@ -532,3 +532,32 @@ def test_every_output_element_is_written(lmh, T):
     torch.cuda.synchronize()
     for t in (lp, ent, lse, q):
         assert bool(torch.isfinite(t).all())
+
+
+# ----------------------------------------------------------------- vocab shards
+@pytest.mark.parametrize("T,H,V,cuts", [(300, 264, 5000, (2048, 4096)), (64, 128, 152064, (65536,)),
+                                        (7, 64, 3072, (1024, 2048)), (130, 8, 1025, (1024,))])
+def test_vocab_shards_merge_to_the_whole_forward(lmh, T, H, V, cuts):
+    """Shards of the weight (cut at 1024-column boundaries) computed separately,
+    their label logits summed as ranks would all-reduce them, and merged: the
+    whole forward's bits."""
+    import torch
+
+    hidden, weight, labels, _ = fused_case(81, T, H, V, w_std=0.2, oov=((0, -100),))
+    h, w, lab = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels)
+    dev = h.device
+    n = -(-V // 1024)
+    pm, ps, pu = (torch.full((n, T), float("nan"), device=dev) for _ in range(3))
+    zl = torch.zeros(T, device=dev)
+    bounds = [0, *cuts, V]
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        c0, c1 = a // 1024, -(-b // 1024)
+        part = torch.full((T,), float("nan"), device=dev)
+        lmh.lmhead_logprob_fwd_partials(h, w[a:b].contiguous(), lab, a, S07, part_m=pm[c0:c1],
+                                        part_s=ps[c0:c1], part_u=pu[c0:c1], label_logit=part)
+        zl += part  # one shard holds each row's label; the others contribute 0
+    lp, ent, lse = lmh.lmhead_logprob_merge(pm, ps, pu, zl, lab, V)
+    ref = lmh.lmhead_logprob_fwd(h, w, lab, S07, want_lse=True)
+    torch.cuda.synchronize()
+    for x, y in zip((lp, ent, lse), ref):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
