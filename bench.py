@@ -20,6 +20,8 @@ Prints ONE JSON line (rank 0). Besides the contract keys it carries:
                  formula on [4096, 152064] logits
   next_rows      the entropy-gradient step and the sum_pi_squared variants of
                  the forward and of the logits path, on the same workloads
+  vocab_shards_fwd  the forward as two vocab shards plus the merge (what a
+                 vocab-parallel rank pair runs), on one GPU
   cpu_baseline   the fp64 CPU oracle timed on a bounded sample on host cores
   e2e            the same step from pinned host inputs: the host-staged
                  forward (copies overlapped with the forward) and the
@@ -640,6 +642,29 @@ def run_gpu(args):
                                                   out_logprob=lp, out_entropy=ent, out_lse=lse,
                                                   out_sum_p2=q2, workspace=ws_f)
         q_ms = kernel_ms(lmh, fq, args.steps, 2, fwd_kernels)
+        # vocab shards (two, cut at a 1024-column boundary) and the merge, as a
+        # vocab-parallel rank pair would run them, on one GPU
+        n_chunks = n_fwd_chunks(V)
+        pm_ = torch.empty(n_chunks, T, device=dev)
+        ps_, pu_ = torch.empty_like(pm_), torch.empty_like(pm_)
+        zl_a, zl_b = torch.empty(T, device=dev), torch.empty(T, device=dev)
+        cut = (n_chunks // 2) * 1024
+        w_a, w_b = weight[:cut], weight[cut:]
+
+        def sharded():
+            lmh.lmhead_logprob_fwd_partials(hidden, w_a, labels, 0, s, part_m=pm_[:cut // 1024],
+                                            part_s=ps_[:cut // 1024], part_u=pu_[:cut // 1024],
+                                            label_logit=zl_a)
+            lmh.lmhead_logprob_fwd_partials(hidden, w_b, labels, cut, s,
+                                            part_m=pm_[cut // 1024:], part_s=ps_[cut // 1024:],
+                                            part_u=pu_[cut // 1024:], label_logit=zl_b)
+            zl_a.add_(zl_b)
+            lmh.lmhead_logprob_merge(pm_, ps_, pu_, zl_a, labels, V, out_logprob=lp,
+                                     out_entropy=ent, out_lse=lse)
+
+        sh_ms = kernel_ms(lmh, sharded, args.steps, 2, fwd_kernels)
+        extras["vocab_shards_fwd"] = {"shards": 2, "ms_kernels": sh_ms,
+                                      "tflops": 2.0 * T * H * V / (sh_ms * 1e-3) / 1e12}
         extras["next_rows"] = {
             "entropy_grad_fwd_bwd": {"ms_kernels_per_step": e_ms, "tokens_per_s": T / (e_ms * 1e-3),
                                      "tflops_as_executed": 8.0 * T * H * V / (e_ms * 1e-3) / 1e12},
