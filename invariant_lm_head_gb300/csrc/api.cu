@@ -324,7 +324,7 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
                 float* out_sum_p2 = nullptr, const std::vector<FwdSlice>* slices = nullptr) {
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
-  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));
   lmh::GemmParams p{};
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
@@ -529,7 +529,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
     const uint16_t* h_c = hidden + c0 * H;
     CUtensorMap t_w, t_h, t_ht, t_dl, t_dl_mn;
-    LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBN));        // [V][K=H]
+    LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));   // [V][K=H]
     LMH_TRY(make_tmap(&t_h, h_c, H, rows, H * 2, lmh::kBK, lmh::kBM));        // [rows][K=H]
     LMH_TRY(make_tmap(&t_ht, w.ht, rows, H, w.tcpad * 2, lmh::kBK, lmh::kBM)); // [M=H][K=rows]
     LMH_TRY(make_tmap(&t_dl, w.dl, V, rows, w.vpad * 2, lmh::kBK, lmh::kBM)); // [rows][K=V]
@@ -765,7 +765,7 @@ int lmhead_logprob_fwd_partials(const uint16_t* hidden, const uint16_t* weight,
                         "zero label_logit"));
   CUtensorMap ta, tb;
   LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
-  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN));
+  LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));
   lmh::GemmParams p{};
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
@@ -959,7 +959,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   if (b_mn)
     LMH_TRY(make_tmap(&tb, B, N, K, N * 2, 64, lmh::kBK));
   else
-    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBN));
+    LMH_TRY(make_tmap(&tb, B, K, N, K * 2, lmh::kBK, lmh::kBBoxRows));
   lmh::GemmParams p{};
   p.status = dev->status;
   p.M = static_cast<int>(M);

@@ -44,6 +44,7 @@
 // bits are fixed by the inputs, the row chunking and the SM count.
 #include <cfloat>
 #include <cstdint>
+#include <cstdlib>
 
 #include <cuda_bf16.h>
 
@@ -55,22 +56,35 @@ namespace lmh {
 
 namespace {
 
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
-constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kMnBoxBytes = 64 * kBK * 2;  // one 64(MN) x 64(K) bf16 box
+constexpr int kABytes = kBM * kBK * 2;           // one 128-row x 64-K A box
+constexpr int kBHalfBytes = kBBoxRows * kBK * 2;  // one 128-row x 64-K B box
+constexpr int kMnBoxBytes = 64 * kBK * 2;         // one 64(MN) x 64(K) bf16 box
 constexpr int kTmemCols = 512;
 constexpr int kBarrierBytes = 256;
 // Two staging buffers for the TMA-store epilogues: 128 rows x 128 bytes
 // (32 fp32 or, using half of it, 32 bf16 columns).
 constexpr int kStagingBytes = kBM * 128;
-constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+
+// The operand ring of one CTA. Alone, a CTA stages the whole 256-row B tile
+// (48 KB a stage, 4 stages); in a CTA pair it stages half of it (32 KB a
+// stage, 6 stages), since the peer holds the other half.
+template <bool kPair>
+struct Ring {
+  static constexpr int kStages = kPair ? 6 : 4;
+  static constexpr int kBBytes = kPair ? kBHalfBytes : 2 * kBHalfBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
+  // full and empty per stage, two accumulator pairs, final; then the TMEM
+  // address, the abort flag, two epilogue go flags and the peer's load count
+  static_assert(8 * (2 * kStages + 5) + 20 <= kBarrierBytes, "barrier area too small");
+};
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
 
-// Unit u -> (m tile, N tiles). Units enumerate (m tile, vocab unit) pairs in
-// groups of group_m m tiles, unit-major inside a group, so concurrently
-// running CTAs share B tiles in L2. The order changes no value.
+// Unit u -> (m unit, N tiles). Units enumerate (m unit, vocab unit) pairs in
+// groups of group_m m units, unit-major inside a group, so concurrently
+// running CTAs share B tiles in L2. An m unit is one 128-row m tile, or two
+// for a CTA pair. The order changes no value.
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
                                             int& n_count, int& vunit) {
   const int per_group = p.group_m * p.n_vunits;
@@ -129,42 +143,59 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float 
                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
 }
 
-template <int E>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+// One CTA's share of the engine. kPair: the CTA is one of a cluster pair that
+// shares every MMA (tcgen05 cta_group::2): the pair owns a 256 x 256 tile,
+// each CTA stages the A rows of its own 128-row half and one 128-row half of
+// the B tile, and each CTA's TMEM receives its 128 rows of the accumulator.
+// CTA 0 issues the MMAs; both CTAs' copies of a stage complete on CTA 0's
+// full barrier, and CTA 0's commits free the stage and hand over the
+// accumulators in both CTAs.
+template <int E, bool kPair>
+__device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                          const CUtensorMap& tmC, const GemmParams& p) {
+  using R = Ring<kPair>;
+  constexpr int kS = R::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t staging = smem_base + kStages * kStageBytes;  // 2 x kStagingBytes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + 2 * kStagingBytes);
-  // barrier layout: full[kStages], empty[kStages], tfull[2], tempty[2], final
+  const uint32_t staging = smem_base + kS * R::kStageBytes;  // 2 x kStagingBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kS * R::kStageBytes + 2 * kStagingBytes);
+  // barrier layout: full[kS], empty[kS], tfull[2], tempty[2], final
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-  const uint32_t final_bar = bar0 + 8u * (2 * kStages + 4);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kS + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kS + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kS + 2 + a); };
+  const uint32_t final_bar = bar0 + 8u * (2 * kS + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) +
-                                                    8 * (2 * kStages + 5));
+                                                    8 * (2 * kS + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_go = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
+  // pair: the number of stage loads CTA 1 issued, published to CTA 0 at the end
+  volatile uint32_t* peer_issued = tmem_slot + 4;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // Position in the persistent schedule: a CTA pair walks the units as one.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const int first_unit = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int unit_stride = kPair ? static_cast<int>(cluster_nid_x()) : static_cast<int>(gridDim.x);
+  auto cta_m_tile = [&](int m_unit) { return kPair ? 2 * m_unit + static_cast<int>(rank) : m_unit; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(full_bar(s), 1);
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(full_bar(s), 1);  // in a pair, only CTA 0's is used: one arrive, both CTAs' bytes
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      // every epilogue thread of the pair releases the accumulator to CTA 0
+      mbar_init(tempty_bar(a), kPair ? 256 : 128);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
+    *peer_issued = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -173,57 +204,81 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (E != (int)Epi::FwdStats) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    __syncwarp();
+    cluster_sync();  // the peer's barriers are initialised before any arrive on them
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int kb_total = (p.K + kBK - 1) / kBK;
+  long long issued = 0;  // stage loads issued by this CTA's producer
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
-      long long issued = 0;
       bool ok = true;
       int wave = 0;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++wave) {
-        int m_tile, n_first, n_count, vunit;
-        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+      for (int u = first_unit; ok && u < p.n_units; u += unit_stride, ++wave) {
+        int m_unit, n_first, n_count, vunit;
+        unit_coords(p, u, m_unit, n_first, n_count, vunit);
+        const int m_tile = cta_m_tile(m_unit);
         // grad_weight walks K (the rows) downwards on odd waves, so a wave
         // starts on the operand rows the previous wave touched last, while
         // they are still in L2.
         const bool k_down = (E == (int)Epi::StoreF32T) && (wave & 1);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
+          // first B row this CTA stages: the whole tile alone, its half in a pair
+          const int b_row0 = n_tile * kBN + (kPair ? static_cast<int>(rank) * kBBoxRows : 0);
           for (int kstep = 0; kstep < kb_total; ++kstep) {
             const int kb = k_down ? kb_total - 1 - kstep : kstep;
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            const uint32_t sA = smem_base + stage * kStageBytes;
-            mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+            const uint32_t sA = smem_base + stage * R::kStageBytes;
+            const uint32_t sB = sA + kABytes;
+            // One arrive per stage, by CTA 0, expecting both CTAs' bytes; both
+            // CTAs' boxes complete on CTA 0's barrier, issued in the pair form
+            // (measured: CTA 0 issuing the plain form made the pair 10 % slower).
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (kPair ? 2 : 1) * R::kStageBytes);
+            const uint32_t fbar = kPair ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+              if constexpr (kPair)
+                tma_load_2d_pair(dst, map, fbar, x, y);
+              else
+                tma_load_2d(dst, map, fbar, x, y);
+            };
             auto load_a = [&]() {
               if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
 #pragma unroll
-                for (int j = 0; j < kBM / 64; ++j)
-                  tma_load_2d(sA + j * kMnBoxBytes, &tmA, full_bar(stage),
-                              m_tile * kBM + 64 * j, kb * kBK);
+                for (int i = 0; i < kBM / 64; ++i)
+                  load(sA + i * kMnBoxBytes, &tmA, m_tile * kBM + 64 * i, kb * kBK);
               } else {
-                tma_load_2d(sA, &tmA, full_bar(stage), kb * kBK, m_tile * kBM);
+                load(sA, &tmA, kb * kBK, m_tile * kBM);
               }
             };
             auto load_b = [&]() {
-              if (p.b_mn) {  // [K][N]: four 64(N) x 64(K) boxes
+              if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
 #pragma unroll
-                for (int j = 0; j < kBN / 64; ++j)
-                  tma_load_2d(sA + kABytes + j * kMnBoxBytes, &tmB, full_bar(stage),
-                              n_tile * kBN + 64 * j, kb * kBK);
-              } else {
-                tma_load_2d(sA + kABytes, &tmB, full_bar(stage), kb * kBK, n_tile * kBN);
+                for (int i = 0; i < R::kBBytes / kMnBoxBytes; ++i)
+                  load(sB + i * kMnBoxBytes, &tmB, b_row0 + 64 * i, kb * kBK);
+              } else {  // [N][K]: 128-row boxes
+#pragma unroll
+                for (int i = 0; i < R::kBBytes / kBHalfBytes; ++i)
+                  load(sB + i * kBHalfBytes, &tmB, kb * kBK, b_row0 + kBBoxRows * i);
               }
             };
             // The forward and dlogits stream W as B: B first, so the DRAM
@@ -238,22 +293,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               load_b();
             }
             ++issued;
-            if (++stage == kStages) {
+            if (++stage == kS) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
       }
-      if (!ok) {
+      if (kPair && rank != 0) {
+        // CTA 0 drains this CTA's copies at the end; it needs their count
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0),
+                              static_cast<uint32_t>(issued));
+      }
+      if (!ok && !kPair) {
         // Drain: wait (bounded, ignoring the abort flag) for the copies this
         // thread issued, so none lands in shared memory after the CTA exits.
         volatile int no_abort = 0;
-        const long long n = issued < kStages ? issued : kStages;
+        const long long n = issued < kS ? issued : kS;
         uint32_t s = stage, ph = phase;
         for (long long i = 0; i < n; ++i) {
           if (s == 0) {
-            s = kStages - 1;
+            s = kS - 1;
             ph ^= 1u;
           } else {
             --s;
@@ -263,14 +323,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && (!kPair || rank == 0)) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc = idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
+      const uint32_t idesc =
+          idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        int m_tile, n_first, n_count, vunit;
-        unit_coords(p, u, m_tile, n_first, n_count, vunit);
+      for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
+        int m_unit, n_first, n_count, vunit;
+        unit_coords(p, u, m_unit, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j, ++it) {
           const uint32_t acc = it & 1u;
           const uint32_t aph = (it >> 1) & 1u;
@@ -286,7 +347,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t sA = smem_base + stage * kStageBytes;
+            const uint32_t sA = smem_base + stage * R::kStageBytes;
             const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
             const uint64_t bdesc =
                 p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
@@ -297,21 +358,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t bstep = p.b_mn ? 128ull : 2ull;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc,
-                          (kb > 0 || k > 0) ? 1u : 0u);
+              const uint32_t accumulate = (kb > 0 || k > 0) ? 1u : 0u;
+              if constexpr (kPair)
+                tc_mma_bf16_pair(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, accumulate);
+              else
+                tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, accumulate);
             }
-            tc_commit(empty_bar(stage));
-            if (++stage == kStages) {
+            // the stage is free in both CTAs once these MMAs have read it
+            if constexpr (kPair)
+              tc_commit_pair(empty_bar(stage), 0x3);
+            else
+              tc_commit(empty_bar(stage));
+            if (++stage == kS) {
               stage = 0;
               phase ^= 1u;
             }
           }
-          if (ok) tc_commit(tfull_bar(acc));
+          if (ok) {
+            if constexpr (kPair)
+              tc_commit_pair(tfull_bar(acc), 0x3);
+            else
+              tc_commit(tfull_bar(acc));
+          }
         }
       }
-      // All MMAs issued by this thread must finish before TMEM is released.
+      // All MMAs issued by this thread must finish before TMEM is released
+      // (in both CTAs of a pair).
       volatile int no_abort = 0;
-      tc_commit(final_bar);
+      if constexpr (kPair)
+        tc_commit_pair(final_bar, 0x3);
+      else
+        tc_commit(final_bar);
+      mbar_wait(final_bar, 0, &no_abort, p.status);
+    } else if (kPair && lane == 0) {
+      // CTA 0's MMAs read this CTA's shared memory and write its TMEM: wait
+      // for their final commit before either is released.
+      volatile int no_abort = 0;
       mbar_wait(final_bar, 0, &no_abort, p.status);
     }
   } else {
@@ -324,11 +406,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int etid = threadIdx.x - 64;
     uint32_t it = 0, chunk_ctr = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      int m_tile, n_first, n_count, vunit;
-      unit_coords(p, u, m_tile, n_first, n_count, vunit);
+    for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
+      int m_unit, n_first, n_count, vunit;
+      unit_coords(p, u, m_unit, n_first, n_count, vunit);
+      const int m_tile = cta_m_tile(m_unit);
       const int row = m_tile * kBM + row_in_tile;
       const bool row_ok = row < p.M;
+      // a pair's second half can lie wholly past the last row: nothing to store
+      const bool tile_live = m_tile * kBM < p.M;
 
       // per-row constants
       int lab = -1;
@@ -424,7 +509,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               stage_row_bf16(buf, row_in_tile, v);
             fence_proxy_async_smem();
             named_barrier(kEpiBarrier, 128);
-            if (etid == 0) {
+            if (etid == 0 && tile_live) {
               // (x, y) of the box in the output: transposed for StoreF32T
               const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
               const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM;
@@ -438,7 +523,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(tempty_bar(acc));
+        if constexpr (kPair)
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));  // CTA 0 reissues the MMAs
+        else
+          mbar_arrive(tempty_bar(acc));
       }
       if (!ok) break;
 
@@ -459,23 +547,101 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    // Neither CTA leaves (or frees TMEM) while the other may still touch its
+    // barriers, shared memory or TMEM. Between the two cluster barriers CTA 0
+    // waits for every stage load still in flight in either CTA: all loads
+    // before the last kS of the further-ahead producer were consumed by MMAs,
+    // so their phases completed. A phase one CTA never loaded gets that
+    // CTA's share settled here (CTA 0's arrive, or CTA 1's bytes as done),
+    // so it completes when the other's bytes land. Each wait is bounded.
+    __syncwarp();
+    cluster_sync();
+    if (rank == 0 && warp == 0 && lane == 0) {
+      const long long n0 = issued, n1 = static_cast<long long>(*peer_issued);
+      const long long hi = n0 > n1 ? n0 : n1;
+      volatile int no_abort = 0;
+      for (long long i = hi > kS ? hi - kS : 0; i < hi; ++i) {
+        const int s = static_cast<int>(i % kS);
+        const uint32_t par = static_cast<uint32_t>((i / kS) & 1);
+        if (i < n0 && i >= n1)
+          mbar_complete_tx(full_bar(s), R::kStageBytes);
+        else if (i >= n0 && i < n1)
+          mbar_arrive_expect_tx(full_bar(s), R::kStageBytes);
+        mbar_wait(full_bar(s), par, &no_abort, p.status);
+      }
+    }
+    __syncwarp();
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
 template <int E>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  gemm_body<E, false>(tmA, tmB, tmC, p);
+}
+
+template <int E>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+  gemm_body<E, true>(tmA, tmB, tmC, p);
+}
+
+// Clusters of two that fit on the device at once (one CTA per SM), per device.
+template <int E>
+int pair_slots(int num_sms) {
+  static int cached[16] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 16 && cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<E>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  n = n < num_sms / 2 ? n : num_sms / 2;
+  if (dev >= 0 && dev < 16) cached[dev] = n;
+  return n;
+}
+
+template <int E>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                       const GemmParams& p, int num_sms, cudaStream_t stream) {
-  // Set on every launch: the attribute belongs to the current device's context.
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<E>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int grid = p.n_units < num_sms ? p.n_units : num_sms;  // persistent: <= one CTA per SM
-  gemm_tc_kernel<E><<<grid, kGemmThreads, kSmemBytes, stream>>>(a, b, c, p);
+                       const GemmParams& p, bool pair, int num_sms, cudaStream_t stream) {
+  cudaError_t e;
+  if (pair) {
+    // Set on every launch: the attribute belongs to the current device's context.
+    e = cudaFuncSetAttribute(gemm_tc_pair_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ring<true>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int slots = pair_slots<E>(num_sms);
+    if (slots <= 0) return cudaErrorInvalidConfiguration;
+    const int clusters = p.n_units < slots ? p.n_units : slots;  // persistent
+    gemm_tc_pair_kernel<E><<<2 * clusters, kGemmThreads, Ring<true>::kSmemBytes, stream>>>(a, b, c, p);
+  } else {
+    e = cudaFuncSetAttribute(gemm_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Ring<false>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = p.n_units < num_sms ? p.n_units : num_sms;  // persistent: <= one CTA per SM
+    gemm_tc_kernel<E><<<grid, kGemmThreads, Ring<false>::kSmemBytes, stream>>>(a, b, c, p);
+  }
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
@@ -483,7 +649,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
+size_t gemm_smem_bytes() { return Ring<false>::kSmemBytes; }
 
 cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
                         int tiles_per_unit, int num_sms, cudaStream_t stream,
@@ -491,7 +657,18 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
   CUtensorMap none{};
   const CUtensorMap& c_map = c ? *c : none;
-  p.n_m_tiles = (p.M + kBM - 1) / kBM;
+  // CTA pairs take 256-row m units. They serve the contractions whose B is
+  // read MN-major (grad_hidden, grad_weight): same-session A/B on the
+  // 16384 x 3584 x 152064 step, pairs -1 % and -5.5 % against single CTAs,
+  // but +3 % on the forward and +1 % on dlogits (K-major B). A launch with a
+  // single 128-row m tile stays on single CTAs, which keep every SM busy
+  // instead of leaving half of each pair idle.
+  const int m_tiles = (p.M + kBM - 1) / kBM;
+  const int mode = gemm_pair_mode();
+  const bool prefer = mode == 1 || (mode < 0 && (e == Epi::StoreBf16 || e == Epi::StoreF32T));
+  const bool pair = prefer && m_tiles >= 2;
+  const int m_rows = pair ? 2 * kBM : kBM;
+  p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
   p.tiles_per_unit = tiles_per_unit;
   const int all_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
@@ -503,26 +680,38 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   const long long units = static_cast<long long>(p.n_m_tiles) * p.n_vunits;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   p.n_units = static_cast<int>(units);
-  // m tiles per raster group, per contraction (same-session sweep of 4/8/16/32
-  // on the Qwen-like step): the N = V contractions (forward, dlogits) share W
-  // tiles across more m tiles, the K = V grad_hidden prefers small groups.
-  p.group_m = (e == Epi::FwdStats || e == Epi::DLogits || e == Epi::StoreF32T)
-                  ? 32
-                  : (e == Epi::StoreBf16 ? 4 : 8);
+  // Rows per raster group, per contraction (same-session sweep of 4/8/16/32
+  // 128-row m tiles on the Qwen-like step): the N = V contractions (forward,
+  // dlogits) share W tiles across more m tiles, the K = V grad_hidden
+  // prefers small groups. A pair's m unit is two m tiles.
+  const int group_tiles = (e == Epi::FwdStats || e == Epi::DLogits || e == Epi::StoreF32T)
+                              ? 32
+                              : (e == Epi::StoreBf16 ? 4 : 8);
+  p.group_m = pair ? group_tiles / 2 : group_tiles;
   if (p.n_units <= 0) return cudaSuccess;
   switch (e) {
     case Epi::FwdStats:
-      return launch_one<(int)Epi::FwdStats>(a, b, c_map, p, num_sms, stream);
+      return launch_one<(int)Epi::FwdStats>(a, b, c_map, p, pair, num_sms, stream);
     case Epi::DLogits:
-      return launch_one<(int)Epi::DLogits>(a, b, c_map, p, num_sms, stream);
+      return launch_one<(int)Epi::DLogits>(a, b, c_map, p, pair, num_sms, stream);
     case Epi::StoreBf16:
-      return launch_one<(int)Epi::StoreBf16>(a, b, c_map, p, num_sms, stream);
+      return launch_one<(int)Epi::StoreBf16>(a, b, c_map, p, pair, num_sms, stream);
     case Epi::StoreF32:
-      return launch_one<(int)Epi::StoreF32>(a, b, c_map, p, num_sms, stream);
+      return launch_one<(int)Epi::StoreF32>(a, b, c_map, p, pair, num_sms, stream);
     case Epi::StoreF32T:
-      return launch_one<(int)Epi::StoreF32T>(a, b, c_map, p, num_sms, stream);
+      return launch_one<(int)Epi::StoreF32T>(a, b, c_map, p, pair, num_sms, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+int gemm_pair_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("LMH_GEMM_CTA_PAIRS");
+    if (v && v[0] == '0') return 0;
+    if (v && v[0] == '1') return 1;
+    return -1;
+  }();
+  return mode;
 }
 
 }  // namespace lmh

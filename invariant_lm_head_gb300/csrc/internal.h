@@ -10,11 +10,13 @@ namespace lmh {
 
 // Tile shape of the tensor-core engine: one CTA owns a 128 x 256 fp32
 // accumulator in TMEM (double-buffered: 2 x 256 of the 512 columns) and walks
-// K in 64-element steps through a 4-stage TMA ring.
+// K in 64-element steps through a TMA ring. CTA pairs share each MMA of a
+// 256 x 256 tile, each CTA staging half of the B tile. K-major B operands
+// are read in 128-row boxes (two per tile alone, one per CTA of a pair).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kBBoxRows = kBN / 2;
 constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 // Forward: a vocab chunk is kFwdTilesPerChunk N-tiles (1024 columns). The
@@ -75,9 +77,13 @@ int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 
 size_t gemm_smem_bytes();
+// Which contractions run on CTA pairs (launches with two or more 128-row m
+// tiles only), from LMH_GEMM_CTA_PAIRS, read once: "0" none (0), "1" all (1),
+// unset the per-contraction default (-1). Either engine gives the same bits.
+int gemm_pair_mode();
 
-// a / b: operand maps with boxes of 64(K) x 128 rows (A) and 64(K) x 256 rows
-// (B) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map
+// a / b: operand maps with boxes of 64(K) x 128 rows (A, and B in kBBoxRows-row
+// boxes) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map
 // of the store epilogues (NULL for FwdStats): fp32 [M][N] with a 32 x 128 box
 // and 128-byte swizzle for StoreF32, fp32 [N][M] with a 128 x 32 box and no
 // swizzle for StoreF32T, bf16 [M][N] with a 32 x 128 box and

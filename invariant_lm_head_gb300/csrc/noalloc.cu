@@ -119,7 +119,7 @@ extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t
 
   CUtensorMap ta, tb;
   if ((rc = lmh::api_make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM)) != LMH_OK) return rc;
-  if ((rc = lmh::api_make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBN)) != LMH_OK) return rc;
+  if ((rc = lmh::api_make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows)) != LMH_OK) return rc;
   lmh::GemmParams p{};
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);

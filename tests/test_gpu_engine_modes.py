@@ -1,0 +1,73 @@
+"""The tensor-core engine runs a contraction either on single CTAs (128-row
+tiles) or on CTA pairs that share each MMA (256-row tiles). Which one runs
+must never change a bit: each output element's dot product walks K in the
+same order either way. Child processes force each engine (the choice is read
+once per process) on ragged shapes, including pairs whose second half lies
+wholly past the last row, and every output is compared bit for bit."""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import sys
+import torch
+sys.path.insert(0, sys.argv[2])
+import workloads as W
+import invariant_lm_head_gb300 as lmh
+
+lmh.build()
+dev = torch.device("cuda:0")
+out = {}
+for (T, H, V, s) in [(777, 520, 3001, 1 / 0.7), (129, 1024, 4099, 1.0), (300, 264, 517, 2.0)]:
+    hidden = W.as_torch_bf16(W.random_bf16(T, (T, H), 1.0)).to(dev)
+    weight = W.as_torch_bf16(W.random_bf16(T + 1, (V, H), 0.05)).to(dev)
+    labels = torch.from_numpy(W.random_labels(T, T, V)).to(dev)
+    grad = torch.from_numpy(W.random_f32(T, T)).to(dev)
+    grad_e = torch.from_numpy(W.random_f32(T + 2, T)).to(dev)
+    lp, ent, lse = lmh.lmhead_logprob_fwd(hidden, weight, labels, s, want_lse=True)
+    gh, gw = lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse)
+    gh2, gw2 = lmh.lmhead_logprob_entropy_bwd(hidden, weight, labels, grad, grad_e, s)
+    for k, v in dict(lp=lp, ent=ent, lse=lse, gh=gh, gw=gw, gh2=gh2, gw2=gw2).items():
+        out[f"{T}_{k}"] = v.cpu()
+M, N, K = 296, 264, 136
+A = W.as_torch_bf16(W.random_bf16(5, (M, K), 1.0)).to(dev)
+B = W.as_torch_bf16(W.random_bf16(6, (N, K), 1.0)).to(dev)
+for ak in (True, False):
+    for bk in (True, False):
+        a = A if ak else A.t().contiguous()
+        b = B if bk else B.t().contiguous()
+        out[f"gemm_{int(ak)}{int(bk)}"] = lmh.lmhead_engine_gemm(a, b, a_kmajor=ak, b_kmajor=bk).cpu()
+torch.cuda.synchronize()
+assert lmh.lmhead_device_status() == 0
+torch.save(out, sys.argv[1])
+'''
+
+
+def test_pair_and_single_engines_give_identical_bits(tmp_path):
+    import torch
+
+    child = tmp_path / "child.py"
+    child.write_text(CHILD)
+    got = {}
+    for mode in ("0", "1"):
+        path = tmp_path / f"out{mode}.pt"
+        env = dict(os.environ, LMH_GEMM_CTA_PAIRS=mode)
+        r = subprocess.run([sys.executable, str(child), str(path), ROOT], env=env, cwd=ROOT,
+                           capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0, r.stderr[-2000:]
+        got[mode] = torch.load(path)
+    single, pair = got["0"], got["1"]
+    assert single.keys() == pair.keys()
+    for k in single:
+        a, b = single[k], pair[k]
+        assert a.shape == b.shape, k
+        same = torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                           b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+        assert same, f"{k}: the single-CTA and CTA-pair engines differ"

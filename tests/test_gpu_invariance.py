@@ -115,6 +115,10 @@ def test_grad_hidden_rows_invariant_across_batches(lmh):
             r1 = min(T, r0 + bs)
             gh, _ = lmh.lmhead_logprob_bwd(h[r0:r1], w, lab[r0:r1], g[r0:r1], S07)
             assert torch.equal(gh, gh_full[r0:r1]), (bs, r0)
+    # shifts that move rows between the two 128-row halves of a CTA pair's tile
+    for shift in (1, 127, 128, 129, 255):
+        gh, _ = lmh.lmhead_logprob_bwd(h[shift:], w, lab[shift:], g[shift:], S07)
+        assert torch.equal(gh, gh_full[shift:]), shift
     perm = torch.randperm(T, generator=torch.Generator().manual_seed(5)).to(h.device)
     gh, _ = lmh.lmhead_logprob_bwd(h[perm].contiguous(), w, lab[perm].contiguous(),
                                    g[perm].contiguous(), S07)
