@@ -657,15 +657,16 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
   CUtensorMap none{};
   const CUtensorMap& c_map = c ? *c : none;
-  // CTA pairs take 256-row m units. They serve the contractions whose B is
-  // read MN-major (grad_hidden, grad_weight): same-session A/B on the
-  // 16384 x 3584 x 152064 step, pairs -1 % and -5.5 % against single CTAs,
-  // but +3 % on the forward and +1 % on dlogits (K-major B). A launch with a
-  // single 128-row m tile stays on single CTAs, which keep every SM busy
-  // instead of leaving half of each pair idle.
+  // CTA pairs take 256-row m units and serve grad_weight. Same-session A/B
+  // of the 16384 x 3584 x 152064 step, which runs at the power cap: pairs
+  // for grad_weight alone -1 % on the step against none; adding grad_hidden
+  // (whose pair raster reads about 1.6x the DRAM bytes) or the K-major-B
+  // contractions gave the gain back. A launch with a single 128-row m tile
+  // stays on single CTAs, which keep every SM busy instead of leaving half of
+  // each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int mode = gemm_pair_mode();
-  const bool prefer = mode == 1 || (mode < 0 && (e == Epi::StoreBf16 || e == Epi::StoreF32T));
+  const bool prefer = mode == 1 || (mode < 0 && e == Epi::StoreF32T);
   const bool pair = prefer && m_tiles >= 2;
   const int m_rows = pair ? 2 * kBM : kBM;
   p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
