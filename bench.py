@@ -557,6 +557,12 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (weight 1.09 GB); no flush"},
         "gpu_launches": launches, "roofline": roofline, "kernels": kernels, "clocks": clk,
         "model_tflops_per_gpu": 6.0 * T * H * V / (ms_per_step * 1e-3) / 1e12,
+        # the whole step against the same sustained rate: 8THV flops as executed
+        # (forward, recomputed logits, grad_hidden, grad_weight)
+        "step_tensor": {"flops_per_step": 8.0 * T * H * V,
+                        "achieved_tflops": round(8.0 * T * H * V / (ms_per_step * 1e-3) / 1e12, 1),
+                        "peak": peak, "frac": round(8.0 * T * H * V / (ms_per_step * 1e-3) / 1e12
+                                                    / peak, 4)},
     }
 
     # ------------------------------------------------- batch invariance (bit mismatches)

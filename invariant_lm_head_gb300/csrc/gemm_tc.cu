@@ -9,13 +9,19 @@
 //
 // One persistent CTA per SM, warp-specialised:
 //   warp 0      TMA producer: a 128x64 A tile and a 256x64 B tile per stage
-//               (one box each when K-major, 64-wide boxes when MN-major), 4 stages
+//               (128-row boxes when K-major, 64-wide boxes when MN-major), 4 stages
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=256, K=16, four per 64-wide stage) into one of two
 //               256-column accumulators, and tcgen05.commit frees the stage
 //   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
+//
+// CTA pairs (grad_weight): a cluster of two CTAs owns a 256x256 tile. Each
+// CTA stages its own 128 A rows and one 128-row half of B (6 stages of 32 KB);
+// CTA 0 issues tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives
+// its 128 accumulator rows, so the epilogue is the same. Both engines walk K
+// in the same MMA order and give the same bits.
 //
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
