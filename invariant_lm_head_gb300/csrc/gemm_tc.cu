@@ -469,11 +469,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
           if constexpr (E == (int)Epi::FwdStats) {
             // y = acc * scale2 (the temperature and log2(e)), folded into
-            // the statistics' shift; the label's y is formed on its own
-            if (nvalid == 32)
-              stat_fold_scaled<32, true>(st, v, p.scale2);
-            else
-              stat_fold_scaled<32, true>(st, v, p.scale2, nvalid);
+            // the statistics' shift; the label's y is formed on its own. The
+            // sum of p^2 is accumulated only when a plane for it was given
+            // (m, s and u do not depend on it).
+            if (p.part_q) {
+              if (nvalid == 32)
+                stat_fold_scaled<32, true>(st, v, p.scale2);
+              else
+                stat_fold_scaled<32, true>(st, v, p.scale2, nvalid);
+            } else {
+              if (nvalid == 32)
+                stat_fold_scaled<32, false>(st, v, p.scale2);
+              else
+                stat_fold_scaled<32, false>(st, v, p.scale2, nvalid);
+            }
             const int rel = lab - col0;
             if (__any_sync(0xffffffffu, rel >= 0 && rel < nvalid)) {
 #pragma unroll
@@ -487,13 +496,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               const int rel = lab - col0;
               const f32x2 sc2 = f2_pack(p.scale2, p.scale2), nl2 = f2_pack(-lse2, -lse2);
               const f32x2 nc1 = f2_pack(-c1, -c1), nc0 = f2_pack(-c0, -c0);
+              if (p.grad_ent) {
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const f32x2 t2 = f2_fma(f2_pack(v[i], v[i + 1]), sc2, nl2);
-                float ta, tb;
-                f2_unpack(t2, ta, tb);
-                const f32x2 d2 = f2_mul(f2_pack(ex2(ta), ex2(tb)), f2_fma(nc1, t2, nc0));
-                f2_unpack(d2, v[i], v[i + 1]);
+                for (int i = 0; i < 32; i += 2) {
+                  const f32x2 t2 = f2_fma(f2_pack(v[i], v[i + 1]), sc2, nl2);
+                  float ta, tb;
+                  f2_unpack(t2, ta, tb);
+                  const f32x2 d2 = f2_mul(f2_pack(ex2(ta), ex2(tb)), f2_fma(nc1, t2, nc0));
+                  f2_unpack(d2, v[i], v[i + 1]);
+                }
+              } else {
+                // no entropy term: the coefficient is the constant -c0
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                  float ta, tb;
+                  f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), sc2, nl2), ta, tb);
+                  const f32x2 d2 = f2_mul(f2_pack(ex2(ta), ex2(tb)), nc0);
+                  f2_unpack(d2, v[i], v[i + 1]);
+                }
               }
               // the one-hot term, in the rare chunks that hold some row's label
               if (__any_sync(0xffffffffu, static_cast<unsigned>(rel) < 32u)) {
