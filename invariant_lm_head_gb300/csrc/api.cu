@@ -323,9 +323,11 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
                 float* out_ent, float* out_lse, const FwdWs& w, cudaStream_t st,
                 float* out_sum_p2 = nullptr, const std::vector<FwdSlice>* slices = nullptr) {
   CUtensorMap ta, tb;
-  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
+  const int a_rows = lmh::short_a_rows(T);
+  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, a_rows ? a_rows : lmh::kBM));
   LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));
   lmh::GemmParams p{};
+  p.a_rows = a_rows;
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
   p.K = static_cast<int>(H);
@@ -764,9 +766,11 @@ int lmhead_logprob_fwd_partials(const uint16_t* hidden, const uint16_t* weight,
   LMH_TRY(launch_status(cudaMemsetAsync(label_logit, 0, static_cast<size_t>(T) * 4, st),
                         "zero label_logit"));
   CUtensorMap ta, tb;
-  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM));
+  const int a_rows = lmh::short_a_rows(T);
+  LMH_TRY(make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, a_rows ? a_rows : lmh::kBM));
   LMH_TRY(make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));
   lmh::GemmParams p{};
+  p.a_rows = a_rows;
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
   p.K = static_cast<int>(H);

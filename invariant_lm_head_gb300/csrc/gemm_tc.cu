@@ -189,6 +189,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int unit_stride = kPair ? static_cast<int>(cluster_nid_x()) : static_cast<int>(gridDim.x);
   auto cta_m_tile = [&](int m_unit) { return kPair ? 2 * m_unit + static_cast<int>(rank) : m_unit; };
 
+  // A short batch's A boxes fill only the first a_rows rows of each A tile:
+  // the rest is zeroed once, before any MMA reads it.
+  const int a_rows = (!kPair && p.a_rows > 0) ? p.a_rows : kBM;
+  if (a_rows < kBM) {
+    const uint32_t n16 = static_cast<uint32_t>((kBM - a_rows) * 128 / 16);
+    for (uint32_t i = threadIdx.x; i < kS * n16; i += blockDim.x) {
+      const uint32_t st = i / n16, j = i - st * n16;
+      st_shared_v4(smem_base + st * R::kStageBytes + static_cast<uint32_t>(a_rows) * 128u + 16u * j,
+                   0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(full_bar(s), 1);  // in a pair, only CTA 0's is used: one arrive, both CTAs' bytes
@@ -259,7 +271,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             // One arrive per stage, by CTA 0, expecting both CTAs' bytes; both
             // CTAs' boxes complete on CTA 0's barrier, issued in the pair form
             // (measured: CTA 0 issuing the plain form made the pair 10 % slower).
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (kPair ? 2 : 1) * R::kStageBytes);
+            if (rank == 0)
+              mbar_arrive_expect_tx(full_bar(stage), (kPair ? 2 : 1) * R::kStageBytes -
+                                                         (kBM - a_rows) * 128);
             const uint32_t fbar = kPair ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
             auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
               if constexpr (kPair)
@@ -681,6 +695,9 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
                         int tiles_per_unit, int num_sms, cudaStream_t stream,
                         const CUtensorMap* c) {
   if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
+  if (p.a_rows != 0 &&
+      (p.a_rows < 8 || p.a_rows > kBM || p.a_rows % 8 != 0 || p.a_mn || p.M > p.a_rows))
+    return cudaErrorInvalidValue;  // a short A box covers every row of a K-major A
   CUtensorMap none{};
   const CUtensorMap& c_map = c ? *c : none;
   // CTA pairs take 256-row m units and serve grad_weight. Same-session A/B

@@ -25,6 +25,12 @@ constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kFwdTilesPerChunk = 4;
 constexpr int kFwdChunkCols = kFwdTilesPerChunk * kBN;
 
+// The A box rows for a forward of M rows: M rounded up to 8 when M < kBM,
+// else 0 (the full kBM-row box).
+inline int short_a_rows(int64_t M) {
+  return M < kBM ? static_cast<int>(M < 8 ? 8 : (M + 7) / 8 * 8) : 0;
+}
+
 // Backward: rows are processed in fixed chunks of kBwdRowChunk.
 constexpr int64_t kBwdRowChunk = 16384;
 
@@ -42,6 +48,11 @@ struct GemmParams {
   // 0 = to the end); launch_gemm turns them into n_vunits, and a unit's vocab
   // unit index stays global, so partials land in their usual planes.
   int vunit_begin, vunit_end;
+  // Rows of each A box (K-major A, single-CTA launches with M <= a_rows): 0
+  // means kBM. A short batch then loads M rounded up to 8 rows instead of a
+  // 128-row box that is almost all out-of-bounds fill; the rest of the A tile
+  // is zero in shared memory, and the valid rows' products are unchanged.
+  int a_rows;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)

@@ -118,9 +118,13 @@ extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t
   float* pzl = reinterpret_cast<float*>(b + 3 * plane);
 
   CUtensorMap ta, tb;
-  if ((rc = lmh::api_make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, lmh::kBM)) != LMH_OK) return rc;
+  const int a_rows = lmh::short_a_rows(T);
+  if ((rc = lmh::api_make_tmap(&ta, hidden, H, T, H * 2, lmh::kBK, a_rows ? a_rows : lmh::kBM)) !=
+      LMH_OK)
+    return rc;
   if ((rc = lmh::api_make_tmap(&tb, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows)) != LMH_OK) return rc;
   lmh::GemmParams p{};
+  p.a_rows = a_rows;
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(V);
   p.K = static_cast<int>(H);
