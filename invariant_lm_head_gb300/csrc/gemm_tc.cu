@@ -641,13 +641,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   gemm_body<E, true>(tmA, tmB, tmC, p);
 }
 
-// Clusters of two that fit on the device at once (one CTA per SM), per device.
+// Clusters of two that fit on the device at once (one CTA per SM), per
+// device; 0 when none does (the caller then runs single CTAs).
 template <int E>
 int pair_slots(int num_sms) {
   static int cached[16] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < 16 && cached[dev] > 0) return cached[dev];
+  if (cudaFuncSetAttribute(gemm_tc_pair_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Ring<true>::kSmemBytes) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
   cfg.blockDim = dim3(kGemmThreads);
@@ -672,7 +678,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
                              Ring<true>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int slots = pair_slots<E>(num_sms);
-    if (slots <= 0) return cudaErrorInvalidConfiguration;
+    if (slots <= 0) return cudaErrorInvalidConfiguration;  // launch_gemm checked it first
     const int clusters = p.n_units < slots ? p.n_units : slots;  // persistent
     gemm_tc_pair_kernel<E><<<2 * clusters, kGemmThreads, Ring<true>::kSmemBytes, stream>>>(a, b, c, p);
   } else {
@@ -710,7 +716,20 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int mode = gemm_pair_mode();
   const bool prefer = mode == 1 || (mode < 0 && e == Epi::StoreF32T);
-  const bool pair = prefer && m_tiles >= 2;
+  bool pair = prefer && m_tiles >= 2;
+  if (pair) {
+    // no room for a cluster of two (a partitioned GPU, say): single CTAs,
+    // which give the same bits
+    int slots = 0;
+    switch (e) {
+      case Epi::FwdStats: slots = pair_slots<(int)Epi::FwdStats>(num_sms); break;
+      case Epi::DLogits: slots = pair_slots<(int)Epi::DLogits>(num_sms); break;
+      case Epi::StoreBf16: slots = pair_slots<(int)Epi::StoreBf16>(num_sms); break;
+      case Epi::StoreF32: slots = pair_slots<(int)Epi::StoreF32>(num_sms); break;
+      case Epi::StoreF32T: slots = pair_slots<(int)Epi::StoreF32T>(num_sms); break;
+    }
+    pair = slots > 0;
+  }
   const int m_rows = pair ? 2 * kBM : kBM;
   p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
   p.n_n_tiles = (p.N + kBN - 1) / kBN;
