@@ -694,6 +694,46 @@ def run_gpu(args):
             "tflops_kernels": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12,
             "frac_of_burst_peak": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12 / peaks["bf16_tflops"]}
         del h2, w2
+        # tiny fused forward T=64 H=256 V=4096: a latency figure, no roofline
+        Tt, Ht, Vt = 64, 256, 4096
+        ht_, wt_, lt_, _ = make_inputs(Tt, Ht, Vt, 1, dev)
+        wst = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, Tt, Ht, Vt), dtype=torch.uint8,
+                          device=dev)
+        lpt, entt = torch.empty(Tt, device=dev), torch.empty(Tt, device=dev)
+        fwdt = lambda: lmh.lmhead_logprob_fwd(ht_, wt_, lt_, 1.0, out_logprob=lpt,  # noqa: E731
+                                              out_entropy=entt, workspace=wst)
+        extras["tiny_fwd"] = {"workload": "fused forward T=64 H=256 V=4096",
+                              "ms_per_call": timed(fwdt, 50, 5),
+                              "ms_kernels": kernel_ms(lmh, fwdt, 50, 5, fwd_kernels)}
+        del ht_, wt_
+        # packed variable-length batch: 32 sequences of seeded lengths in
+        # [128, 4096], concatenated; H=5120 V=152064; one fwd+bwd step
+        import workloads as W
+
+        Tp, Hp, Vp = int(sum(W.packed_lengths())), 5120, 152064
+        hp, wp, lbp, gp = make_inputs(Tp, Hp, Vp, 5, dev)
+        lpp, entp, lsep = (torch.empty(Tp, device=dev) for _ in range(3))
+        ghp = torch.empty(Tp, Hp, dtype=torch.bfloat16, device=dev)
+        gwp = torch.empty(Vp, Hp, device=dev)
+        wsfp = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, Tp, Hp, Vp), dtype=torch.uint8,
+                           device=dev)
+        wsbp = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_BWD, Tp, Hp, Vp), dtype=torch.uint8,
+                           device=dev)
+
+        def packed_step():
+            lmh.lmhead_logprob_fwd(hp, wp, lbp, 1.0, out_logprob=lpp, out_entropy=entp,
+                                   out_lse=lsep, workspace=wsfp)
+            lmh.lmhead_logprob_bwd(hp, wp, lbp, gp, 1.0, lse=lsep, grad_hidden=ghp,
+                                   grad_weight=gwp, workspace=wsbp)
+
+        p_ms = kernel_ms(lmh, packed_step, 3, 2, step_kernels)
+        p_tf = 8.0 * Tp * Hp * Vp / (p_ms * 1e-3) / 1e12
+        extras["packed_varlen_fwd_bwd"] = {
+            "workload": f"32 sequences, lengths in [128, 4096], T={Tp} H={Hp} V={Vp}",
+            "ms_kernels_per_step": p_ms, "tokens_per_s": Tp / (p_ms * 1e-3),
+            "tflops_as_executed": p_tf, "frac_of_sustained": p_tf / peak}
+        del hp, wp, ghp, gwp, wsfp, wsbp
+        torch.cuda.empty_cache()
         # logits path: bf16 logits [8192, 152064] (2.49 GB > L2)
         T3, V3 = 8192, 152064
         g3 = torch.Generator(device=dev)

@@ -46,8 +46,8 @@
  *  - The environment variable LMH_GEMM_CTA_PAIRS, read once per process,
  *    picks the tensor-core engine: "0" single CTAs for every contraction,
  *    "1" CTA pairs (two SMs per MMA) wherever a launch has more than 128
- *    rows, unset the default (pairs for grad_weight only). Every output is
- *    bit-identical whichever engine runs.
+ *    rows, unset the default (pairs for grad_weight and grad_hidden only).
+ *    Every output is bit-identical whichever engine runs.
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H

@@ -20,8 +20,12 @@
 // CTA pairs (grad_weight): a cluster of two CTAs owns a 256x256 tile. Each
 // CTA stages its own 128 A rows and one 128-row half of B (6 stages of 32 KB);
 // CTA 0 issues tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives
-// its 128 accumulator rows, so the epilogue is the same. Both engines walk K
-// in the same MMA order and give the same bits.
+// its 128 accumulator rows, so the epilogue is the same. Wide pairs
+// (grad_hidden) own 256x512 tiles: two N=256 pair MMAs per K step into one
+// 512-column accumulator per CTA, which halves how often the B operand is
+// re-read; the epilogue no longer overlaps the next tile, which a long K
+// (= V) hides. Every engine walks K in the same MMA order and gives the same
+// bits.
 //
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
@@ -71,13 +75,23 @@ constexpr int kBarrierBytes = 256;
 // (32 fp32 or, using half of it, 32 bf16 columns).
 constexpr int kStagingBytes = kBM * 128;
 
+// Engine modes: one CTA per 128 x 256 tile; a CTA pair per 256 x 256 tile;
+// a CTA pair per 256 x 512 tile ("wide": two N=256 pair MMAs per K step into
+// one 512-column accumulator per CTA, not double-buffered, for contractions
+// whose K is long enough to hide nothing behind the epilogue).
+constexpr int kSingle = 0, kPairMode = 1, kWideMode = 2;
+
 // The operand ring of one CTA. Alone, a CTA stages the whole 256-row B tile
 // (48 KB a stage, 4 stages); in a CTA pair it stages half of it (32 KB a
-// stage, 6 stages), since the peer holds the other half.
-template <bool kPair>
+// stage, 6 stages), since the peer holds the other half; in a wide pair it
+// stages half of each of the two 256-column B blocks (48 KB, 4 stages).
+template <int kMode>
 struct Ring {
-  static constexpr int kStages = kPair ? 6 : 4;
-  static constexpr int kBBytes = kPair ? kBHalfBytes : 2 * kBHalfBytes;
+  static constexpr int kStages = kMode == kPairMode ? 6 : 4;
+  static constexpr int kBBytes = kMode == kPairMode ? kBHalfBytes : 2 * kBHalfBytes;
+  static constexpr int kNBlocks = kMode == kWideMode ? 2 : 1;  // N=256 MMAs per K step
+  static constexpr int kTileN = kNBlocks * kBN;                // accumulator columns
+  static constexpr int kAccs = kMode == kWideMode ? 1 : 2;     // accumulators in TMEM
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
@@ -156,10 +170,11 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float 
 // CTA 0 issues the MMAs; both CTAs' copies of a stage complete on CTA 0's
 // full barrier, and CTA 0's commits free the stage and hand over the
 // accumulators in both CTAs.
-template <int E, bool kPair>
+template <int E, int kMode>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmC, const GemmParams& p) {
-  using R = Ring<kPair>;
+  constexpr bool kPair = kMode != kSingle;
+  using R = Ring<kMode>;
   constexpr int kS = R::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -258,8 +273,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         const bool k_down = (E == (int)Epi::StoreF32T) && (wave & 1);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
-          // first B row this CTA stages: the whole tile alone, its half in a pair
-          const int b_row0 = n_tile * kBN + (kPair ? static_cast<int>(rank) * kBBoxRows : 0);
+          // first B row this CTA stages in each 256-column block: the whole
+          // block alone, its half in a pair
+          const int b_row0 = n_tile * R::kTileN + (kPair ? static_cast<int>(rank) * kBBoxRows : 0);
           for (int kstep = 0; kstep < kb_total; ++kstep) {
             const int kb = k_down ? kb_total - 1 - kstep : kstep;
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
@@ -291,14 +307,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               }
             };
             auto load_b = [&]() {
-              if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
+              constexpr int kBlockBytes = R::kBBytes / R::kNBlocks;
 #pragma unroll
-                for (int i = 0; i < R::kBBytes / kMnBoxBytes; ++i)
-                  load(sB + i * kMnBoxBytes, &tmB, b_row0 + 64 * i, kb * kBK);
-              } else {  // [N][K]: 128-row boxes
+              for (int nb = 0; nb < R::kNBlocks; ++nb) {
+                const uint32_t dst = sB + nb * kBlockBytes;
+                const int row = b_row0 + nb * kBN;
+                if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
 #pragma unroll
-                for (int i = 0; i < R::kBBytes / kBHalfBytes; ++i)
-                  load(sB + i * kBHalfBytes, &tmB, kb * kBK, b_row0 + kBBoxRows * i);
+                  for (int i = 0; i < kBlockBytes / kMnBoxBytes; ++i)
+                    load(dst + i * kMnBoxBytes, &tmB, row + 64 * i, kb * kBK);
+                } else {  // [N][K]: 128-row boxes
+#pragma unroll
+                  for (int i = 0; i < kBlockBytes / kBHalfBytes; ++i)
+                    load(dst + i * kBHalfBytes, &tmB, kb * kBK, row + kBBoxRows * i);
+                }
               }
             };
             // The forward and dlogits stream W as B: B first, so the DRAM
@@ -353,8 +375,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         int m_unit, n_first, n_count, vunit;
         unit_coords(p, u, m_unit, n_first, n_count, vunit);
         for (int j = 0; ok && j < n_count; ++j, ++it) {
-          const uint32_t acc = it & 1u;
-          const uint32_t aph = (it >> 1) & 1u;
+          const uint32_t acc = it % R::kAccs;
+          const uint32_t aph = (it / R::kAccs) & 1u;
           if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
@@ -376,13 +398,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             // descriptor's 16-byte address units that is +2 or +128.
             const uint64_t astep = p.a_mn ? 128ull : 2ull;
             const uint64_t bstep = p.b_mn ? 128ull : 2ull;
+            // a wide pair's second N block: its B half is the next kBlockBytes
+            // of the stage (>> 4 in descriptor units), its columns the next 256
+            constexpr uint64_t kBlockStep = (R::kBBytes / R::kNBlocks) >> 4;
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               const uint32_t accumulate = (kb > 0 || k > 0) ? 1u : 0u;
-              if constexpr (kPair)
-                tc_mma_bf16_pair(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, accumulate);
-              else
-                tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + bstep * k, idesc, accumulate);
+#pragma unroll
+              for (int nb = 0; nb < R::kNBlocks; ++nb) {
+                const uint64_t bd = bdesc + kBlockStep * nb + bstep * k;
+                if constexpr (kPair)
+                  tc_mma_bf16_pair(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
+                else
+                  tc_mma_bf16(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
+              }
             }
             // the stage is free in both CTAs once these MMAs have read it
             if constexpr (kPair)
@@ -463,8 +492,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 
       for (int j = 0; j < n_count; ++j, ++it) {
         const int n_tile = n_first + j;
-        const uint32_t acc = it & 1u;
-        const uint32_t aph = (it >> 1) & 1u;
+        const uint32_t acc = it % R::kAccs;
+        const uint32_t aph = (it / R::kAccs) & 1u;
         if (etid == 0) epi_go[it & 1u] = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
         named_barrier(kEpiBarrier, 128);
         if (!epi_go[it & 1u]) {
@@ -474,8 +503,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          const int col0 = n_tile * kBN + c * 32;
+        for (int c = 0; c < R::kTileN / 32; ++c) {
+          const int col0 = n_tile * R::kTileN + c * 32;
           if (col0 >= p.N) break;  // uniform over the CTA
           const int nvalid = min(32, p.N - col0);
           float v[32];
@@ -577,8 +606,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           p.part_s[o] = st.s;
           p.part_u[o] = st.u;
           if (p.part_q) p.part_q[o] = st.q;
-          const int c0 = n_first * kBN;
-          const int c1 = min(p.N, (n_first + n_count) * kBN);
+          const int c0 = n_first * R::kTileN;
+          const int c1 = min(p.N, (n_first + n_count) * R::kTileN);
           if (lab >= c0 && lab < c1) p.part_zl[row] = zl;
         }
       }
@@ -630,36 +659,38 @@ template <int E>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  gemm_body<E, false>(tmA, tmB, tmC, p);
+  gemm_body<E, kSingle>(tmA, tmB, tmC, p);
 }
 
-template <int E>
+// kMode: kPairMode or kWideMode
+template <int E, int kMode>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  gemm_body<E, true>(tmA, tmB, tmC, p);
+  gemm_body<E, kMode>(tmA, tmB, tmC, p);
 }
 
 // Clusters of two that fit on the device at once (one CTA per SM), per
 // device; 0 when none does (the caller then runs single CTAs).
-template <int E>
+template <int E, int kMode>
 int pair_slots(int num_sms) {
   static int cached[16] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev >= 0 && dev < 16 && cached[dev] > 0) return cached[dev];
-  if (cudaFuncSetAttribute(gemm_tc_pair_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Ring<true>::kSmemBytes) != cudaSuccess) {
+  if (cudaFuncSetAttribute(gemm_tc_pair_kernel<E, kMode>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Ring<kMode>::kSmemBytes) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
   cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = Ring<true>::kSmemBytes;
+  cfg.dynamicSmemBytes = Ring<kMode>::kSmemBytes;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<E>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<E, kMode>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -668,71 +699,89 @@ int pair_slots(int num_sms) {
   return n;
 }
 
-template <int E>
+template <int E, int kMode>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                       const GemmParams& p, bool pair, int num_sms, cudaStream_t stream) {
+                       const GemmParams& p, int num_sms, cudaStream_t stream) {
   cudaError_t e;
-  if (pair) {
+  if constexpr (kMode != kSingle) {
     // Set on every launch: the attribute belongs to the current device's context.
-    e = cudaFuncSetAttribute(gemm_tc_pair_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Ring<true>::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_tc_pair_kernel<E, kMode>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<kMode>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int slots = pair_slots<E>(num_sms);
+    const int slots = pair_slots<E, kMode>(num_sms);
     if (slots <= 0) return cudaErrorInvalidConfiguration;  // launch_gemm checked it first
     const int clusters = p.n_units < slots ? p.n_units : slots;  // persistent
-    gemm_tc_pair_kernel<E><<<2 * clusters, kGemmThreads, Ring<true>::kSmemBytes, stream>>>(a, b, c, p);
+    gemm_tc_pair_kernel<E, kMode>
+        <<<2 * clusters, kGemmThreads, Ring<kMode>::kSmemBytes, stream>>>(a, b, c, p);
   } else {
     e = cudaFuncSetAttribute(gemm_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Ring<false>::kSmemBytes);
+                             Ring<kSingle>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.n_units < num_sms ? p.n_units : num_sms;  // persistent: <= one CTA per SM
-    gemm_tc_kernel<E><<<grid, kGemmThreads, Ring<false>::kSmemBytes, stream>>>(a, b, c, p);
+    gemm_tc_kernel<E><<<grid, kGemmThreads, Ring<kSingle>::kSmemBytes, stream>>>(a, b, c, p);
   }
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }
 
+// Engines each contraction is built for: every one on single CTAs and CTA
+// pairs; the store epilogues also on wide pairs.
+template <int E>
+constexpr bool kHasWide = E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32;
+
+template <int E>
+int slots_for(int mode, int num_sms) {
+  if (mode == kPairMode) return pair_slots<E, kPairMode>(num_sms);
+  if constexpr (kHasWide<E>)
+    if (mode == kWideMode) return pair_slots<E, kWideMode>(num_sms);
+  return 0;
+}
+
+template <int E>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const GemmParams& p, int mode, int num_sms, cudaStream_t stream) {
+  if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, num_sms, stream);
+  if constexpr (kHasWide<E>)
+    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, num_sms, stream);
+  return launch_one<E, kSingle>(a, b, c, p, num_sms, stream);
+}
+
 }  // namespace
 
-size_t gemm_smem_bytes() { return Ring<false>::kSmemBytes; }
+size_t gemm_smem_bytes() { return Ring<kSingle>::kSmemBytes; }
 
-cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
-                        int tiles_per_unit, int num_sms, cudaStream_t stream,
-                        const CUtensorMap* c) {
-  if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
-  if (p.a_rows != 0 &&
-      (p.a_rows < 8 || p.a_rows > kBM || p.a_rows % 8 != 0 || p.a_mn || p.M > p.a_rows))
-    return cudaErrorInvalidValue;  // a short A box covers every row of a K-major A
-  CUtensorMap none{};
-  const CUtensorMap& c_map = c ? *c : none;
-  // CTA pairs take 256-row m units and serve grad_weight. Same-session A/B
-  // of the 16384 x 3584 x 152064 step, which runs at the power cap: pairs
-  // for grad_weight alone -1 % on the step against none; adding grad_hidden
-  // (whose pair raster reads about 1.6x the DRAM bytes) or the K-major-B
-  // contractions gave the gain back. A launch with a single 128-row m tile
-  // stays on single CTAs, which keep every SM busy instead of leaving half of
-  // each pair idle.
+namespace {
+
+template <int E>
+cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                          GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
+  // Engine per contraction (same-session A/Bs of the 16384 x 3584 x 152064
+  // step, which runs at the power cap): CTA pairs for grad_weight (-1 % on
+  // the step against single CTAs); wide pairs for grad_hidden, whose long K
+  // (= V) hides the epilogue and whose W stream is re-read once per wave;
+  // single CTAs for the forward and dlogits (pairs were 1-3 % slower). A
+  // launch with a single 128-row m tile stays on single CTAs, which keep every
+  // SM busy instead of leaving half of each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
-  const int mode = gemm_pair_mode();
-  const bool prefer = mode == 1 || (mode < 0 && e == Epi::StoreF32T);
-  bool pair = prefer && m_tiles >= 2;
-  if (pair) {
-    // no room for a cluster of two (a partitioned GPU, say): single CTAs,
-    // which give the same bits
-    int slots = 0;
-    switch (e) {
-      case Epi::FwdStats: slots = pair_slots<(int)Epi::FwdStats>(num_sms); break;
-      case Epi::DLogits: slots = pair_slots<(int)Epi::DLogits>(num_sms); break;
-      case Epi::StoreBf16: slots = pair_slots<(int)Epi::StoreBf16>(num_sms); break;
-      case Epi::StoreF32: slots = pair_slots<(int)Epi::StoreF32>(num_sms); break;
-      case Epi::StoreF32T: slots = pair_slots<(int)Epi::StoreF32T>(num_sms); break;
-    }
-    pair = slots > 0;
+  const int env = gemm_pair_mode();
+  constexpr bool kStoreWide = E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32;
+  int mode = kSingle;
+  if (m_tiles >= 2) {
+    if (env == 1)
+      mode = kStoreWide ? kWideMode : kPairMode;
+    else if (env < 0)
+      mode = E == (int)Epi::StoreF32T ? kPairMode
+                                       : (E == (int)Epi::StoreBf16 ? kWideMode : kSingle);
   }
-  const int m_rows = pair ? 2 * kBM : kBM;
+  // no room for a cluster of two (a partitioned GPU, say): single CTAs, which
+  // give the same bits
+  if (mode != kSingle && slots_for<E>(mode, num_sms) <= 0) mode = kSingle;
+  const int m_rows = mode != kSingle ? 2 * kBM : kBM;
+  const int tile_n = mode == kWideMode ? 2 * kBN : kBN;
+  if (E == (int)Epi::FwdStats && tile_n != kBN) return cudaErrorInvalidValue;  // chunk grid
   p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
-  p.n_n_tiles = (p.N + kBN - 1) / kBN;
+  p.n_n_tiles = (p.N + tile_n - 1) / tile_n;
   p.tiles_per_unit = tiles_per_unit;
   const int all_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
   const int vu_end = (p.vunit_end > 0 && p.vunit_end < all_vunits) ? p.vunit_end : all_vunits;
@@ -744,25 +793,41 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   p.n_units = static_cast<int>(units);
   // Rows per raster group, per contraction (same-session sweep of 4/8/16/32
-  // 128-row m tiles on the Qwen-like step): the N = V contractions (forward,
-  // dlogits) share W tiles across more m tiles, the K = V grad_hidden
-  // prefers small groups. A pair's m unit is two m tiles.
-  const int group_tiles = (e == Epi::FwdStats || e == Epi::DLogits || e == Epi::StoreF32T)
+  // 128-row m tiles on the Qwen-like step; 1, 2 and 4 again for grad_hidden):
+  // the N = V contractions (forward, dlogits) share W tiles across more m
+  // tiles, the K = V grad_hidden prefers small groups. A pair's m unit is two
+  // m tiles.
+  const int group_tiles = (E == (int)Epi::FwdStats || E == (int)Epi::DLogits ||
+                           E == (int)Epi::StoreF32T)
                               ? 32
-                              : (e == Epi::StoreBf16 ? 4 : 8);
-  p.group_m = pair ? group_tiles / 2 : group_tiles;
+                              : (E == (int)Epi::StoreBf16 ? 4 : 8);
+  p.group_m = mode != kSingle ? group_tiles / 2 : group_tiles;
   if (p.n_units <= 0) return cudaSuccess;
+  return launch_mode<E>(a, b, c, p, mode, num_sms, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmParams p,
+                        int tiles_per_unit, int num_sms, cudaStream_t stream,
+                        const CUtensorMap* c) {
+  if (e != Epi::FwdStats && !c) return cudaErrorInvalidValue;  // output map required
+  if (p.a_rows != 0 &&
+      (p.a_rows < 8 || p.a_rows > kBM || p.a_rows % 8 != 0 || p.a_mn || p.M > p.a_rows))
+    return cudaErrorInvalidValue;  // a short A box covers every row of a K-major A
+  CUtensorMap none{};
+  const CUtensorMap& c_map = c ? *c : none;
   switch (e) {
     case Epi::FwdStats:
-      return launch_one<(int)Epi::FwdStats>(a, b, c_map, p, pair, num_sms, stream);
+      return launch_gemm_e<(int)Epi::FwdStats>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
     case Epi::DLogits:
-      return launch_one<(int)Epi::DLogits>(a, b, c_map, p, pair, num_sms, stream);
+      return launch_gemm_e<(int)Epi::DLogits>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
     case Epi::StoreBf16:
-      return launch_one<(int)Epi::StoreBf16>(a, b, c_map, p, pair, num_sms, stream);
+      return launch_gemm_e<(int)Epi::StoreBf16>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
     case Epi::StoreF32:
-      return launch_one<(int)Epi::StoreF32>(a, b, c_map, p, pair, num_sms, stream);
+      return launch_gemm_e<(int)Epi::StoreF32>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
     case Epi::StoreF32T:
-      return launch_one<(int)Epi::StoreF32T>(a, b, c_map, p, pair, num_sms, stream);
+      return launch_gemm_e<(int)Epi::StoreF32T>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }
