@@ -20,8 +20,8 @@
  * A row's logprob, entropy, lse and grad_hidden row are bit-identical whatever
  * batch, chunk, offset or packing the row arrives in. grad_weight sums over
  * rows: it is deterministic run to run for identical inputs on the same GPU
- * model (its summation order also depends on the SM count), not invariant to
- * the order of rows.
+ * model (its summation order also depends on the SM count and the engine
+ * chosen below), not invariant to the order of rows.
  *
  * Conventions shared by all entry points
  *  - bf16 tensors are passed as uint16_t bit patterns, row-major, device memory.
@@ -47,7 +47,9 @@
  *    picks the tensor-core engine: "0" single CTAs for every contraction,
  *    "1" CTA pairs (two SMs per MMA) wherever a launch has more than 128
  *    rows, unset the default (pairs for grad_weight and grad_hidden only).
- *    Every output is bit-identical whichever engine runs.
+ *    log-prob, entropy, lse, sum_p2 and grad_hidden are bit-identical
+ *    whichever engine runs. grad_weight is deterministic for a given engine
+ *    and SM count; its summation order follows the engine's waves.
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H

@@ -17,15 +17,16 @@
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
 //
-// CTA pairs (grad_weight): a cluster of two CTAs owns a 256x256 tile. Each
-// CTA stages its own 128 A rows and one 128-row half of B (6 stages of 32 KB);
-// CTA 0 issues tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives
-// its 128 accumulator rows, so the epilogue is the same. Wide pairs
-// (grad_hidden) own 256x512 tiles: two N=256 pair MMAs per K step into one
-// 512-column accumulator per CTA, which halves how often the B operand is
-// re-read; the epilogue no longer overlaps the next tile, which a long K
-// (= V) hides. Every engine walks K in the same MMA order and gives the same
-// bits.
+// CTA pairs: a cluster of two CTAs owns a 256x256 tile. Each CTA stages its
+// own 128 A rows and one 128-row half of B (6 stages of 32 KB); CTA 0 issues
+// tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives its 128
+// accumulator rows, so the epilogue is the same. Wide pairs (grad_hidden,
+// grad_weight) own 256x512 tiles: two N=256 pair MMAs per K step into one
+// 512-column accumulator per CTA, which halves how often an operand is
+// re-read; the epilogue no longer overlaps the next tile, which their K
+// (V or 16384 rows) mostly hides. Every engine walks K in the same MMA order
+// for the forward, dlogits and grad_hidden, so their bits do not depend on
+// the engine.
 //
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
@@ -51,7 +52,7 @@
 // no atomics, and the forward, dlogits and grad_hidden contractions walk K in
 // ascending order for every tile. grad_weight, a sum over rows that no row's
 // output depends on, walks K downwards on a CTA's odd waves for L2 reuse; its
-// bits are fixed by the inputs, the row chunking and the SM count.
+// bits are fixed by the inputs, the row chunking, the SM count and the engine.
 #include <cfloat>
 #include <cstdint>
 #include <cstdlib>
@@ -725,25 +726,23 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   return e;
 }
 
-// Engines each contraction is built for: every one on single CTAs and CTA
-// pairs; the store epilogues also on wide pairs.
+// The paired engine each contraction is built for (besides single CTAs):
+// wide pairs for the store epilogues, whose K is long or whose epilogue is
+// light; pairs for the forward and dlogits, whose K (= H) is too short to
+// hide an epilogue that no longer overlaps the next tile.
 template <int E>
-constexpr bool kHasWide = E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32;
+constexpr int kPairedMode = (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) ? kPairMode
+                                                                                 : kWideMode;
 
 template <int E>
 int slots_for(int mode, int num_sms) {
-  if (mode == kPairMode) return pair_slots<E, kPairMode>(num_sms);
-  if constexpr (kHasWide<E>)
-    if (mode == kWideMode) return pair_slots<E, kWideMode>(num_sms);
-  return 0;
+  return mode == kPairedMode<E> ? pair_slots<E, kPairedMode<E>>(num_sms) : 0;
 }
 
 template <int E>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const GemmParams& p, int mode, int num_sms, cudaStream_t stream) {
-  if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, num_sms, stream);
-  if constexpr (kHasWide<E>)
-    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, num_sms, stream);
+  if (mode == kPairedMode<E>) return launch_one<E, kPairedMode<E>>(a, b, c, p, num_sms, stream);
   return launch_one<E, kSingle>(a, b, c, p, num_sms, stream);
 }
 
@@ -757,22 +756,20 @@ template <int E>
 cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
   // Engine per contraction (same-session A/Bs of the 16384 x 3584 x 152064
-  // step, which runs at the power cap): CTA pairs for grad_weight (-1 % on
-  // the step against single CTAs); wide pairs for grad_hidden, whose long K
-  // (= V) hides the epilogue and whose W stream is re-read once per wave;
-  // single CTAs for the forward and dlogits (pairs were 1-3 % slower). A
-  // launch with a single 128-row m tile stays on single CTAs, which keep every
-  // SM busy instead of leaving half of each pair idle.
+  // step, which runs at the power cap): wide pairs for grad_hidden (kernel
+  // -13 %, step -1.8 %) and grad_weight (kernel -6 %, step -1.4 %, against
+  // 256-wide pairs, which had been -1 % against single CTAs); single CTAs for
+  // the forward and dlogits (pairs were 1-3 % slower). A launch with a single
+  // 128-row m tile stays on single CTAs, which keep every SM busy instead of
+  // leaving half of each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int env = gemm_pair_mode();
-  constexpr bool kStoreWide = E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32;
   int mode = kSingle;
   if (m_tiles >= 2) {
     if (env == 1)
-      mode = kStoreWide ? kWideMode : kPairMode;
-    else if (env < 0)
-      mode = E == (int)Epi::StoreF32T ? kPairMode
-                                       : (E == (int)Epi::StoreBf16 ? kWideMode : kSingle);
+      mode = kPairedMode<E>;
+    else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T))
+      mode = kWideMode;
   }
   // no room for a cluster of two (a partitioned GPU, say): single CTAs, which
   // give the same bits

@@ -1,9 +1,15 @@
-"""The tensor-core engine runs a contraction either on single CTAs (128-row
-tiles) or on CTA pairs that share each MMA (256-row tiles). Which one runs
-must never change a bit: each output element's dot product walks K in the
-same order either way. Child processes force each engine (the choice is read
+"""The tensor-core engine runs a contraction on single CTAs (128 x 256
+tiles), on CTA pairs that share each MMA (256 x 256), or on wide pairs
+(256 x 512). Which one runs must not change a bit of the log-probs, entropy,
+lse or grad_hidden: each output element's dot product walks K in the same
+order on every engine. Child processes force each engine (the choice is read
 once per process) on ragged shapes, including pairs whose second half lies
-wholly past the last row, and every output is compared bit for bit."""
+wholly past the last row, and every output is compared bit for bit.
+
+grad_weight walks K downwards on a CTA's odd waves, so its summation order
+follows the engine's wave structure. The shapes here fit each grad_weight
+launch in one wave, where that order is the same, so grad_weight and the
+bare engine GEMM are compared bit for bit as well."""
 
 import os
 import subprocess
