@@ -220,10 +220,12 @@ def test_entropy_backward_without_entropy_grad_equals_plain_backward(lmh):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-def test_backward_deterministic_run_to_run(lmh):
+# (2048, 1024, 40000): grad_weight runs on wide CTA pairs over 316 units, more
+# than four waves, so the odd waves' downward K walk is exercised too.
+@pytest.mark.parametrize("T,H,V", [(400, 128, 3000), (2048, 1024, 40000)])
+def test_backward_deterministic_run_to_run(lmh, T, H, V):
     import torch
 
-    T, H, V = 400, 128, 3000
     hidden, weight, labels, grad = fused_case(51, T, H, V)
     h, w, lab, g = to_dev_bf16(hidden), to_dev_bf16(weight), to_dev(labels), to_dev(grad)
     a = lmh.lmhead_logprob_bwd(h, w, lab, g, S07)
