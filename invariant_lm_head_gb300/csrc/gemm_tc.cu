@@ -50,7 +50,8 @@
 // Batch invariance: the work split depends only on N (vocab) and never on M
 // (rows), each row is reduced by one thread in a fixed column order, there are
 // no atomics, and the forward, dlogits and grad_hidden contractions walk K in
-// ascending order for every tile. grad_weight, a sum over rows that no row's
+// ascending order for every tile. Which engine runs depends on M (a pair
+// needs two m tiles), and changes none of their bits. grad_weight, a sum over rows that no row's
 // output depends on, walks K downwards on a CTA's odd waves for L2 reuse; its
 // bits are fixed by the inputs, the row chunking, the SM count and the engine.
 #include <cfloat>
@@ -164,13 +165,13 @@ __device__ __forceinline__ void stage_row_bf16(uint32_t buf, int r, const float 
                  pack_bf16x2(v[8 * j + 4], v[8 * j + 5]), pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
 }
 
-// One CTA's share of the engine. kPair: the CTA is one of a cluster pair that
-// shares every MMA (tcgen05 cta_group::2): the pair owns a 256 x 256 tile,
-// each CTA stages the A rows of its own 128-row half and one 128-row half of
-// the B tile, and each CTA's TMEM receives its 128 rows of the accumulator.
-// CTA 0 issues the MMAs; both CTAs' copies of a stage complete on CTA 0's
-// full barrier, and CTA 0's commits free the stage and hand over the
-// accumulators in both CTAs.
+// One CTA's share of the engine. In the pair modes the CTA is one of a
+// cluster pair that shares every MMA (tcgen05 cta_group::2): the pair owns a
+// 256 x 256 tile (256 x 512 when wide), each CTA stages the A rows of its own
+// 128-row half and its 128-row half of each 256-column B block, and each
+// CTA's TMEM receives its 128 rows of the accumulator. CTA 0 issues the MMAs;
+// both CTAs' copies of a stage complete on CTA 0's full barrier, and CTA 0's
+// commits free the stage and hand over the accumulators in both CTAs.
 template <int E, int kMode>
 __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                           const CUtensorMap& tmC, const GemmParams& p) {
