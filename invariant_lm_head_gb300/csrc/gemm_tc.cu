@@ -206,17 +206,20 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int unit_stride = kPair ? static_cast<int>(cluster_nid_x()) : static_cast<int>(gridDim.x);
   auto cta_m_tile = [&](int m_unit) { return kPair ? 2 * m_unit + static_cast<int>(rank) : m_unit; };
 
-  // A short batch's A boxes fill only the first a_rows rows of each A tile:
-  // the rest is zeroed once, before any MMA reads it.
+  // A short batch's A boxes fill only the first a_rows rows of each A tile
+  // (single CTAs only): the rest is zeroed once, before any MMA reads it.
   const int a_rows = (!kPair && p.a_rows > 0) ? p.a_rows : kBM;
-  if (a_rows < kBM) {
-    const uint32_t n16 = static_cast<uint32_t>((kBM - a_rows) * 128 / 16);
-    for (uint32_t i = threadIdx.x; i < kS * n16; i += blockDim.x) {
-      const uint32_t st = i / n16, j = i - st * n16;
-      st_shared_v4(smem_base + st * R::kStageBytes + static_cast<uint32_t>(a_rows) * 128u + 16u * j,
-                   0u, 0u, 0u, 0u);
+  if constexpr (!kPair) {
+    if (a_rows < kBM) {
+      const uint32_t n16 = static_cast<uint32_t>((kBM - a_rows) * 128 / 16);
+      for (uint32_t i = threadIdx.x; i < kS * n16; i += blockDim.x) {
+        const uint32_t st = i / n16, j = i - st * n16;
+        st_shared_v4(
+            smem_base + st * R::kStageBytes + static_cast<uint32_t>(a_rows) * 128u + 16u * j, 0u,
+            0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kS; ++s) {

@@ -27,9 +27,6 @@ namespace {
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
 // Fixed-order CTA reduction of per-thread states: shuffle-down tree inside
 // each warp, then warp 0's lane 0 folds the warp results in warp order.
 template <bool kQ>
