@@ -450,14 +450,18 @@ int staging_events(Staging& sg, size_t n) {
   return LMH_OK;
 }
 
-// Vocab slices of the staged forward, in 1024-column units: the first small,
-// so the tensor cores start soon after the first copies land, then doubling up
-// to a quarter of the vocabulary; a tail shorter than the first slice joins
-// the slice before it. Copies run several times faster than the forward
-// consumes the weight, so only the first slice's copy is exposed.
+// Vocab slices of the host-staged forward, in 1024-column units. The first
+// (1/32 of the vocabulary) is small, so the first GEMM launch starts soon
+// after hidden has landed. Later slices grow by 3/2 up to a quarter of the
+// vocabulary, and a tail shorter than the first slice joins the slice before
+// it. At the 16384 x 3584 x 152064 step the GEMM uses a vocab unit (7.3 MB of
+// W) in about 67 us and the copy link (about 211 GB/s) brings one in about
+// 35 us, so slice i+1 (1.5x slice i) lands before the GEMM is done with slice
+// i. (Against a schedule of n/16 doubling, the end-to-end step measured the
+// same within run-to-run noise.)
 std::vector<FwdSlice> staged_slices(int n_vunits) {
   std::vector<FwdSlice> out;
-  const int first = n_vunits < 16 ? 1 : (n_vunits + 15) / 16;
+  const int first = n_vunits < 32 ? 1 : (n_vunits + 31) / 32;
   const int cap = std::max(first, (n_vunits + 3) / 4);
   int b = 0, size = first;
   while (b < n_vunits) {
@@ -465,7 +469,7 @@ std::vector<FwdSlice> staged_slices(int n_vunits) {
     if (n_vunits - e > 0 && n_vunits - e < first) e = n_vunits;
     out.push_back(FwdSlice{b, e, nullptr});
     b = e;
-    size = std::min(cap, size * 2);
+    size = std::min(cap, std::max(size + 1, size * 3 / 2));
   }
   return out;
 }
