@@ -54,6 +54,7 @@
 // needs two m tiles), and changes none of their bits. grad_weight, a sum over rows that no row's
 // output depends on, walks K downwards on a CTA's odd waves for L2 reuse; its
 // bits are fixed by the inputs, the row chunking, the SM count and the engine.
+#include <atomic>
 #include <cfloat>
 #include <cstdint>
 #include <cstdlib>
@@ -677,13 +678,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 }
 
 // Clusters of two that fit on the device at once (one CTA per SM), per
-// device; 0 when none does (the caller then runs single CTAs).
+// device; 0 when none does (the caller then runs single CTAs). The cache is
+// shared by host threads: any of them may fill a slot, with the same value.
 template <int E, int kMode>
 int pair_slots(int num_sms) {
-  static int cached[16] = {0};
+  static std::atomic<int> cached[16];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 16 && cached[dev] > 0) return cached[dev];
+  if (dev >= 0 && dev < 16) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   if (cudaFuncSetAttribute(gemm_tc_pair_kernel<E, kMode>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Ring<kMode>::kSmemBytes) != cudaSuccess) {
@@ -700,7 +705,7 @@ int pair_slots(int num_sms) {
     return 0;
   }
   n = n < num_sms / 2 ? n : num_sms / 2;
-  if (dev >= 0 && dev < 16) cached[dev] = n;
+  if (dev >= 0 && dev < 16) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
