@@ -46,7 +46,8 @@
  *  - The environment variable LMH_GEMM_CTA_PAIRS, read once per process,
  *    picks the tensor-core engine: "0" single CTAs for every contraction,
  *    "1" CTA pairs (two SMs per MMA) wherever a launch has more than 128
- *    rows, unset the default (pairs for grad_weight and grad_hidden only).
+ *    rows, unset the default (pairs for grad_weight and grad_hidden, and for
+ *    a forward of 2 to 32 row tiles of 128 in even number).
  *    log-prob, entropy, lse, sum_p2 and grad_hidden are bit-identical
  *    whichever engine runs. grad_weight is deterministic for a given engine
  *    and SM count; its summation order follows the engine's waves.

@@ -768,9 +768,13 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // step, which runs at the power cap): wide pairs for grad_hidden (kernel
   // -13 %, step -1.8 %) and grad_weight (kernel -6 %, step -1.4 %, against
   // 256-wide pairs, which had been -1 % against single CTAs); single CTAs for
-  // the forward and dlogits (pairs were 1-3 % slower). A launch with a single
-  // 128-row m tile stays on single CTAs, which keep every SM busy instead of
-  // leaving half of each pair idle.
+  // dlogits (pairs 1 % slower). The forward runs on pairs for an even number
+  // of m tiles up to 32 (T up to 4096; alone at H = 3584, V = 152064: -8.5 %
+  // at 129 rows, -2 % at 2048, even at 4096; -2 % on 4096 x 4096 x 32000),
+  // where no pair half lies past the last row (3 m tiles on pairs: +14 %,
+  // 9: +4.5 %), and on single CTAs above (16384 rows on pairs: +3 %). A
+  // launch with a single 128-row m tile stays on single CTAs, which keep every
+  // SM busy instead of leaving half of each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int env = gemm_pair_mode();
   int mode = kSingle;
@@ -779,6 +783,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
       mode = kPairedMode<E>;
     else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T))
       mode = kWideMode;
+    else if (env < 0 && E == (int)Epi::FwdStats && m_tiles <= 32 && m_tiles % 2 == 0)
+      mode = kPairMode;
   }
   // no room for a cluster of two (a partitioned GPU, say): single CTAs, which
   // give the same bits
