@@ -767,14 +767,14 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // Engine per contraction (same-session A/Bs of the 16384 x 3584 x 152064
   // step, which runs at the power cap): wide pairs for grad_hidden (kernel
   // -13 %, step -1.8 %) and grad_weight (kernel -6 %, step -1.4 %, against
-  // 256-wide pairs, which had been -1 % against single CTAs); single CTAs for
-  // dlogits (pairs 1 % slower). The forward runs on pairs for an even number
-  // of m tiles up to 32 (T up to 4096; alone at H = 3584, V = 152064: -8.5 %
-  // at 129 rows, -2 % at 2048, even at 4096; -2 % on 4096 x 4096 x 32000),
-  // where no pair half lies past the last row (3 m tiles on pairs: +14 %,
-  // 9: +4.5 %), and on single CTAs above (16384 rows on pairs: +3 %). A
-  // launch with a single 128-row m tile stays on single CTAs, which keep every
-  // SM busy instead of leaving half of each pair idle.
+  // 256-wide pairs, which had been -1 % against single CTAs). The forward and
+  // dlogits (K = H) run on pairs for an even number of m tiles up to 32 (T up
+  // to 4096; alone at H = 3584, V = 152064, forward: -8.5 % at 129 rows, -2 %
+  // at 2048, even at 4096; dlogits: -11 % at 512 rows, -3.5 % at 4096), where
+  // no pair half lies past the last row (forward on 3 m tiles: +14 %, on 9:
+  // +4.5 %), and on single CTAs above (16384 rows on pairs: forward +3 %,
+  // dlogits +0.6 %). A launch with a single 128-row m tile stays on single
+  // CTAs, which keep every SM busy instead of leaving half of each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int env = gemm_pair_mode();
   int mode = kSingle;
@@ -783,7 +783,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
       mode = kPairedMode<E>;
     else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T))
       mode = kWideMode;
-    else if (env < 0 && E == (int)Epi::FwdStats && m_tiles <= 32 && m_tiles % 2 == 0)
+    else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles <= 32 &&
+             m_tiles % 2 == 0)
       mode = kPairMode;
   }
   // no room for a cluster of two (a partitioned GPU, say): single CTAs, which
