@@ -767,7 +767,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // Engine per contraction (same-session A/Bs of the 16384 x 3584 x 152064
   // step, which runs at the power cap): wide pairs for grad_hidden (kernel
   // -13 %, step -1.8 %) and grad_weight (kernel -6 %, step -1.4 %, against
-  // 256-wide pairs, which had been -1 % against single CTAs). The forward and
+  // 256-wide pairs, which had been -1 % against single CTAs), when their waves
+  // take less time than single CTAs' (below). The forward and
   // dlogits (K = H) run on pairs for an even number of m tiles up to 32 (T up
   // to 4096; alone at H = 3584, V = 152064, forward: -8.5 % at 129 rows, -2 %
   // at 2048, even at 4096; dlogits: -11 % at 512 rows, -3.5 % at 4096), where
@@ -781,8 +782,23 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   if (m_tiles >= 2) {
     if (env == 1)
       mode = kPairedMode<E>;
-    else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T))
-      mode = kWideMode;
+    else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T)) {
+      // A wide unit does twice a single CTA's work per SM in about 1.55x its
+      // time (grad_hidden alone: 1.257 against 0.79-0.82 ms when both fit in
+      // one wave), so wide pairs win only when they need enough fewer waves:
+      // at H = 3584 they lost below 2048 rows (1.26 against 0.8 ms) and at
+      // 3072-4096, and won at 2048 and from 8192 rows up, as this predicts.
+      const long long units_single =
+          static_cast<long long>(m_tiles) * ((p.N + kBN - 1) / kBN);
+      const long long units_wide =
+          static_cast<long long>((m_tiles + 1) / 2) * ((p.N + 2 * kBN - 1) / (2 * kBN));
+      const int slots = slots_for<E>(kWideMode, num_sms);
+      if (slots > 0 && num_sms > 0) {
+        const long long waves_single = (units_single + num_sms - 1) / num_sms;
+        const long long waves_wide = (units_wide + slots - 1) / slots;
+        if (waves_wide * 155 < waves_single * 100) mode = kWideMode;
+      }
+    }
     else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles <= 32 &&
              m_tiles % 2 == 0)
       mode = kPairMode;
