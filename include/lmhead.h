@@ -293,8 +293,9 @@ int lmhead_logprob_merge(const float* part_m, const float* part_s, const float* 
  * allocated. The partials need 12 * ceil(V / 1024) * T + 4 * T bytes (each
  * part rounded up to 256); larger calls return LMH_ERR_WORKSPACE with nothing
  * launched (for V = 152064 that is T up to about 9300 rows).
- * The first call on a device looks up the scratch array's device address
- * (cudaGetSymbolAddress); make it before any stream capture. All calls share
+ * The library's first call on a device (of any entry point) looks up the
+ * scratch array's device address (cudaGetSymbolAddress); make it before any
+ * stream capture. All calls share
  * the one array, which keeps the previous call's contents (nothing in it needs
  * to start at zero). Calls that overlap on the GPU (other streams, or
  * unordered host threads) race on it: serialise them.

@@ -48,6 +48,7 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   unsigned* status = nullptr;
   int* selftest = nullptr;
+  void* noalloc_scratch = nullptr;  // lmhead_logprob_fwd_noalloc's array on this device
 };
 
 std::mutex g_mu;
@@ -77,6 +78,8 @@ int device_info(DeviceInfo** out) {
         (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.selftest),
                                   g_lmh_selftest_result)) != cudaSuccess)
       return fail(LMH_ERR_LAUNCH, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    const int rc = lmh::noalloc_scratch_lookup(&d.noalloc_scratch);
+    if (rc != LMH_OK) return rc;
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -243,20 +246,7 @@ int launch_status(cudaError_t e, const char* what) {
 // Opt-in diagnostics: with timing enabled, every launch is bracketed by two
 // CUDA events recorded on the launching stream; lmhead_timing_read() returns
 // the kind and duration of each launch. Off by default (no events recorded).
-enum Kind : int {
-  K_FWD_GEMM = 0,
-  K_FWD_MERGE,
-  K_DLOGITS_GEMM,
-  K_DHIDDEN_GEMM,
-  K_DWEIGHT_GEMM,
-  K_LOGITS_ROWWISE,
-  K_ENGINE_GEMM,
-  K_SELFTEST,
-  K_LOGITS_ROWWISE_DIV,
-  K_HIDDEN_TRANSPOSE,
-  K_COUNT
-};
-const char* const kKindNames[K_COUNT] = {
+const char* const kKindNames[lmh::K_COUNT] = {
     "fused_fwd_gemm", "fwd_merge",   "dlogits_gemm",  "grad_hidden_gemm",  "grad_weight_gemm",
     "logits_rowwise", "engine_gemm", "selftest_wait", "logits_rowwise_div",
     "hidden_transpose"};
@@ -281,29 +271,9 @@ cudaEvent_t take_event() {
   return e;
 }
 
-struct KernelTimer {
-  int kind;
-  cudaStream_t st;
-  cudaEvent_t b = nullptr;
-  KernelTimer(int k, cudaStream_t s) : kind(k), st(s) {
-    if (!g_timing.load(std::memory_order_relaxed)) return;
-    std::lock_guard<std::mutex> lk(g_tmu);
-    b = take_event();
-    if (b) cudaEventRecord(b, st);
-  }
-  ~KernelTimer() {
-    if (!b) return;
-    std::lock_guard<std::mutex> lk(g_tmu);
-    cudaEvent_t e = take_event();
-    if (!e) return;
-    cudaEventRecord(e, st);
-    g_recs.push_back(TimingRec{kind, b, e});
-  }
-};
-
 #define LMH_LAUNCH(kind, st, expr, what)                  \
   do {                                                    \
-    KernelTimer _kt((kind), (st));                        \
+    lmh::KernelTimer _kt((kind), (st));                   \
     int _rc = launch_status((expr), (what));              \
     if (_rc != LMH_OK) return _rc;                        \
   } while (0)
@@ -342,7 +312,7 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_zl = w.pzl;
   p.part_ld = T;
   if (!slices) {
-    LMH_LAUNCH(K_FWD_GEMM, st,
+    LMH_LAUNCH(lmh::K_FWD_GEMM, st,
                lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
                "fused forward");
   } else {
@@ -354,13 +324,13 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
       }
       p.vunit_begin = sl.begin;
       p.vunit_end = sl.end;
-      LMH_LAUNCH(K_FWD_GEMM, st,
+      LMH_LAUNCH(lmh::K_FWD_GEMM, st,
                  lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms,
                                   st),
                  "fused forward (vocab slice)");
     }
   }
-  LMH_LAUNCH(K_FWD_MERGE, st,
+  LMH_LAUNCH(lmh::K_FWD_MERGE, st,
              lmh::launch_fwd_merge(w.pm, w.ps, w.pu, out_sum_p2 ? w.pq : nullptr, w.pzl, labels, T,
                                    n_fwd_chunks(V), V, out_lp, out_ent, out_lse, out_sum_p2, st),
              "forward merge");
@@ -419,7 +389,7 @@ int logits_entry(const uint16_t* logits, const int32_t* labels, int64_t T, int64
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(divide ? K_LOGITS_ROWWISE_DIV : K_LOGITS_ROWWISE, st,
+  LMH_LAUNCH(divide ? lmh::K_LOGITS_ROWWISE_DIV : lmh::K_LOGITS_ROWWISE, st,
              lmh::launch_logits_logprob(logits, labels, T, V, temp_value, divide,
                                         row_temperature, out_logprob, out_entropy, out_lse,
                                         out_sum_p2, dev->sms, dev->status, st),
@@ -557,7 +527,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     LMH_TRY(make_out_tmap(&o_dl, w.dl, V, rows, w.vpad * 2, false));
     LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
     LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true, true));
-    LMH_LAUNCH(K_DLOGITS_GEMM, st,
+    LMH_LAUNCH(lmh::K_DLOGITS_GEMM, st,
                lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, &o_dl),
                "dlogits");
 
@@ -567,12 +537,12 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     q.N = static_cast<int>(H);
     q.K = static_cast<int>(V);
     q.b_mn = 1;
-    LMH_LAUNCH(K_DHIDDEN_GEMM, st,
+    LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
                lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
                "grad_hidden");
 
     // hidden^T of the chunk, so grad_weight reads its A operand K-major
-    LMH_LAUNCH(K_HIDDEN_TRANSPOSE, st,
+    LMH_LAUNCH(lmh::K_HIDDEN_TRANSPOSE, st,
                lmh::launch_transpose_bf16(h_c, rows, H, H, w.ht, w.tcpad, st), "hidden transpose");
 
     lmh::GemmParams r{};
@@ -584,7 +554,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     r.a_mn = 0;
     r.b_mn = 1;
     r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
-    LMH_LAUNCH(K_DWEIGHT_GEMM, st,
+    LMH_LAUNCH(lmh::K_DWEIGHT_GEMM, st,
                lmh::launch_gemm(lmh::Epi::StoreF32T, t_ht, t_dl_mn, r, 1, dev->sms, st, &o_gw),
                "grad_weight");
   }
@@ -594,6 +564,22 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
 }  // namespace
 
 namespace lmh {
+KernelTimer::KernelTimer(int kind, cudaStream_t st) : kind_(kind), st_(st) {
+  if (!g_timing.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  b_ = take_event();
+  if (b_) cudaEventRecord(b_, st_);
+}
+
+KernelTimer::~KernelTimer() {
+  if (!b_) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  cudaEvent_t e = take_event();
+  if (!e) return;
+  cudaEventRecord(e, st_);
+  g_recs.push_back(TimingRec{kind_, b_, e});
+}
+
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int api_set_error(int code, const char* msg) {
@@ -607,6 +593,14 @@ int api_device(int* sms, unsigned** status) {
   if (rc != LMH_OK) return rc;
   *sms = d->sms;
   *status = d->status;
+  return LMH_OK;
+}
+
+int api_noalloc_scratch(void** scratch) {
+  DeviceInfo* d = nullptr;
+  const int rc = device_info(&d);
+  if (rc != LMH_OK) return rc;
+  *scratch = d->noalloc_scratch;
   return LMH_OK;
 }
 
@@ -656,7 +650,7 @@ int lmhead_timing_read(int* kinds, float* ms, int capacity, int* count) {
 }
 
 const char* lmhead_timing_kind_name(int kind) {
-  return (kind >= 0 && kind < K_COUNT) ? kKindNames[kind] : "";
+  return (kind >= 0 && kind < lmh::K_COUNT) ? kKindNames[kind] : "";
 }
 
 const char* lmhead_last_error_string(void) { return t_err; }
@@ -789,7 +783,7 @@ int lmhead_logprob_fwd_partials(const uint16_t* hidden, const uint16_t* weight,
   p.part_q = nullptr;
   p.part_zl = label_logit;
   p.part_ld = T;
-  LMH_LAUNCH(K_FWD_GEMM, st,
+  LMH_LAUNCH(lmh::K_FWD_GEMM, st,
              lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev->sms, st),
              "forward partials");
   return ok();
@@ -812,7 +806,7 @@ int lmhead_logprob_merge(const float* part_m, const float* part_s, const float* 
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_FWD_MERGE, st,
+  LMH_LAUNCH(lmh::K_FWD_MERGE, st,
              lmh::launch_fwd_merge(part_m, part_s, part_u, nullptr, label_logit, labels, T,
                                    n_fwd_chunks(V), V, out_logprob, out_entropy, out_lse, nullptr,
                                    st),
@@ -913,7 +907,7 @@ int lmhead_selftest_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) 
   DeviceInfo* dev = nullptr;
   LMH_TRY(device_info(&dev));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_SELFTEST, st, lmh::launch_wait_selftest(dev->status, limit_ns, dev->selftest, st),
+  LMH_LAUNCH(lmh::K_SELFTEST, st, lmh::launch_wait_selftest(dev->status, limit_ns, dev->selftest, st),
              "wait self-test");
   int result = -1;
   cudaError_t e;
@@ -933,7 +927,7 @@ int lmhead_selftest_division(float temperature, int* mismatches, struct CUstream
   cudaError_t e;
   if ((e = cudaMemsetAsync(dev->selftest, 0, sizeof(int), st)) != cudaSuccess)
     return fail(LMH_ERR_LAUNCH, "division self-test: %s", cudaGetErrorString(e));
-  LMH_LAUNCH(K_SELFTEST, st, lmh::launch_division_selftest(temperature, dev->selftest, st),
+  LMH_LAUNCH(lmh::K_SELFTEST, st, lmh::launch_division_selftest(temperature, dev->selftest, st),
              "division self-test");
   int count = -1;
   if ((e = cudaMemcpyAsync(&count, dev->selftest, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
@@ -979,7 +973,7 @@ int lmhead_engine_gemm(const uint16_t* A, const uint16_t* B, int64_t M, int64_t 
   CUtensorMap tc;
   LMH_TRY(make_out_tmap(&tc, D, N, M, N * 4, true));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  LMH_LAUNCH(K_ENGINE_GEMM, st,
+  LMH_LAUNCH(lmh::K_ENGINE_GEMM, st,
              lmh::launch_gemm(lmh::Epi::StoreF32, ta, tb, p, 1, dev->sms, st, &tc),
              "engine gemm");
   return ok();

@@ -79,11 +79,49 @@ struct GemmParams {
 // Counts every kernel this library launches (reported by lmhead_kernel_launches).
 void note_launch();
 
+// Kinds of launch that the opt-in per-launch timing records (their names,
+// reported by lmhead_timing_kind_name, are in api.cu).
+enum KernelKind : int {
+  K_FWD_GEMM = 0,
+  K_FWD_MERGE,
+  K_DLOGITS_GEMM,
+  K_DHIDDEN_GEMM,
+  K_DWEIGHT_GEMM,
+  K_LOGITS_ROWWISE,
+  K_ENGINE_GEMM,
+  K_SELFTEST,
+  K_LOGITS_ROWWISE_DIV,
+  K_HIDDEN_TRANSPOSE,
+  K_COUNT
+};
+
+// Brackets the launches made during its lifetime with two CUDA events on
+// `st` while timing is enabled (lmhead_timing_enable), recording `kind`;
+// does nothing otherwise. Defined in api.cu.
+class KernelTimer {
+ public:
+  KernelTimer(int kind, cudaStream_t st);
+  ~KernelTimer();
+  KernelTimer(const KernelTimer&) = delete;
+  KernelTimer& operator=(const KernelTimer&) = delete;
+
+ private:
+  int kind_;
+  cudaStream_t st_;
+  cudaEvent_t b_ = nullptr;
+};
+
 // Shared host helpers of the C ABI (defined in api.cu): record the calling
 // thread's error message, query the current device (sm_103 check, SM count,
 // status word) and encode a 2-D bf16 TMA descriptor. Each returns an LMH_* code.
 int api_set_error(int code, const char* msg);
 int api_device(int* sms, unsigned** status);
+// The device address of the no-allocation forward's scratch array on the
+// current device, from the same per-device record as the status word.
+int api_noalloc_scratch(void** scratch);
+// Looks up that address with the current device's context (defined in
+// noalloc.cu, the file that holds the array); called once per device.
+int noalloc_scratch_lookup(void** scratch);
 int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
 

@@ -15,10 +15,11 @@
 //    fit is rejected with LMH_ERR_WORKSPACE before anything is launched.
 //  * The array occupies that much memory on every GPU where the library's
 //    device code is loaded, until the process exits.
-//  * Set-up: the first call on each device looks up the array's device address
-//    with cudaGetSymbolAddress (the array's name in host code is only a
-//    host-side stand-in, never a device address). Make that first call before
-//    any stream capture.
+//  * Set-up: the library's first call on each device (of any entry point)
+//    looks up the array's device address with cudaGetSymbolAddress, with that
+//    device current, and keeps it in the same per-device record as the status
+//    word (the array's name in host code is only a host-side stand-in, never a
+//    device address). Make that first call before any stream capture.
 //  * Every call shares the one array, and it keeps the last call's contents.
 //    Nothing in it has to start at zero: each call writes every partial it
 //    later reads. Calls whose kernels overlap on the GPU (different streams, or
@@ -27,7 +28,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
-#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -39,40 +39,31 @@ namespace {
 
 constexpr size_t kScratchBytes = static_cast<size_t>(LMH_NOALLOC_SCRATCH_BYTES);
 constexpr size_t kAlign = 256;
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
-
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once
-// per device, with that device current).
-int scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return lmh::api_set_error(LMH_ERR_LAUNCH, "no usable current device");
-  std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p) {
-      char msg[256];
-      snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-      return lmh::api_set_error(LMH_ERR_LAUNCH, msg);
-    }
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
-  return LMH_OK;
-}
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) != 0; }
 
 }  // namespace
+
+namespace lmh {
+// Called once per device, with that device current, when the library first
+// sets the device up (api.cu keeps the result beside the status word). In
+// host code g_noalloc_scratch names a host-side stand-in, never the device
+// array, so its device address has to be looked up.
+int noalloc_scratch_lookup(void** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(no-alloc scratch): %s", cudaGetErrorString(e));
+    return api_set_error(LMH_ERR_LAUNCH, msg);
+  }
+  *out = p;
+  return LMH_OK;
+}
+}  // namespace lmh
 
 extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t* weight,
                                           const int32_t* labels, int64_t T, int64_t H, int64_t V,
@@ -110,7 +101,7 @@ extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t
   int rc = lmh::api_device(&sms, &status);
   if (rc != LMH_OK) return rc;
   void* base = nullptr;
-  if ((rc = scratch_address(&base)) != LMH_OK) return rc;
+  if ((rc = lmh::api_noalloc_scratch(&base)) != LMH_OK) return rc;
   char* b = static_cast<char*>(base);
   float* pm = reinterpret_cast<float*>(b);
   float* ps = reinterpret_cast<float*>(b + plane);
@@ -138,11 +129,16 @@ extern "C" int lmhead_logprob_fwd_noalloc(const uint16_t* hidden, const uint16_t
   p.part_zl = pzl;
   p.part_ld = T;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e =
-      lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, sms, st);
-  if (e == cudaSuccess)
+  cudaError_t e;
+  {
+    lmh::KernelTimer timer(lmh::K_FWD_GEMM, st);
+    e = lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, sms, st);
+  }
+  if (e == cudaSuccess) {
+    lmh::KernelTimer timer(lmh::K_FWD_MERGE, st);
     e = lmh::launch_fwd_merge(pm, ps, pu, nullptr, pzl, labels, T, static_cast<int>(n_chunks), V,
                               out_logprob, out_entropy, out_lse, nullptr, st);
+  }
   if (e != cudaSuccess) {
     char msg[256];
     snprintf(msg, sizeof(msg), "no-alloc forward launch: %s", cudaGetErrorString(e));

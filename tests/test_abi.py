@@ -136,6 +136,43 @@ def test_argument_errors_are_reported_without_a_launch(lib):
     assert lib.lmhead_selftest_wait_timeout(10, None) == lmh.LMH_ERR_INVALID_ARG
 
 
+def test_noalloc_argument_errors_are_reported_without_a_launch(lib):
+    # lmhead_logprob_fwd_noalloc checks its arguments before any CUDA call;
+    # fake, never dereferenced addresses.
+    def call(**kw):
+        a = dict(hidden=16, weight=16, labels=16, T=4, H=256, V=4096, s=1.0, lp=16, ent=None,
+                 lse=None)
+        a.update(kw)
+        return lib.lmhead_logprob_fwd_noalloc(a["hidden"], a["weight"], a["labels"], a["T"],
+                                              a["H"], a["V"], a["s"], a["lp"], a["ent"], a["lse"],
+                                              None)
+
+    before = lib.lmhead_kernel_launches()
+    big = 2147483392 + 1  # one past LMH_MAX_DIM
+    assert call(T=-1) == lmh.LMH_ERR_INVALID_ARG
+    assert call(T=big) == lmh.LMH_ERR_INVALID_ARG
+    assert call(V=0) == lmh.LMH_ERR_INVALID_ARG
+    assert call(V=big) == lmh.LMH_ERR_INVALID_ARG
+    assert call(H=0) == lmh.LMH_ERR_INVALID_ARG
+    assert call(H=big + 7) == lmh.LMH_ERR_INVALID_ARG
+    assert call(H=12) == lmh.LMH_ERR_ALIGNMENT
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert call(s=bad) == lmh.LMH_ERR_INVALID_ARG
+    for name in ("hidden", "weight", "labels", "lp"):
+        assert call(**{name: None}) == lmh.LMH_ERR_INVALID_ARG
+    assert call(hidden=24) == lmh.LMH_ERR_ALIGNMENT
+    assert call(weight=8) == lmh.LMH_ERR_ALIGNMENT
+    assert call(labels=18) == lmh.LMH_ERR_ALIGNMENT
+    assert call(lp=18) == lmh.LMH_ERR_ALIGNMENT
+    assert call(ent=18) == lmh.LMH_ERR_ALIGNMENT
+    assert call(lse=18) == lmh.LMH_ERR_ALIGNMENT
+    # partials beyond the fixed 16 MiB scratch are refused before any device use
+    assert call(T=16384, V=152064) == lmh.LMH_ERR_WORKSPACE
+    assert b"scratch" in lib.lmhead_last_error_string()
+    assert call(T=0, hidden=None, weight=None, labels=None, lp=None) == lmh.LMH_OK
+    assert lib.lmhead_kernel_launches() == before
+
+
 def test_binding_refuses_a_missing_library(tmp_path):
     with pytest.raises(RuntimeError):
         lmh.library(str(tmp_path / "nope.so"))
