@@ -423,6 +423,57 @@ def kernel_ms(lmh, fn, steps, warmup, names):
     return sum(ms for n, ms in recs if n in names) / steps
 
 
+def kernel_breakdown(lmh, fn, steps, warmup):
+    """Average device time per call of each library kernel kind (CUDA events
+    recorded by the library on the launching stream)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    lmh.lmhead_timing_enable(True)
+    for _ in range(steps):
+        fn()
+    recs = lmh.lmhead_timing_read()
+    lmh.lmhead_timing_enable(False)
+    per = {}
+    for name, ms in recs:
+        per[name] = per.get(name, 0.0) + ms / steps
+    return per
+
+
+def peak_mem(workspace_bytes: int):
+    """Device memory of a leg: torch's peak allocation since the last reset
+    (every buffer of the leg, the library's workspace included; the library
+    itself allocates nothing) and the workspace handed to the library."""
+    import torch
+
+    return {"max_memory_allocated_gb": round(torch.cuda.max_memory_allocated() / 1e9, 3),
+            "library_workspace_gb": round(workspace_bytes / 1e9, 3)}
+
+
+def bwd_roofline_ms(T, H, V, peaks):
+    """Per-kernel lower bounds of the backward of T rows (T <= 16384): each
+    GEMM at max(its 2THV flops at the burst bf16 peak, its algorithmic bytes at
+    the HBM peak), the transpose at HBM speed."""
+    flop_ms = 2.0 * T * H * V / (peaks["bf16_tflops"] * 1e12) * 1e3
+
+    def hbm(b):
+        return b / (peaks["hbm_gbs"] * 1e9) * 1e3
+
+    return {
+        # read W and hidden, write bf16 dl
+        "dlogits_gemm": max(flop_ms, hbm(2.0 * V * H + 2.0 * T * H + 2.0 * T * V)),
+        # read dl and W, write bf16 grad_hidden
+        "grad_hidden_gemm": max(flop_ms, hbm(2.0 * T * V + 2.0 * V * H + 2.0 * T * H)),
+        "hidden_transpose": hbm(4.0 * T * H),
+        # read the two fp32 partials of grad_hidden, write it in bf16
+        "grad_hidden_sum": hbm(10.0 * T * H),
+        # read hidden^T and dl, write fp32 grad_weight
+        "grad_weight_gemm": max(flop_ms, hbm(2.0 * T * H + 2.0 * T * V + 4.0 * V * H)),
+    }
+
+
 def timed(fn, steps, warmup):
     import torch
 
@@ -477,11 +528,13 @@ def run_gpu(args):
         lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse, grad_hidden=gh,
                                grad_weight=gw, workspace=ws_b)
 
+    torch.cuda.reset_peak_memory_stats(dev)
     for _ in range(args.warmup):
         fwd()
         bwd()
     torch.cuda.synchronize()
     lmh.lmhead_device_status()
+    main_mem = peak_mem(ws_f.numel() + ws_b.numel())
 
     uuid = None
     try:
@@ -530,6 +583,8 @@ def run_gpu(args):
     bytes_per_launch = {  # HBM-bound helpers of the step
         "fwd_merge": (12.0 * n_fwd_chunks(V) + 20.0) * T,  # m, s, u; zl, label; 3 outputs
         "hidden_transpose": 4.0 * min(T, rows_per_chunk) * H,
+        # the two K segments' fp32 partials of grad_hidden in, bf16 out
+        "grad_hidden_sum": 10.0 * min(T, rows_per_chunk) * H,
     }
     for k, info in kernels.items():
         if k in flops_per_launch:
@@ -556,6 +611,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws} (rows per GPU fixed)",
                    "l2": "inputs larger than L2 (weight 1.09 GB); no flush"},
         "gpu_launches": launches, "roofline": roofline, "kernels": kernels, "clocks": clk,
+        "peak_mem": main_mem,
         "model_tflops_per_gpu": 6.0 * T * H * V / (ms_per_step * 1e-3) / 1e12,
         # the whole step against the same sustained rate: 8THV flops as executed
         # (forward, recomputed logits, grad_hidden, grad_weight)
@@ -641,7 +697,7 @@ def run_gpu(args):
                                            workspace=ws_b)
 
         step_kernels = ("fused_fwd_gemm", "fwd_merge", "dlogits_gemm", "grad_hidden_gemm",
-                        "hidden_transpose", "grad_weight_gemm")
+                        "grad_hidden_sum", "hidden_transpose", "grad_weight_gemm")
         e_ms = kernel_ms(lmh, ent_step, args.steps, 2, step_kernels)
         q2 = torch.empty(T, device=dev)
         fq = lambda: lmh.lmhead_logprob_fwd_stats(hidden, weight, labels, s,  # noqa: E731
@@ -676,10 +732,53 @@ def run_gpu(args):
                                      "tflops_as_executed": 8.0 * T * H * V / (e_ms * 1e-3) / 1e12},
             "fwd_with_sum_p2": {"ms_kernels": q_ms, "tokens_per_s": T / (q_ms * 1e-3),
                                 "tflops": 2.0 * T * H * V / (q_ms * 1e-3) / 1e12}}
+        # the backward of short batches of the same head (the row counts of a
+        # rollout's log-prob recompute and of training micro-batches), per kernel
+        # against its roofline: each GEMM at max(2THV flops at the burst peak,
+        # its algorithmic bytes at HBM speed)
+        small_b = {}
+        for Ts in (128, 512, 1024, 2048):
+            lmh.lmhead_logprob_fwd(hidden[:Ts], weight, labels[:Ts], s, out_logprob=lp[:Ts],
+                                   out_entropy=ent[:Ts], out_lse=lse[:Ts], workspace=ws_f)
+            fb = lambda: lmh.lmhead_logprob_bwd(hidden[:Ts], weight, labels[:Ts],  # noqa: E731
+                                                grad[:Ts], s, lse=lse[:Ts], grad_hidden=gh[:Ts],
+                                                grad_weight=gw, workspace=ws_b)
+            per = kernel_breakdown(lmh, fb, args.steps, 3)
+            bound = bwd_roofline_ms(Ts, H, V, peaks)
+            tot = sum(per.values())
+            small_b[f"T={Ts}"] = {
+                "ms_kernels": round(tot, 4), "tokens_per_s": Ts / (tot * 1e-3),
+                "kernels_ms": {k: round(v, 4) for k, v in per.items()},
+                "roofline_ms": round(sum(bound.values()), 4),
+                "frac_of_roofline": round(sum(bound.values()) / tot, 4),
+                "kernel_frac": {k: round(bound[k] / per[k], 4) for k in bound if k in per}}
+        extras["bwd_small_batches"] = {
+            "workload": "backward of T rows, H=3584 V=152064, lse given",
+            "peaks": f"bf16_tflops (burst) {peaks['bf16_tflops']} and hbm_gbs "
+                     f"{peaks['hbm_gbs']} {peak_src}", **small_b}
+        # the backward's memory lever: a smaller row chunk shrinks the dl
+        # scratch (bf16 [row_chunk, V]) at some cost in time; the default
+        # workspace is freed first, so each peak holds one workspace
+        ws_b = None
+        torch.cuda.empty_cache()
+        chunks = {}
+        for rc in (16384, 8192, 4096):
+            wsb_c = torch.empty(lmh.lmhead_workspace_size_bwd(T, H, V, rc), dtype=torch.uint8,
+                                device=dev)
+            torch.cuda.reset_peak_memory_stats(dev)
+            fc = lambda: lmh.lmhead_logprob_bwd_chunked(  # noqa: E731
+                hidden, weight, labels, grad, s, row_chunk=rc, lse=lse, grad_hidden=gh,
+                grad_weight=gw, workspace=wsb_c)
+            per = kernel_breakdown(lmh, fc, max(3, args.steps // 4), 2)
+            chunks[f"row_chunk={rc}"] = {"bwd_ms_kernels": round(sum(per.values()), 4),
+                                         "peak_mem": peak_mem(wsb_c.numel())}
+            del wsb_c
+        extras["bwd_row_chunks"] = {"workload": WORKLOAD + ", backward only", **chunks}
         gh = gw = ws_b = hidden = weight = None  # free before the next legs
         torch.cuda.empty_cache()
         # forward only, Llama-like shape
         T2, H2, V2 = 4096, 4096, 32000
+        torch.cuda.reset_peak_memory_stats(dev)
         h2, w2, l2, _ = make_inputs(T2, H2, V2, 99, dev)
         ws2 = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, T2, H2, V2), dtype=torch.uint8,
                           device=dev)
@@ -692,10 +791,12 @@ def run_gpu(args):
         extras["fwd_only"]["T=4096 H=4096 V=32000"] = {
             "tokens_per_s": T2 / (f2 * 1e-3), "ms_per_call": f2, "ms_kernels": fk2,
             "tflops_kernels": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12,
-            "frac_of_burst_peak": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+            "frac_of_burst_peak": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "peak_mem": peak_mem(ws2.numel())}
         del h2, w2
         # tiny fused forward T=64 H=256 V=4096: a latency figure, no roofline
         Tt, Ht, Vt = 64, 256, 4096
+        torch.cuda.reset_peak_memory_stats(dev)
         ht_, wt_, lt_, _ = make_inputs(Tt, Ht, Vt, 1, dev)
         wst = torch.empty(lmh.lmhead_workspace_size(lmh.LMH_OP_FWD, Tt, Ht, Vt), dtype=torch.uint8,
                           device=dev)
@@ -704,13 +805,15 @@ def run_gpu(args):
                                               out_entropy=entt, workspace=wst)
         extras["tiny_fwd"] = {"workload": "fused forward T=64 H=256 V=4096",
                               "ms_per_call": timed(fwdt, 50, 5),
-                              "ms_kernels": kernel_ms(lmh, fwdt, 50, 5, fwd_kernels)}
+                              "ms_kernels": kernel_ms(lmh, fwdt, 50, 5, fwd_kernels),
+                              "peak_mem": peak_mem(wst.numel())}
         del ht_, wt_
         # packed variable-length batch: 32 sequences of seeded lengths in
         # [128, 4096], concatenated; H=5120 V=152064; one fwd+bwd step
         import workloads as W
 
         Tp, Hp, Vp = int(sum(W.packed_lengths())), 5120, 152064
+        torch.cuda.reset_peak_memory_stats(dev)
         hp, wp, lbp, gp = make_inputs(Tp, Hp, Vp, 5, dev)
         lpp, entp, lsep = (torch.empty(Tp, device=dev) for _ in range(3))
         ghp = torch.empty(Tp, Hp, dtype=torch.bfloat16, device=dev)
@@ -731,11 +834,13 @@ def run_gpu(args):
         extras["packed_varlen_fwd_bwd"] = {
             "workload": f"32 sequences, lengths in [128, 4096], T={Tp} H={Hp} V={Vp}",
             "ms_kernels_per_step": p_ms, "tokens_per_s": Tp / (p_ms * 1e-3),
-            "tflops_as_executed": p_tf, "frac_of_sustained": p_tf / peak}
+            "tflops_as_executed": p_tf, "frac_of_sustained": p_tf / peak,
+            "peak_mem": peak_mem(wsfp.numel() + wsbp.numel())}
         del hp, wp, ghp, gwp, wsfp, wsbp
         torch.cuda.empty_cache()
         # logits path: bf16 logits [8192, 152064] (2.49 GB > L2)
         T3, V3 = 8192, 152064
+        torch.cuda.reset_peak_memory_stats(dev)
         g3 = torch.Generator(device=dev)
         g3.manual_seed(7)
         x = (torch.randn(T3, V3, generator=g3, device=dev) * 2.0
@@ -772,7 +877,7 @@ def run_gpu(args):
                          "peak_source": f"hbm_gbs {peak_src}",
                          "traffic": traffic_for("logits_rowwise"),
                          "algorithmic_bytes_per_launch": T3 * V3 * 2},
-            "clocks": l_clk}
+            "clocks": l_clk, "peak_mem": peak_mem(0)}
         # sampler-parity (division) form on the same logits, and the mismatch
         # counts against torch's own fp32 sampler formula on the GPU
         temps = torch.full((T3,), 0.7, dtype=torch.float32, device=dev)

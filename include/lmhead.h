@@ -52,6 +52,13 @@
  *    log-prob, entropy, lse, sum_p2 and grad_hidden are bit-identical
  *    whichever engine runs. grad_weight is deterministic for a given engine
  *    and SM count; its summation order follows the engine's waves.
+ *  - By default a short grad_hidden (few 128-row tiles) also runs on
+ *    narrower tiles (64, 128 or 192 columns, or 128-column pairs) so that it
+ *    spreads over more SMs; each output element's K walk, and so its bits,
+ *    stay the same. LMH_GEMM_STORE_ENGINE (a diagnostic, read once per
+ *    process) forces the engine of grad_hidden and grad_weight: "w" wide
+ *    pairs, "p256" / "p128" pairs, "s256" / "s192" / "s128" / "s64" single
+ *    CTAs; it overrides LMH_GEMM_CTA_PAIRS for them.
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
@@ -84,8 +91,10 @@ struct CUstream_st; /* cudaStream_t */
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
  * Returns SIZE_MAX for invalid arguments. The forward needs 16 bytes per row
  * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
- * row, a bf16 dlogits buffer of min(T, 16384) x V and a bf16 transpose of one
- * 16384-row chunk of hidden (H x min(T, 16384)).
+ * row, a bf16 dlogits buffer of min(T, 16384) x V, a bf16 transpose of one
+ * 16384-row chunk of hidden (H x min(T, 16384)) and the fp32 partials of one
+ * chunk's grad_hidden, one per half of the vocabulary (2 x min(T, 16384) x H,
+ * rows rounded up to 128).
  */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 
@@ -135,8 +144,11 @@ int lmhead_logprob_fwd_stats(const uint16_t* hidden, const uint16_t* weight, con
  *   workspace     >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) bytes
  * Rows are processed in fixed chunks of 16384; dlogits of a chunk are rounded
  * to bf16 before both contractions; grad_weight sums the chunks in ascending
- * order. T == 0 zeroes grad_weight (then only grad_weight has to be a valid
- * pointer).
+ * order. grad_hidden sums over the vocabulary in two fixed halves (the first
+ * ceil(nk / 2) of the nk 64-column blocks, then the rest), each in order, and
+ * rounds their fp32 sum once; the halves depend on V alone, so every row gets
+ * the same association in any batch. T == 0 zeroes grad_weight (then only
+ * grad_weight has to be a valid pointer).
  */
 int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                        const float* grad_logprob, const float* lse, int64_t T, int64_t H,
@@ -162,6 +174,31 @@ int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
                                int64_t T, int64_t H, int64_t V, float inv_temperature,
                                uint16_t* grad_hidden, float* grad_weight, void* workspace,
                                size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * lmhead_logprob_entropy_bwd with a caller-chosen row chunk, to bound the
+ * backward's memory. The verl page recomputes the logits chunk by chunk in
+ * its checkpointed backward so that no [rows, V] activation stays alive; here
+ * the workspace holds one chunk's bf16 dlogits [row_chunk, V] and its
+ * transposed hidden [H, row_chunk], so a smaller chunk shrinks it (at
+ * H = 3584, V = 152064: about 5.1 GB at 16384 rows, 1.3 GB at 4096).
+ *   row_chunk  a multiple of 128 in [128, 1048576]; LMH_ERR_INVALID_ARG else
+ *   workspace  >= lmhead_workspace_size_bwd(T, H, V, row_chunk) bytes
+ * Everything else as lmhead_logprob_entropy_bwd (grad_entropy may be NULL,
+ * then the plain backward). grad_hidden does not depend on row_chunk, bit for
+ * bit: each row's dlogits and its K = V walk are the same. grad_weight sums
+ * the chunks in ascending order, so its rounding depends on row_chunk
+ * (deterministically). lmhead_logprob_bwd uses row_chunk = 16384.
+ */
+int lmhead_logprob_bwd_chunked(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* labels, const float* grad_logprob,
+                               const float* grad_entropy, const float* lse, const float* entropy,
+                               int64_t T, int64_t H, int64_t V, float inv_temperature,
+                               int64_t row_chunk, uint16_t* grad_hidden, float* grad_weight,
+                               void* workspace, size_t workspace_bytes,
+                               struct CUstream_st* stream);
+/* Workspace bytes of lmhead_logprob_bwd_chunked (SIZE_MAX for bad arguments). */
+size_t lmhead_workspace_size_bwd(int64_t T, int64_t H, int64_t V, int64_t row_chunk);
 
 /*
  * Sampler formula on materialised logits (verl page, the
@@ -278,6 +315,42 @@ int lmhead_logprob_merge(const float* part_m, const float* part_s, const float* 
                          const float* label_logit, const int32_t* labels, int64_t T, int64_t V,
                          float* out_logprob, float* out_entropy, float* out_lse,
                          struct CUstream_st* stream);
+
+/*
+ * The backward of one vocab shard (the SkyRL page's chunked distributed
+ * log-prob, whose tensor-parallel ranks each hold a slice of the vocabulary).
+ * The shard holds rows [v_offset, v_offset + V) of the weight; labels index
+ * the whole vocabulary, and a label outside the shard gets no one-hot term
+ * here (its shard adds it), so no caller shifts labels.
+ *   lse          f32 [T], required: the whole vocabulary's lse, as
+ *                lmhead_logprob_merge returns it (a shard cannot recompute it)
+ *   grad_logprob, grad_entropy, entropy  as lmhead_logprob_entropy_bwd;
+ *                entropy (the whole distribution's) is required with
+ *                grad_entropy
+ *   v_offset     >= 0 (no alignment needed in the backward)
+ *   grad_hidden_part  f32 [T, H], overwritten with this shard's dlogits * W,
+ *                16-byte aligned. The whole grad_hidden is the sum over the
+ *                shards: lmhead_sum_ranks_bf16 adds the ranks' parts in rank
+ *                order and rounds once, so every rank gets the same bits.
+ *   grad_weight  f32 [V, H], overwritten: this shard's rows (no exchange)
+ *   workspace    >= lmhead_workspace_size(LMH_OP_BWD, T, H, V) (V = the shard's)
+ */
+int lmhead_logprob_bwd_shard(const uint16_t* hidden, const uint16_t* weight,
+                             const int32_t* labels, const float* grad_logprob,
+                             const float* grad_entropy, const float* lse, const float* entropy,
+                             int64_t T, int64_t H, int64_t V, int64_t v_offset,
+                             float inv_temperature, float* grad_hidden_part, float* grad_weight,
+                             void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream);
+
+/*
+ * out[i] = bf16(((parts[0][i] + parts[1][i]) + ...) + parts[n_parts - 1][i]),
+ * round to nearest once at the end: a fixed, rank-ordered sum of the shards'
+ * grad_hidden partials after they are all-gathered (parts f32
+ * [n_parts][count], contiguous; out bf16 [count]). n_parts in [1, 65536].
+ */
+int lmhead_sum_ranks_bf16(const float* parts, int64_t n_parts, int64_t count, uint16_t* out,
+                          struct CUstream_st* stream);
 
 /*
  * Forward without a workspace, for callers that cannot allocate device memory

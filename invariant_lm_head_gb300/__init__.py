@@ -73,6 +73,12 @@ SIGNATURES = {
                                     ctypes.c_size_t, _P], ctypes.c_int),
     "lmhead_logprob_fwd_noalloc": ([_P, _P, _P, _I64, _I64, _I64, _F, _P, _P, _P, _P],
                                    ctypes.c_int),
+    "lmhead_logprob_bwd_chunked": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _F, _I64, _P, _P,
+                                    _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "lmhead_workspace_size_bwd": ([_I64, _I64, _I64, _I64], ctypes.c_size_t),
+    "lmhead_logprob_bwd_shard": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F, _P, _P,
+                                  _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "lmhead_sum_ranks_bf16": ([_P, _I64, _I64, _P, _P], ctypes.c_int),
 }
 
 _lib_handle: Optional[ctypes.CDLL] = None
@@ -297,6 +303,96 @@ def lmhead_logprob_entropy_bwd(hidden, weight, labels, grad_logprob, grad_entrop
         _ptr(grad_weight), _ptr(ws), ws_bytes, _stream_ptr(stream))
     _check("lmhead_logprob_entropy_bwd", rc)
     return grad_hidden, grad_weight
+
+
+def lmhead_workspace_size_bwd(T: int, H: int, V: int, row_chunk: int) -> int:
+    """Workspace bytes of lmhead_logprob_bwd_chunked."""
+    n = library().lmhead_workspace_size_bwd(T, H, V, row_chunk)
+    if n == ctypes.c_size_t(-1).value:
+        _check("lmhead_workspace_size_bwd", LMH_ERR_INVALID_ARG)
+    return n
+
+
+def lmhead_logprob_bwd_chunked(hidden, weight, labels, grad_logprob, inv_temperature: float = 1.0,
+                               *, row_chunk: int, grad_entropy=None, lse=None, entropy=None,
+                               grad_hidden=None, grad_weight=None, workspace=None, stream=None):
+    """Backward with a chosen row chunk (bounded workspace). Returns (grad_hidden, grad_weight)."""
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight, "weight", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    for t, n in ((grad_logprob, "grad_logprob"), (grad_entropy, "grad_entropy"), (lse, "lse"),
+                 (entropy, "entropy")):
+        if t is not None:
+            _need(t, n, torch.float32, dev, 1)
+    T, H = hidden.shape
+    V = weight.shape[0]
+    if grad_hidden is None:
+        grad_hidden = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    if grad_weight is None:
+        grad_weight = torch.empty(V, H, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(lmhead_workspace_size_bwd(T, H, V, row_chunk), 16),
+                                dtype=torch.uint8, device=dev)
+    rc = library().lmhead_logprob_bwd_chunked(
+        _ptr(hidden), _ptr(weight), _ptr(labels), _ptr(grad_logprob), _ptr(grad_entropy),
+        _ptr(lse), _ptr(entropy), T, H, V, float(inv_temperature), int(row_chunk),
+        _ptr(grad_hidden), _ptr(grad_weight), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream))
+    _check("lmhead_logprob_bwd_chunked", rc)
+    return grad_hidden, grad_weight
+
+
+def lmhead_logprob_bwd_shard(hidden, weight_shard, labels, grad_logprob, lse, v_offset: int,
+                             inv_temperature: float = 1.0, *, grad_entropy=None, entropy=None,
+                             grad_hidden_part=None, grad_weight=None, workspace=None, stream=None):
+    """One vocab shard's backward (see include/lmhead.h).
+
+    lse (and entropy, with grad_entropy) are the whole vocabulary's, f32 [T].
+    Returns (grad_hidden_part f32 [T, H], grad_weight f32 [V_shard, H]).
+    """
+    torch = _torch()
+    dev = hidden.device
+    _need(hidden, "hidden", torch.bfloat16, dev, 2)
+    _need(weight_shard, "weight_shard", torch.bfloat16, dev, 2)
+    _need(labels, "labels", torch.int32, dev, 1)
+    for t, n in ((grad_logprob, "grad_logprob"), (grad_entropy, "grad_entropy"), (lse, "lse"),
+                 (entropy, "entropy")):
+        if t is not None:
+            _need(t, n, torch.float32, dev, 1)
+    T, H = hidden.shape
+    V = weight_shard.shape[0]
+    if grad_hidden_part is None:
+        grad_hidden_part = torch.empty(T, H, dtype=torch.float32, device=dev)
+    if grad_weight is None:
+        grad_weight = torch.empty(V, H, dtype=torch.float32, device=dev)
+    ws, ws_bytes = _workspace(LMH_OP_BWD, T, H, V, workspace, dev)
+    rc = library().lmhead_logprob_bwd_shard(
+        _ptr(hidden), _ptr(weight_shard), _ptr(labels), _ptr(grad_logprob), _ptr(grad_entropy),
+        _ptr(lse), _ptr(entropy), T, H, V, int(v_offset), float(inv_temperature),
+        _ptr(grad_hidden_part), _ptr(grad_weight), _ptr(ws), ws_bytes, _stream_ptr(stream))
+    _check("lmhead_logprob_bwd_shard", rc)
+    return grad_hidden_part, grad_weight
+
+
+def lmhead_sum_ranks_bf16(parts, *, out=None, stream=None):
+    """bf16 of the rank-ordered sum of parts [n, ...] (f32) over its first axis."""
+    torch = _torch()
+    dev = parts.device
+    if not isinstance(parts, torch.Tensor) or parts.dtype != torch.float32:
+        raise TypeError("parts must be a float32 tensor")
+    if parts.device != dev or not parts.is_contiguous() or parts.dim() < 2:
+        raise ValueError("parts must be a contiguous tensor [n, ...]")
+    n = parts.shape[0]
+    count = parts[0].numel()
+    if out is None:
+        out = torch.empty(parts.shape[1:], dtype=torch.bfloat16, device=dev)
+    if out.dtype != torch.bfloat16 or out.numel() != count or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor of parts[0]'s size")
+    rc = library().lmhead_sum_ranks_bf16(_ptr(parts), n, count, _ptr(out), _stream_ptr(stream))
+    _check("lmhead_sum_ranks_bf16", rc)
+    return out
 
 
 def logprob_from_logits(logits, labels, inv_temperature: float = 1.0, *, out_logprob=None,

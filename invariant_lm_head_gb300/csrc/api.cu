@@ -190,13 +190,15 @@ struct BwdWs {
   float* ent;
   uint16_t* dl;  // [Tc][Vpad] bf16 dlogits of one row chunk
   uint16_t* ht;  // [H][Tcpad] bf16 transpose of one row chunk of hidden
-  int64_t vpad, tc, tcpad;
+  float* ghp;    // [2][ghp_rows][H] fp32 partials of grad_hidden, one per K segment
+  int64_t vpad, tc, tcpad, ghp_rows;
 };
 
-BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
+BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V,
+                int64_t row_chunk = lmh::kBwdRowChunk) {
   BwdWs w;
   w.vpad = round_up(V, 8);
-  w.tc = T < lmh::kBwdRowChunk ? T : lmh::kBwdRowChunk;
+  w.tc = T < row_chunk ? T : row_chunk;
   w.fwd = carve_fwd(c, T, V);
   w.lse = c.take<float>(T);
   w.lp = c.take<float>(T);
@@ -204,6 +206,8 @@ BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V) {
   w.dl = c.take<uint16_t>(w.tc * w.vpad);
   w.tcpad = round_up(w.tc, 8);
   w.ht = c.take<uint16_t>(H * w.tcpad);
+  w.ghp_rows = round_up(w.tc, lmh::kBM);
+  w.ghp = c.take<float>(2 * w.ghp_rows * H);
   return w;
 }
 
@@ -249,7 +253,7 @@ int launch_status(cudaError_t e, const char* what) {
 const char* const kKindNames[lmh::K_COUNT] = {
     "fused_fwd_gemm", "fwd_merge",   "dlogits_gemm",  "grad_hidden_gemm",  "grad_weight_gemm",
     "logits_rowwise", "engine_gemm", "selftest_wait", "logits_rowwise_div",
-    "hidden_transpose"};
+    "hidden_transpose", "sum_parts_bf16", "grad_hidden_sum"};
 
 struct TimingRec {
   int kind;
@@ -452,19 +456,36 @@ int copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cu
   return LMH_OK;
 }
 
+// Options of one backward call beyond the sizes and pointers.
+struct BwdOpts {
+  // A vocab shard: this call's weight holds rows [v_offset, v_offset + V) of
+  // the whole head, labels index the whole vocabulary, and lse (and entropy)
+  // are those of the whole distribution, so they cannot be recomputed here.
+  int64_t v_offset = 0;
+  bool shard = false;
+  // Rows per chunk: dl and the transposed hidden hold this many rows.
+  int64_t row_chunk = lmh::kBwdRowChunk;
+};
+
 // Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
-// chunk of kBwdRowChunk rows, in ascending order:
+// chunk of o.row_chunk rows, in ascending order:
 //   dl   = recomputed logits -> dlogits (bf16 [rows][Vpad])
-//   dH   = dl * W          (A = dl K-major, B = W MN-major)
+//   dH   = dl * W          (A = dl K-major, B = W MN-major); bf16, or fp32
+//                          into grad_hidden_f32 (a vocab shard's partial)
 //   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
 //   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
 int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                  const float* grad_lp, const float* grad_ent, const float* lse, const float* ent,
                  int64_t T, int64_t H, int64_t V, float s, uint16_t* grad_hidden,
-                 float* grad_weight, void* workspace, size_t workspace_bytes,
-                 struct CUstream_st* stream) {
+                 float* grad_hidden_f32, float* grad_weight, void* workspace,
+                 size_t workspace_bytes, struct CUstream_st* stream, const BwdOpts& o = BwdOpts{}) {
   LMH_TRY(check_dims(T, H, V, true));
   LMH_TRY(check_temperature(s));
+  if (o.v_offset < 0 || o.v_offset > LMH_MAX_DIM - V)
+    return fail(LMH_ERR_INVALID_ARG, "v_offset=%lld out of range", (long long)o.v_offset);
+  if (o.row_chunk < lmh::kBM || o.row_chunk % lmh::kBM != 0 || o.row_chunk > lmh::kBwdMaxRowChunk)
+    return fail(LMH_ERR_INVALID_ARG, "row_chunk=%lld must be a multiple of %d in [%d, %lld]",
+                (long long)o.row_chunk, lmh::kBM, lmh::kBM, (long long)lmh::kBwdMaxRowChunk);
   LMH_TRY(check_ptr(grad_weight, 16, "grad_weight"));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   DeviceInfo* dev = nullptr;
@@ -482,16 +503,24 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   LMH_TRY(check_ptr(grad_ent, 4, "grad_entropy", true));
   LMH_TRY(check_ptr(lse, 4, "lse", true));
   LMH_TRY(check_ptr(ent, 4, "entropy", true));
-  LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
+  if (grad_hidden_f32)
+    LMH_TRY(check_ptr(grad_hidden_f32, 16, "grad_hidden_part"));
+  else
+    LMH_TRY(check_ptr(grad_hidden, 16, "grad_hidden"));
   if (!grad_lp && !grad_ent)
     return fail(LMH_ERR_INVALID_ARG, "grad_logprob and grad_entropy are both NULL");
-  const size_t need = lmhead_workspace_size(LMH_OP_BWD, T, H, V);
+  if (o.shard && (!lse || (grad_ent && !ent)))
+    return fail(LMH_ERR_INVALID_ARG,
+                "a vocab shard needs the whole vocabulary's lse (and entropy with grad_entropy)");
+  Carver sizing{nullptr};
+  carve_bwd(sizing, T, H, V, o.row_chunk);
+  const size_t need = sizing.off + kRegionAlign;
   if (!workspace || workspace_bytes < need)
     return fail(LMH_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu", need, workspace_bytes);
   LMH_TRY(check_ptr(workspace, 16, "workspace"));
   LMH_TRY(device_info(&dev));
   Carver c{static_cast<char*>(workspace)};
-  const BwdWs w = carve_bwd(c, T, H, V);
+  const BwdWs w = carve_bwd(c, T, H, V, o.row_chunk);
 
   if (!lse || (grad_ent && !ent)) {
     LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, s, w.lp, w.ent, w.lse, w.fwd, st));
@@ -501,8 +530,8 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   CUtensorMap t_w_mn;
   LMH_TRY(make_tmap(&t_w_mn, weight, H, V, H * 2, 64, lmh::kBK));  // [K=V][N=H]
 
-  for (int64_t c0 = 0; c0 < T; c0 += lmh::kBwdRowChunk) {
-    const int64_t rows = (T - c0) < lmh::kBwdRowChunk ? (T - c0) : lmh::kBwdRowChunk;
+  for (int64_t c0 = 0; c0 < T; c0 += o.row_chunk) {
+    const int64_t rows = (T - c0) < o.row_chunk ? (T - c0) : o.row_chunk;
     const uint16_t* h_c = hidden + c0 * H;
     CUtensorMap t_w, t_h, t_ht, t_dl, t_dl_mn;
     LMH_TRY(make_tmap(&t_w, weight, H, V, H * 2, lmh::kBK, lmh::kBBoxRows));   // [V][K=H]
@@ -519,27 +548,54 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     p.scale2 = s * lmh::kLog2e;
     p.inv_temp = s;
     p.labels = labels + c0;
+    p.label_base = o.v_offset;  // a label outside the shard gets no one-hot term
     p.grad = grad_lp ? grad_lp + c0 : nullptr;
     p.grad_ent = grad_ent ? grad_ent + c0 : nullptr;
     p.lse = lse + c0;
     p.ent = grad_ent ? ent + c0 : nullptr;
     CUtensorMap o_dl, o_gh, o_gw;
     LMH_TRY(make_out_tmap(&o_dl, w.dl, V, rows, w.vpad * 2, false));
-    LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
+    if (grad_hidden_f32)
+      LMH_TRY(make_out_tmap(&o_gh, grad_hidden_f32 + c0 * H, H, rows, H * 4, true));
+    else
+      LMH_TRY(make_out_tmap(&o_gh, grad_hidden + c0 * H, H, rows, H * 2, false));
     LMH_TRY(make_out_tmap(&o_gw, grad_weight, H, V, H * 4, true, true));
     LMH_LAUNCH(lmh::K_DLOGITS_GEMM, st,
                lmh::launch_gemm(lmh::Epi::DLogits, t_h, t_w, p, 1, dev->sms, st, &o_dl),
                "dlogits");
 
+    // grad_hidden sums dl * W over K = V in two fixed halves, P0 over the
+    // first ceil(nk / 2) 64-wide K blocks and P1 over the rest, each walked in
+    // order, then bf16(P0 + P1) (one K block: P0 alone). The split depends on
+    // V only, so every row and every batch gets the same association; it
+    // gives a short batch two independent MMA chains on two SMs per tile.
     lmh::GemmParams q{};
     q.status = dev->status;
     q.M = static_cast<int>(rows);
     q.N = static_cast<int>(H);
     q.K = static_cast<int>(V);
     q.b_mn = 1;
-    LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
-               lmh::launch_gemm(lmh::Epi::StoreBf16, t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
-               "grad_hidden");
+    const int64_t nk = (V + lmh::kBK - 1) / lmh::kBK;
+    if (nk >= 2) {
+      q.k_split = static_cast<int>((nk + 1) / 2);
+      q.seg_rows = static_cast<int>(w.ghp_rows);
+      CUtensorMap o_ghp;
+      LMH_TRY(make_out_tmap(&o_ghp, w.ghp, H, 2 * w.ghp_rows, H * 4, true));
+      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
+                 lmh::launch_gemm(lmh::Epi::StoreF32, t_dl, t_w_mn, q, 1, dev->sms, st, &o_ghp),
+                 "grad_hidden");
+      void* gh_out = grad_hidden_f32 ? static_cast<void*>(grad_hidden_f32 + c0 * H)
+                                     : static_cast<void*>(grad_hidden + c0 * H);
+      LMH_LAUNCH(lmh::K_DHIDDEN_SUM, st,
+                 lmh::launch_sum_parts(w.ghp, 2, w.ghp_rows * H, rows * H, gh_out,
+                                       grad_hidden_f32 == nullptr, dev->sms, st),
+                 "grad_hidden segments");
+    } else {
+      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
+                 lmh::launch_gemm(grad_hidden_f32 ? lmh::Epi::StoreF32 : lmh::Epi::StoreBf16,
+                                  t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
+                 "grad_hidden");
+    }
 
     // hidden^T of the chunk, so grad_weight reads its A operand K-major
     LMH_LAUNCH(lmh::K_HIDDEN_TRANSPOSE, st,
@@ -699,8 +755,8 @@ int lmhead_logprob_bwd(const uint16_t* hidden, const uint16_t* weight, const int
                        struct CUstream_st* stream) {
   if (T > 0 && !grad_logprob) return fail(LMH_ERR_INVALID_ARG, "grad_logprob is NULL");
   return run_backward(hidden, weight, labels, grad_logprob, nullptr, lse, nullptr, T, H, V,
-                      inv_temperature, grad_hidden, grad_weight, workspace, workspace_bytes,
-                      stream);
+                      inv_temperature, grad_hidden, nullptr, grad_weight, workspace,
+                      workspace_bytes, stream);
 }
 
 int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
@@ -710,8 +766,68 @@ int lmhead_logprob_entropy_bwd(const uint16_t* hidden, const uint16_t* weight,
                                uint16_t* grad_hidden, float* grad_weight, void* workspace,
                                size_t workspace_bytes, struct CUstream_st* stream) {
   return run_backward(hidden, weight, labels, grad_logprob, grad_entropy, lse, entropy, T, H, V,
-                      inv_temperature, grad_hidden, grad_weight, workspace, workspace_bytes,
-                      stream);
+                      inv_temperature, grad_hidden, nullptr, grad_weight, workspace,
+                      workspace_bytes, stream);
+}
+
+int lmhead_logprob_bwd_chunked(const uint16_t* hidden, const uint16_t* weight,
+                               const int32_t* labels, const float* grad_logprob,
+                               const float* grad_entropy, const float* lse, const float* entropy,
+                               int64_t T, int64_t H, int64_t V, float inv_temperature,
+                               int64_t row_chunk, uint16_t* grad_hidden, float* grad_weight,
+                               void* workspace, size_t workspace_bytes,
+                               struct CUstream_st* stream) {
+  BwdOpts o;
+  o.row_chunk = row_chunk;
+  return run_backward(hidden, weight, labels, grad_logprob, grad_entropy, lse, entropy, T, H, V,
+                      inv_temperature, grad_hidden, nullptr, grad_weight, workspace,
+                      workspace_bytes, stream, o);
+}
+
+size_t lmhead_workspace_size_bwd(int64_t T, int64_t H, int64_t V, int64_t row_chunk) {
+  if (check_dims(T, H, V, true) != LMH_OK) return SIZE_MAX;
+  if (row_chunk < lmh::kBM || row_chunk % lmh::kBM != 0 || row_chunk > lmh::kBwdMaxRowChunk) {
+    fail(LMH_ERR_INVALID_ARG, "row_chunk=%lld must be a multiple of %d in [%d, %lld]",
+         (long long)row_chunk, lmh::kBM, lmh::kBM, (long long)lmh::kBwdMaxRowChunk);
+    return SIZE_MAX;
+  }
+  Carver c{nullptr};
+  carve_bwd(c, T, H, V, row_chunk);
+  return c.off + kRegionAlign;
+}
+
+int lmhead_logprob_bwd_shard(const uint16_t* hidden, const uint16_t* weight,
+                             const int32_t* labels, const float* grad_logprob,
+                             const float* grad_entropy, const float* lse, const float* entropy,
+                             int64_t T, int64_t H, int64_t V, int64_t v_offset,
+                             float inv_temperature, float* grad_hidden_part, float* grad_weight,
+                             void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream) {
+  BwdOpts o;
+  o.v_offset = v_offset;
+  o.shard = true;
+  return run_backward(hidden, weight, labels, grad_logprob, grad_entropy, lse, entropy, T, H, V,
+                      inv_temperature, nullptr, grad_hidden_part, grad_weight, workspace,
+                      workspace_bytes, stream, o);
+}
+
+int lmhead_sum_ranks_bf16(const float* parts, int64_t n_parts, int64_t count, uint16_t* out,
+                          struct CUstream_st* stream) {
+  if (n_parts < 1 || n_parts > 65536)
+    return fail(LMH_ERR_INVALID_ARG, "n_parts=%lld must be in [1, 65536]", (long long)n_parts);
+  if (count < 0 || count > (int64_t(1) << 40))
+    return fail(LMH_ERR_INVALID_ARG, "count=%lld out of range", (long long)count);
+  if (count == 0) return ok();
+  LMH_TRY(check_ptr(parts, 4, "parts"));
+  LMH_TRY(check_ptr(out, 2, "out"));
+  DeviceInfo* dev = nullptr;
+  LMH_TRY(device_info(&dev));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  LMH_LAUNCH(lmh::K_SUM_PARTS, st,
+             lmh::launch_sum_parts(parts, static_cast<int>(n_parts), count, count, out, true,
+                                   dev->sms, st),
+             "rank-ordered sum");
+  return ok();
 }
 
 int logprob_from_logits(const uint16_t* logits, const int32_t* labels, int64_t T, int64_t V,

@@ -28,6 +28,12 @@
 // for the forward, dlogits and grad_hidden, so their bits do not depend on
 // the engine.
 //
+// Narrow tiles: single CTAs and pairs also take tiles of fewer columns (64,
+// 128 or 192 alone, 128 in a pair; MN-major B only), so a short grad_hidden
+// (K = V, few row tiles) spreads over more SMs. Their ring is cut into more,
+// smaller stages (up to 8) of the same bytes. The column split changes no
+// element's K walk, so no bit.
+//
 // Epilogues (one per contraction of the method):
 //   FwdStats   the fused forward of the SkyRL pull request "Triton backend for
 //              fused LM-head log-prob" (vocab projection folded into an online
@@ -83,6 +89,8 @@ constexpr int kStagingBytes = kBM * 128;
 // one 512-column accumulator per CTA, not double-buffered, for contractions
 // whose K is long enough to hide nothing behind the epilogue).
 constexpr int kSingle = 0, kPairMode = 1, kWideMode = 2;
+// Most stages a ring is cut into (narrow tiles have smaller stages).
+constexpr int kMaxStages = 8;
 
 // The operand ring of one CTA. Alone, a CTA stages the whole 256-row B tile
 // (48 KB a stage, 4 stages); in a CTA pair it stages half of it (32 KB a
@@ -100,7 +108,7 @@ struct Ring {
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
   // full and empty per stage, two accumulator pairs, final; then the TMEM
   // address, the abort flag, two epilogue go flags and the peer's load count
-  static_assert(8 * (2 * kStages + 5) + 20 <= kBarrierBytes, "barrier area too small");
+  static_assert(8 * (2 * kMaxStages + 5) + 20 <= kBarrierBytes, "barrier area too small");
 };
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
 
@@ -109,7 +117,14 @@ constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue thread
 // running CTAs share B tiles in L2. An m unit is one 128-row m tile, or two
 // for a CTA pair. The order changes no value.
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
-                                            int& n_count, int& vunit) {
+                                            int& n_count, int& vunit, int& seg) {
+  // with a K split, the second K segment's units follow all of the first's
+  seg = 0;
+  if (p.k_split > 0) {
+    const int per_seg = p.n_units >> 1;
+    seg = u >= per_seg ? 1 : 0;
+    u -= seg * per_seg;
+  }
   const int per_group = p.group_m * p.n_vunits;
   const int g = u / per_group;
   const int first_m = g * p.group_m;
@@ -178,13 +193,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                                           const CUtensorMap& tmC, const GemmParams& p) {
   constexpr bool kPair = kMode != kSingle;
   using R = Ring<kMode>;
-  constexpr int kS = R::kStages;
+  constexpr int kS = kMaxStages;  // barrier slots
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t staging = smem_base + kS * R::kStageBytes;  // 2 x kStagingBytes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kS * R::kStageBytes + 2 * kStagingBytes);
+  constexpr uint32_t kRingBytes = R::kStages * R::kStageBytes;
+  const uint32_t staging = smem_base + kRingBytes;  // 2 x kStagingBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes + 2 * kStagingBytes);
   // barrier layout: full[kS], empty[kS], tfull[2], tempty[2], final
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -207,16 +223,28 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int unit_stride = kPair ? static_cast<int>(cluster_nid_x()) : static_cast<int>(gridDim.x);
   auto cta_m_tile = [&](int m_unit) { return kPair ? 2 * m_unit + static_cast<int>(rank) : m_unit; };
 
+  // Output columns of a tile, and the B rows (of 64 K elements) this CTA
+  // stages per stage: a wide pair's two 128-row halves, a pair's half of its
+  // tile, or a single CTA's whole tile. A stage's bytes follow from them, and
+  // the ring holds as many stages as fit (up to kMaxStages), so a narrow
+  // tile keeps as many bytes in flight as a full one: its loads are
+  // latency-bound, not MMA-bound.
+  const int tile_n = kMode == kWideMode ? R::kTileN : p.tile_n;
+  const int b_rows = kMode == kWideMode ? 2 * kBBoxRows : (kPair ? tile_n / 2 : tile_n);
+  const uint32_t stage_tx = static_cast<uint32_t>(kABytes + b_rows * kBK * 2);
+  const uint32_t stage_stride = (stage_tx + 1023u) & ~1023u;  // 1024-byte swizzle atoms
+  const uint32_t n_st = min(static_cast<uint32_t>(kMaxStages), kRingBytes / stage_stride);
+
   // A short batch's A boxes fill only the first a_rows rows of each A tile
   // (single CTAs only): the rest is zeroed once, before any MMA reads it.
   const int a_rows = (!kPair && p.a_rows > 0) ? p.a_rows : kBM;
   if constexpr (!kPair) {
     if (a_rows < kBM) {
       const uint32_t n16 = static_cast<uint32_t>((kBM - a_rows) * 128 / 16);
-      for (uint32_t i = threadIdx.x; i < kS * n16; i += blockDim.x) {
+      for (uint32_t i = threadIdx.x; i < n_st * n16; i += blockDim.x) {
         const uint32_t st = i / n16, j = i - st * n16;
         st_shared_v4(
-            smem_base + st * R::kStageBytes + static_cast<uint32_t>(a_rows) * 128u + 16u * j, 0u,
+            smem_base + st * stage_stride + static_cast<uint32_t>(a_rows) * 128u + 16u * j, 0u,
             0u, 0u, 0u);
       }
       fence_proxy_async_smem();
@@ -270,9 +298,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       bool ok = true;
       int wave = 0;
       for (int u = first_unit; ok && u < p.n_units; u += unit_stride, ++wave) {
-        int m_unit, n_first, n_count, vunit;
-        unit_coords(p, u, m_unit, n_first, n_count, vunit);
+        int m_unit, n_first, n_count, vunit, seg;
+        unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
         const int m_tile = cta_m_tile(m_unit);
+        const int kb0 = seg ? p.k_split : 0;
+        const int kb_n = (p.k_split > 0 ? (seg ? kb_total : p.k_split) : kb_total) - kb0;
         // grad_weight walks K (the rows) downwards on odd waves, so a wave
         // starts on the operand rows the previous wave touched last, while
         // they are still in L2.
@@ -281,21 +311,22 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const int n_tile = n_first + j;
           // first B row this CTA stages in each 256-column block: the whole
           // block alone, its half in a pair
-          const int b_row0 = n_tile * R::kTileN + (kPair ? static_cast<int>(rank) * kBBoxRows : 0);
-          for (int kstep = 0; kstep < kb_total; ++kstep) {
-            const int kb = k_down ? kb_total - 1 - kstep : kstep;
+          const int b_row0 = n_tile * tile_n +
+                             (kPair ? static_cast<int>(rank) * (b_rows / R::kNBlocks) : 0);
+          for (int kstep = 0; kstep < kb_n; ++kstep) {
+            const int kb = kb0 + (k_down ? kb_n - 1 - kstep : kstep);
             if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
               ok = false;
               break;
             }
-            const uint32_t sA = smem_base + stage * R::kStageBytes;
+            const uint32_t sA = smem_base + stage * stage_stride;
             const uint32_t sB = sA + kABytes;
             // One arrive per stage, by CTA 0, expecting both CTAs' bytes; both
             // CTAs' boxes complete on CTA 0's barrier, issued in the pair form
             // (measured: CTA 0 issuing the plain form made the pair 10 % slower).
             if (rank == 0)
-              mbar_arrive_expect_tx(full_bar(stage), (kPair ? 2 : 1) * R::kStageBytes -
-                                                         (kBM - a_rows) * 128);
+              mbar_arrive_expect_tx(full_bar(stage),
+                                    (kPair ? 2u : 1u) * stage_tx - (kBM - a_rows) * 128);
             const uint32_t fbar = kPair ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
             auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
               if constexpr (kPair)
@@ -314,17 +345,18 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             };
             auto load_b = [&]() {
               constexpr int kBlockBytes = R::kBBytes / R::kNBlocks;
+              // B rows of one N block this CTA stages (a multiple of 64, and
+              // of 128 when B is K-major)
+              const int block_rows = b_rows / R::kNBlocks;
 #pragma unroll
               for (int nb = 0; nb < R::kNBlocks; ++nb) {
                 const uint32_t dst = sB + nb * kBlockBytes;
                 const int row = b_row0 + nb * kBN;
                 if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
-#pragma unroll
-                  for (int i = 0; i < kBlockBytes / kMnBoxBytes; ++i)
+                  for (int i = 0; i < block_rows / 64; ++i)
                     load(dst + i * kMnBoxBytes, &tmB, row + 64 * i, kb * kBK);
                 } else {  // [N][K]: 128-row boxes
-#pragma unroll
-                  for (int i = 0; i < kBlockBytes / kBHalfBytes; ++i)
+                  for (int i = 0; i < block_rows / kBBoxRows; ++i)
                     load(dst + i * kBHalfBytes, &tmB, kb * kBK, row + kBBoxRows * i);
                 }
               }
@@ -341,7 +373,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               load_b();
             }
             ++issued;
-            if (++stage == kS) {
+            if (++stage == n_st) {
               stage = 0;
               phase ^= 1u;
             }
@@ -357,11 +389,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         // Drain: wait (bounded, ignoring the abort flag) for the copies this
         // thread issued, so none lands in shared memory after the CTA exits.
         volatile int no_abort = 0;
-        const long long n = issued < kS ? issued : kS;
+        const long long n = issued < n_st ? issued : n_st;
         uint32_t s = stage, ph = phase;
         for (long long i = 0; i < n; ++i) {
           if (s == 0) {
-            s = kS - 1;
+            s = n_st - 1;
             ph ^= 1u;
           } else {
             --s;
@@ -373,13 +405,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   } else if (warp == 1) {
     if (lane == 0 && (!kPair || rank == 0)) {
       // ------------------------------------------------------------ MMA issuer
-      const uint32_t idesc =
-          idesc_bf16_f32(kPair ? 2 * kBM : kBM, kBN, p.a_mn != 0, p.b_mn != 0);
+      // one MMA covers the whole tile, or one 256-column block of a wide tile
+      const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM,
+                                            static_cast<uint32_t>(kMode == kWideMode ? kBN : tile_n),
+                                            p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
       for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
-        int m_unit, n_first, n_count, vunit;
-        unit_coords(p, u, m_unit, n_first, n_count, vunit);
+        int m_unit, n_first, n_count, vunit, seg;
+        unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
+        const int kb_n =
+            p.k_split > 0 ? (seg ? kb_total - p.k_split : p.k_split) : kb_total;
         for (int j = 0; ok && j < n_count; ++j, ++it) {
           const uint32_t acc = it % R::kAccs;
           const uint32_t aph = (it / R::kAccs) & 1u;
@@ -389,13 +425,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * kBN;
-          for (int kb = 0; kb < kb_total; ++kb) {
+          for (int kb = 0; kb < kb_n; ++kb) {
             if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sA = smem_base + stage * R::kStageBytes;
+            const uint32_t sA = smem_base + stage * stage_stride;
             const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
             const uint64_t bdesc =
                 p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
@@ -424,7 +460,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               tc_commit_pair(empty_bar(stage), 0x3);
             else
               tc_commit(empty_bar(stage));
-            if (++stage == kS) {
+            if (++stage == n_st) {
               stage = 0;
               phase ^= 1u;
             }
@@ -462,8 +498,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     uint32_t it = 0, chunk_ctr = 0;
     bool ok = true;
     for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
-      int m_unit, n_first, n_count, vunit;
-      unit_coords(p, u, m_unit, n_first, n_count, vunit);
+      int m_unit, n_first, n_count, vunit, seg;
+      unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
       const int m_tile = cta_m_tile(m_unit);
       const int row = m_tile * kBM + row_in_tile;
       const bool row_ok = row < p.M;
@@ -509,8 +545,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
 #pragma unroll 1
-        for (int c = 0; c < R::kTileN / 32; ++c) {
-          const int col0 = n_tile * R::kTileN + c * 32;
+        for (int c = 0; c < tile_n / 32; ++c) {
+          const int col0 = n_tile * tile_n + c * 32;
           if (col0 >= p.N) break;  // uniform over the CTA
           const int nvalid = min(32, p.N - col0);
           float v[32];
@@ -587,7 +623,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             if (etid == 0 && tile_live) {
               // (x, y) of the box in the output: transposed for StoreF32T
               const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
-              const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM;
+              const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM + seg * p.seg_rows;
               if ((E == (int)Epi::StoreF32 || E == (int)Epi::StoreF32T) && p.accumulate)
                 tma_reduce_add_2d(&tmC, buf, ox, oy);
               else
@@ -612,8 +648,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           p.part_s[o] = st.s;
           p.part_u[o] = st.u;
           if (p.part_q) p.part_q[o] = st.q;
-          const int c0 = n_first * R::kTileN;
-          const int c1 = min(p.N, (n_first + n_count) * R::kTileN);
+          const int c0 = n_first * tile_n;
+          const int c1 = min(p.N, (n_first + n_count) * tile_n);
           if (lab >= c0 && lab < c1) p.part_zl[row] = zl;
         }
       }
@@ -626,7 +662,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     // Neither CTA leaves (or frees TMEM) while the other may still touch its
     // barriers, shared memory or TMEM. Between the two cluster barriers CTA 0
     // waits for every stage load still in flight in either CTA: all loads
-    // before the last kS of the further-ahead producer were consumed by MMAs,
+    // before the last n_st of the further-ahead producer were consumed by MMAs,
     // so their phases completed. A phase one CTA never loaded gets that
     // CTA's share settled here (CTA 0's arrive, or CTA 1's bytes as done),
     // so it completes when the other's bytes land. Each wait is bounded.
@@ -636,13 +672,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const long long n0 = issued, n1 = static_cast<long long>(*peer_issued);
       const long long hi = n0 > n1 ? n0 : n1;
       volatile int no_abort = 0;
-      for (long long i = hi > kS ? hi - kS : 0; i < hi; ++i) {
-        const int s = static_cast<int>(i % kS);
-        const uint32_t par = static_cast<uint32_t>((i / kS) & 1);
+      for (long long i = hi > n_st ? hi - n_st : 0; i < hi; ++i) {
+        const int s = static_cast<int>(i % n_st);
+        const uint32_t par = static_cast<uint32_t>((i / n_st) & 1);
         if (i < n0 && i >= n1)
-          mbar_complete_tx(full_bar(s), R::kStageBytes);
+          mbar_complete_tx(full_bar(s), stage_tx);
         else if (i >= n0 && i < n1)
-          mbar_arrive_expect_tx(full_bar(s), R::kStageBytes);
+          mbar_arrive_expect_tx(full_bar(s), stage_tx);
         mbar_wait(full_bar(s), par, &no_abort, p.status);
       }
     }
@@ -735,82 +771,139 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
   return e;
 }
 
-// The paired engine each contraction is built for (besides single CTAs):
-// wide pairs for the store epilogues, whose K is long or whose epilogue is
-// light; pairs for the forward and dlogits, whose K (= H) is too short to
-// hide an epilogue that no longer overlaps the next tile.
+// Engines each contraction is built for besides single CTAs: pairs for all;
+// wide pairs for the store epilogues (not the forward, whose chunk grid is
+// 256-column tiles, nor dlogits, whose K = H is too short to hide an epilogue
+// that no longer overlaps the next tile).
 template <int E>
-constexpr int kPairedMode = (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) ? kPairMode
-                                                                                 : kWideMode;
+constexpr bool kHasWide = !(E == (int)Epi::FwdStats || E == (int)Epi::DLogits);
 
 template <int E>
 int slots_for(int mode, int num_sms) {
-  return mode == kPairedMode<E> ? pair_slots<E, kPairedMode<E>>(num_sms) : 0;
+  if (mode == kPairMode) return pair_slots<E, kPairMode>(num_sms);
+  if constexpr (kHasWide<E>)
+    if (mode == kWideMode) return pair_slots<E, kWideMode>(num_sms);
+  return 0;
 }
 
 template <int E>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const GemmParams& p, int mode, int num_sms, cudaStream_t stream) {
-  if (mode == kPairedMode<E>) return launch_one<E, kPairedMode<E>>(a, b, c, p, num_sms, stream);
+  if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, num_sms, stream);
+  if constexpr (kHasWide<E>)
+    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, num_sms, stream);
   return launch_one<E, kSingle>(a, b, c, p, num_sms, stream);
 }
 
-}  // namespace
+// An engine and tile width for one launch.
+struct Engine {
+  int mode, tile_n;
+};
 
-size_t gemm_smem_bytes() { return Ring<kSingle>::kSmemBytes; }
-
-namespace {
+// Estimated time of a launch on engine `g` whose K loop dominates (grad_hidden,
+// K = V): waves of units over the SMs (or cluster slots), times the time of one
+// wave. The wave times are measured, not modelled: alone on a GB300, one wave
+// of grad_hidden at H = 3584, V = 152064 took (ms) single CTAs 0.653 (64
+// columns), 0.686 (128), 0.80 (192), 0.88 (256); pairs 0.697 (128), 0.72
+// (256); wide pairs 1.258 (512). A narrow tile does a quarter of a full one's
+// work in three quarters of its time: its K steps are bound by operand
+// delivery, not by the MMAs. The costs below are those times over 0.88.
+// With a K split, every tile is two units of half the K loop each.
+double engine_cost(const Engine& g, long long m_tiles, long long n, int num_sms, int slots,
+                   int segs = 1) {
+  const long long rows = g.mode == kSingle ? 1 : 2;
+  const long long m_units = (m_tiles + rows - 1) / rows;
+  const long long units = m_units * ((n + g.tile_n - 1) / g.tile_n) * segs;
+  const long long lanes = g.mode == kSingle ? num_sms : slots;
+  if (lanes <= 0) return 1e30;
+  const long long waves = (units + lanes - 1) / lanes;
+  double wave;
+  if (g.mode == kWideMode)
+    wave = 1.43;
+  else if (g.mode == kPairMode)
+    wave = g.tile_n == 128 ? 0.79 : 0.82;
+  else
+    wave = g.tile_n == 64 ? 0.74 : g.tile_n == 128 ? 0.78 : g.tile_n == 192 ? 0.91 : 1.0;
+  return static_cast<double>(waves) * wave / segs;
+}
 
 template <int E>
 cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
-  // Engine per contraction (same-session A/Bs of the 16384 x 3584 x 152064
-  // step, which runs at the power cap): wide pairs for grad_hidden (kernel
-  // -13 %, step -1.8 %) and grad_weight (kernel -6 %, step -1.4 %, against
-  // 256-wide pairs, which had been -1 % against single CTAs), when their waves
-  // take less time than single CTAs' (below). The forward and
-  // dlogits (K = H) run on pairs for an even number of m tiles up to 32 (T up
-  // to 4096; alone at H = 3584, V = 152064, forward: -8.5 % at 129 rows, -2 %
-  // at 2048, even at 4096; dlogits: -11 % at 512 rows, -3.5 % at 4096), where
-  // no pair half lies past the last row (forward on 3 m tiles: +14 %, on 9:
-  // +4.5 %), and on single CTAs above (16384 rows on pairs: forward +3 %,
-  // dlogits +0.6 %). A launch with a single 128-row m tile stays on single
-  // CTAs, which keep every SM busy instead of leaving half of each pair idle.
+  // Engine per contraction. The forward and dlogits (K = H) run on pairs
+  // for an even number of m tiles up to 32 (T up to 4096; alone at H = 3584,
+  // V = 152064, forward: -8.5 % at 129 rows, -2 % at 2048, even at 4096;
+  // dlogits: -11 % at 512 rows, -3.5 % at 4096), where no pair half lies past
+  // the last row (forward on 3 m tiles: +14 %, on 9: +4.5 %), and on single
+  // CTAs above (16384 rows on pairs: forward +3 %, dlogits +0.6 %).
+  // grad_weight and grad_hidden take the engines below; at the 16384 x 3584 x
+  // 152064 step, which runs at the power cap, both are on wide pairs (kernels
+  // -6 % and -13 %, step -1.4 % and -1.8 %). A pair needs two m tiles: a
+  // launch with a single 128-row m tile runs on single CTAs, which keep every
+  // SM busy instead of leaving half of each pair idle.
   const int m_tiles = (p.M + kBM - 1) / kBM;
   const int env = gemm_pair_mode();
-  int mode = kSingle;
-  if (m_tiles >= 2) {
-    if (env == 1)
-      mode = kPairedMode<E>;
-    else if (env < 0 && (E == (int)Epi::StoreBf16 || E == (int)Epi::StoreF32T)) {
-      // A wide unit does twice a single CTA's work per SM in about 1.55x its
-      // time (grad_hidden alone: 1.257 against 0.79-0.82 ms when both fit in
-      // one wave), so wide pairs win only when they need enough fewer waves:
-      // at H = 3584 they lost below 2048 rows (1.26 against 0.8 ms) and at
-      // 3072-4096, and won at 2048 and from 8192 rows up, as this predicts.
-      const long long units_single =
-          static_cast<long long>(m_tiles) * ((p.N + kBN - 1) / kBN);
-      const long long units_wide =
-          static_cast<long long>((m_tiles + 1) / 2) * ((p.N + 2 * kBN - 1) / (2 * kBN));
-      const int slots = slots_for<E>(kWideMode, num_sms);
-      if (slots > 0 && num_sms > 0) {
-        const long long waves_single = (units_single + num_sms - 1) / num_sms;
-        const long long waves_wide = (units_wide + slots - 1) / slots;
-        if (waves_wide * 155 < waves_single * 100) mode = kWideMode;
+  Engine g{kSingle, kBN};
+  if (env == 1 && m_tiles >= 2) {
+    g.mode = kHasWide<E> ? kWideMode : kPairMode;
+  } else if (env < 0 && E == (int)Epi::StoreF32T) {
+    // grad_weight (K = the chunk's rows): 256-wide pairs, whose epilogue
+    // overlaps the next tile's MMAs, while K is short enough for the fp32
+    // output's stores to matter; wide pairs from 2048 rows. Alone at H =
+    // 3584, V = 152064 (ms, pairs / wide): 0.34 / 0.36 at 128 rows, 0.44 /
+    // 0.54 at 512, 0.69 / 0.79 at 1024, 1.29 / 1.28 at 2048, 2.62 / 2.50 at
+    // 4096, 5.47 / 5.01 at 8192.
+    if (m_tiles >= 2) g = p.K < 2048 ? Engine{kPairMode, kBN} : Engine{kWideMode, 2 * kBN};
+  } else if (env < 0 && kHasWide<E>) {
+    // grad_hidden and the bare engine GEMM: the cheapest engine by
+    // engine_cost (pairs only over two or more m tiles). Narrower tiles need
+    // an MN-major B (64-column boxes); each output element's K walk is the
+    // same on all of them.
+    const int wide_slots = m_tiles >= 2 ? slots_for<E>(kWideMode, num_sms) : 0;
+    const int pair_slots_n = m_tiles >= 2 ? slots_for<E>(kPairMode, num_sms) : 0;
+    const Engine cand[7] = {{kWideMode, 2 * kBN}, {kPairMode, kBN}, {kSingle, kBN},
+                            {kPairMode, 128},     {kSingle, 192},  {kSingle, 128},
+                            {kSingle, 64}};
+    const int n_cand = p.b_mn ? 7 : 3;
+    double best = 1e30;
+    for (int i = 0; i < n_cand; ++i) {
+      const int slots = cand[i].mode == kWideMode ? wide_slots : pair_slots_n;
+      const double cost =
+          engine_cost(cand[i], m_tiles, p.N, num_sms, slots, p.k_split > 0 ? 2 : 1);
+      if (cost < best * 0.999) {
+        best = cost;
+        g = cand[i];
       }
     }
-    else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles <= 32 &&
-             m_tiles % 2 == 0)
-      mode = kPairMode;
+  } else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles >= 2 &&
+             m_tiles <= 32 && m_tiles % 2 == 0) {
+    g.mode = kPairMode;
+  }
+  // LMH_GEMM_STORE_ENGINE forces the store contractions' engine and width
+  if constexpr (kHasWide<E>) {
+    int fm = -1, fn = 0;
+    gemm_store_engine(&fm, &fn);
+    if (fm == kSingle || (fm >= 0 && m_tiles >= 2)) {
+      g = Engine{fm, fn};
+      if (!p.b_mn && fm != kWideMode) g.tile_n = kBN;  // narrow tiles need an MN-major B
+    }
   }
   // no room for a cluster of two (a partitioned GPU, say): single CTAs, which
   // give the same bits
-  if (mode != kSingle && slots_for<E>(mode, num_sms) <= 0) mode = kSingle;
-  const int m_rows = mode != kSingle ? 2 * kBM : kBM;
-  const int tile_n = mode == kWideMode ? 2 * kBN : kBN;
-  if (E == (int)Epi::FwdStats && tile_n != kBN) return cudaErrorInvalidValue;  // chunk grid
+  if (g.mode != kSingle && slots_for<E>(g.mode, num_sms) <= 0) g = Engine{kSingle, kBN};
+  if (g.mode == kWideMode) g.tile_n = 2 * kBN;
+  if (E == (int)Epi::FwdStats && g.tile_n != kBN) return cudaErrorInvalidValue;  // chunk grid
+  const int kb_total = (p.K + kBK - 1) / kBK;
+  if (p.k_split != 0 && (!(E == (int)Epi::StoreF32 || E == (int)Epi::StoreBf16) || p.k_split < 0 ||
+                         p.k_split >= kb_total || p.seg_rows < (p.M + kBM - 1) / kBM * kBM))
+    return cudaErrorInvalidValue;  // a K split: two non-empty segments, partials apart
+  if (g.mode != kWideMode && g.tile_n != kBN &&
+      (!p.b_mn || g.tile_n % 64 != 0 || (g.mode == kPairMode && g.tile_n != 128)))
+    return cudaErrorInvalidValue;  // narrow tiles need 64-column MN-major B boxes
+  const int m_rows = g.mode != kSingle ? 2 * kBM : kBM;
+  p.tile_n = g.mode == kWideMode ? 0 : g.tile_n;
   p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
-  p.n_n_tiles = (p.N + tile_n - 1) / tile_n;
+  p.n_n_tiles = (p.N + g.tile_n - 1) / g.tile_n;
   p.tiles_per_unit = tiles_per_unit;
   const int all_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
   const int vu_end = (p.vunit_end > 0 && p.vunit_end < all_vunits) ? p.vunit_end : all_vunits;
@@ -818,7 +911,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   p.n_vunits = vu_end - p.vunit_begin;
   // Unit indices are int on the device; sizes whose unit count does not fit
   // are refused (they would need terabytes of workspace anyway).
-  const long long units = static_cast<long long>(p.n_m_tiles) * p.n_vunits;
+  const long long units =
+      static_cast<long long>(p.n_m_tiles) * p.n_vunits * (p.k_split > 0 ? 2 : 1);
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
   p.n_units = static_cast<int>(units);
   // Rows per raster group, per contraction (same-session sweep of 4/8/16/32
@@ -830,9 +924,9 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
                            E == (int)Epi::StoreF32T)
                               ? 32
                               : (E == (int)Epi::StoreBf16 ? 4 : 8);
-  p.group_m = mode != kSingle ? group_tiles / 2 : group_tiles;
+  p.group_m = g.mode != kSingle ? group_tiles / 2 : group_tiles;
   if (p.n_units <= 0) return cudaSuccess;
-  return launch_mode<E>(a, b, c, p, mode, num_sms, stream);
+  return launch_mode<E>(a, b, c, p, g.mode, num_sms, stream);
 }
 
 }  // namespace
@@ -859,6 +953,20 @@ cudaError_t launch_gemm(Epi e, const CUtensorMap& a, const CUtensorMap& b, GemmP
       return launch_gemm_e<(int)Epi::StoreF32T>(a, b, c_map, p, tiles_per_unit, num_sms, stream);
   }
   return cudaErrorInvalidValue;
+}
+
+void gemm_store_engine(int* mode, int* tile_n) {
+  static const Engine forced = [] {
+    const char* v = std::getenv("LMH_GEMM_STORE_ENGINE");
+    if (!v || !v[0]) return Engine{-1, 0};
+    if (v[0] == 'w' && v[1] == 0) return Engine{kWideMode, 2 * kBN};
+    const int n = std::atoi(v + 1);
+    if (v[0] == 'p' && (n == 128 || n == 256)) return Engine{kPairMode, n};
+    if (v[0] == 's' && (n == 64 || n == 128 || n == 192 || n == 256)) return Engine{kSingle, n};
+    return Engine{-1, 0};
+  }();
+  *mode = forced.mode;
+  *tile_n = forced.tile_n;
 }
 
 int gemm_pair_mode() {

@@ -31,8 +31,10 @@ inline int short_a_rows(int64_t M) {
   return M < kBM ? static_cast<int>(M < 8 ? 8 : (M + 7) / 8 * 8) : 0;
 }
 
-// Backward: rows are processed in fixed chunks of kBwdRowChunk.
+// Backward: rows are processed in fixed chunks of kBwdRowChunk (or of a
+// caller's multiple of kBM up to kBwdMaxRowChunk).
 constexpr int64_t kBwdRowChunk = 16384;
+constexpr int64_t kBwdMaxRowChunk = 1 << 20;
 
 // StoreF32T stores the transpose: D[m][n] goes to out[n][m].
 enum class Epi : int { FwdStats = 0, DLogits = 1, StoreBf16 = 2, StoreF32 = 3, StoreF32T = 4 };
@@ -53,6 +55,17 @@ struct GemmParams {
   // 128-row box that is almost all out-of-bounds fill; the rest of the A tile
   // is zero in shared memory, and the valid rows' products are unchanged.
   int a_rows;
+  // Columns of each tile on single CTAs and CTA pairs (set by launch_gemm):
+  // 256, or 64, 128 or 192 for an MN-major B (a pair: 128 or 256), so that a
+  // short launch spreads over more SMs. Each output element's K walk is the
+  // same for every width, so the width changes no bit.
+  int tile_n;
+  // Store contractions: a K split fixed by K alone. When k_split > 0, every
+  // output tile is two units, one per K segment ([0, k_split) and [k_split,
+  // end) in 64-wide K blocks); segment s writes its fp32 partial at output
+  // row offset s * seg_rows, and a separate kernel adds the two in order.
+  int k_split;
+  int seg_rows;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -92,6 +105,8 @@ enum KernelKind : int {
   K_SELFTEST,
   K_LOGITS_ROWWISE_DIV,
   K_HIDDEN_TRANSPOSE,
+  K_SUM_PARTS,
+  K_DHIDDEN_SUM,
   K_COUNT
 };
 
@@ -134,6 +149,13 @@ size_t gemm_smem_bytes();
 // grad_hidden give the same bits on every engine; grad_weight's summation
 // order follows the engine's waves.
 int gemm_pair_mode();
+// From LMH_GEMM_STORE_ENGINE, read once (a diagnostic, for tests and
+// measurements): the engine and tile width forced on the store contractions
+// (grad_hidden, grad_weight and the bare engine GEMM): "w" wide pairs,
+// "p256" / "p128" pairs, "s256" / "s192" / "s128" / "s64" single CTAs. Pairs
+// need two m tiles, and widths below 256 an MN-major B; *mode is -1 when
+// unset or not one of these (the cost model then decides).
+void gemm_store_engine(int* mode, int* tile_n);
 
 // a / b: operand maps with boxes of 64(K) x 128 rows (A, and B in kBBoxRows-row
 // boxes) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map
@@ -169,6 +191,11 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
                              const float* pzl, const int32_t* labels, int64_t T, int n_vunits,
                              int64_t V, float* out_logprob, float* out_entropy, float* out_lse,
                              float* out_sum_p2, cudaStream_t stream);
+
+// out[i] = sum_r parts[r * stride + i], r ascending (n_parts >= 1), for
+// i < count; bf16 (rounded once) when out_bf16, else fp32.
+cudaError_t launch_sum_parts(const float* parts, int n_parts, int64_t stride, int64_t count,
+                             void* out, bool out_bf16, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(unsigned* status, unsigned long long limit_ns, int* result,
                                  cudaStream_t stream);

@@ -176,10 +176,13 @@ __device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(
 __device__ __forceinline__ f32x2 bf16x2_f2(uint32_t w) { return f2_pack(bf16_lo_f(w), bf16_hi_f(w)); }
 
 struct ScaleMul {
+  static constexpr bool kNeedsMin = false;  // group_fast ignores the group's minimum
   float c;
   __device__ __forceinline__ float y(float x) const { return __fmul_rn(x, c); }
   // Every group takes the one-FMA path.
-  __device__ __forceinline__ bool group_fast(const uint4 (&)[4], int) const { return true; }
+  __device__ __forceinline__ bool group_fast(const uint4 (&)[4], int, float, float, float) const {
+    return true;
+  }
   // d[i] = the shifted pair y - m of the two bf16 of word i (words of w in
   // order, 4 per 16-byte vector).
   __device__ __forceinline__ void shift_fast(const uint4 (&w)[4], float neg_m,
@@ -216,6 +219,7 @@ static __device__ __noinline__ float div_ieee(float x, float t) { return __fdiv_
 // which runs this same packed routine). Other inputs (zero, tiny or huge |x|,
 // inf, extreme t) take the IEEE division.
 struct ScaleDiv {
+  static constexpr bool kNeedsMin = true;
   float t;
   float r;  // 1/t rounded to nearest, or 0 when t is outside [2^-20, 2^20]
   __device__ __forceinline__ static ScaleDiv make(float temperature) {
@@ -243,9 +247,19 @@ struct ScaleDiv {
     return div_ieee(x, t);
   }
   __device__ __forceinline__ float y(float x) const { return __fmul_rn(quotient(x), kLog2e); }
-  // True when every value of the first nv vectors is in the fast path's range.
-  __device__ __forceinline__ bool group_fast(const uint4 (&w)[4], int nv) const {
+  // True when the fast path gives every shifted value of the group's first nv
+  // vectors exactly: gmax and gmin are the group's largest and smallest raw
+  // values, mn the running maximum of y after the group. Huge values (|x| >
+  // 2^100, inf) need the IEEE division. Tiny ones (|x| < 2^-100, zero
+  // included) are outside the fast path's proven range, but once |mn| >=
+  // 2^-40 they cannot change a shifted value: |z log2(e)| < 2^-79 is below
+  // half an ulp of mn, so d = z log2(e) - m rounds to -m whatever the last
+  // bits of z. Only then is the group's smallest magnitude checked.
+  __device__ __forceinline__ bool group_fast(const uint4 (&w)[4], int nv, float gmax, float gmin,
+                                             float mn) const {
     if (r == 0.f) return false;
+    if (!(gmax <= 0x1p100f && gmin >= -0x1p100f)) return false;
+    if (fabsf(mn) >= 0x1p-40f) return true;
     __nv_bfloat162 amax = __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w[0].x));
     __nv_bfloat162 amin = amax;
 #pragma unroll
@@ -302,23 +316,29 @@ template <bool kQ, class S>
 __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&w)[4], int nv,
                                                   const S& sc) {
   __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&w[0].x);
+  __nv_bfloat162 n2 = m2;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (k < nv) {
       const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (k > 0 || q > 0) m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&ws[q]));
+        if (k > 0 || q > 0) {
+          const __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&ws[q]);
+          m2 = __hmax2(m2, v);
+          if (S::kNeedsMin) n2 = __hmin2(n2, v);
+        }
     }
   }
   const float gmax = fmaxf(__low2float(m2), __high2float(m2));
+  const float gmin = fminf(__low2float(n2), __high2float(n2));
   const float mn = fmaxf(st.m, sc.y(gmax));
   const float d0 = __fsub_rn(st.m, mn);
   const float a = ex2(d0);
   const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
   const float s = __fmul_rn(st.s, a);
   f32x2 d[16];
-  if (sc.group_fast(w, nv))
+  if (sc.group_fast(w, nv, gmax, gmin, mn))
     sc.shift_fast(w, -mn, d);
   else
     sc.shift_exact(w, nv, -mn, d);

@@ -372,6 +372,57 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// out[i] = ((parts[0][i] + parts[1][i]) + parts[2][i]) + ..., in that order,
+// rounded once at the end to bf16 (kBf16) or kept in fp32; part r starts at
+// parts + r * stride. It adds the two K segments' partials of grad_hidden, and
+// the ranks' grad_hidden partials of a vocab-parallel head, so that every
+// caller gets the same bits. Four elements per thread and step when the
+// buffers allow 16-byte loads.
+template <bool kBf16>
+__global__ void __launch_bounds__(256)
+    sum_parts_kernel(const float* __restrict__ parts, int n_parts, int64_t stride, int64_t count,
+                     void* __restrict__ out) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool vec = (count & 3) == 0 && (stride & 3) == 0 &&
+                   (reinterpret_cast<uintptr_t>(parts) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & (kBf16 ? 7 : 15)) == 0;
+  if (vec) {
+    const int64_t n4 = count >> 2;
+    for (int64_t i = tid; i < n4; i += step) {
+      float4 acc = reinterpret_cast<const float4*>(parts)[i];
+      for (int r = 1; r < n_parts; ++r) {
+        const float4 v = reinterpret_cast<const float4*>(parts + static_cast<int64_t>(r) * stride)[i];
+        acc.x = __fadd_rn(acc.x, v.x);
+        acc.y = __fadd_rn(acc.y, v.y);
+        acc.z = __fadd_rn(acc.z, v.z);
+        acc.w = __fadd_rn(acc.w, v.w);
+      }
+      if constexpr (kBf16) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        reinterpret_cast<uint2*>(out)[i] = w;
+      } else {
+        reinterpret_cast<float4*>(out)[i] = acc;
+      }
+    }
+  } else {
+    for (int64_t i = tid; i < count; i += step) {
+      float acc = parts[i];
+      for (int r = 1; r < n_parts; ++r) acc = __fadd_rn(acc, parts[static_cast<int64_t>(r) * stride + i]);
+      if constexpr (kBf16) {
+        const __nv_bfloat16 b = __float2bfloat16_rn(acc);
+        static_cast<uint16_t*>(out)[i] = *reinterpret_cast<const uint16_t*>(&b);
+      } else {
+        static_cast<float*>(out)[i] = acc;
+      }
+    }
+  }
+}
+
 // Every bf16 bit pattern x: the library's quotient x / t against IEEE fp32
 // division; counts the inputs whose result bits differ (NaN equals NaN).
 __global__ void division_selftest_kernel(float t, int* mismatches) {
@@ -467,6 +518,23 @@ cudaError_t launch_transpose_bf16(const uint16_t* in, int64_t rows, int64_t cols
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
   transpose_bf16_kernel<<<grid, 256, 0, stream>>>(in, rows, cols, in_ld, out, out_ld);
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
+cudaError_t launch_sum_parts(const float* parts, int n_parts, int64_t stride, int64_t count,
+                             void* out, bool out_bf16, int num_sms, cudaStream_t stream) {
+  if (count <= 0) return cudaSuccess;
+  const int64_t work = (count + 3) / 4;
+  int64_t blocks = (work + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+  if (blocks > cap) blocks = cap;
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (out_bf16)
+    sum_parts_kernel<true><<<g, 256, 0, stream>>>(parts, n_parts, stride, count, out);
+  else
+    sum_parts_kernel<false><<<g, 256, 0, stream>>>(parts, n_parts, stride, count, out);
   const cudaError_t e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;

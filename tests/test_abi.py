@@ -173,6 +173,38 @@ def test_noalloc_argument_errors_are_reported_without_a_launch(lib):
     assert lib.lmhead_kernel_launches() == before
 
 
+def test_chunked_shard_and_sum_argument_errors(lib):
+    # fake, never dereferenced addresses: each case fails validation first
+    before = lib.lmhead_kernel_launches()
+    big = (1 << 64) - 1
+    ws = lib.lmhead_workspace_size_bwd
+    for bad in (0, 100, 129, -128, (1 << 20) + 128):
+        assert ws(16384, 3584, 152064, bad) == big
+    # a smaller row chunk needs a smaller workspace; 16384 rows match the plain backward
+    assert ws(16384, 3584, 152064, 4096) < ws(16384, 3584, 152064, 16384)
+    assert ws(16384, 3584, 152064, 16384) == lib.lmhead_workspace_size(lmh.LMH_OP_BWD, 16384,
+                                                                      3584, 152064)
+    ch = lib.lmhead_logprob_bwd_chunked
+    args = [16, 16, 16, 16, None, 16, None, 4, 256, 4096, 1.0, 128, 16, 16, 256, 1 << 30, None]
+    assert ch(*args[:11], 100, *args[12:]) == lmh.LMH_ERR_INVALID_ARG
+    assert ch(*args[:11], 0, *args[12:]) == lmh.LMH_ERR_INVALID_ARG
+    assert b"row_chunk" in lib.lmhead_last_error_string()
+    assert ch(*args[:3], None, None, *args[5:]) == lmh.LMH_ERR_INVALID_ARG  # no upstream grad
+    assert ch(*args[:15], 16, None) == lmh.LMH_ERR_WORKSPACE
+    sh = lib.lmhead_logprob_bwd_shard
+    sargs = [16, 16, 16, 16, None, 16, None, 4, 256, 4096, 1024, 1.0, 16, 16, 256, 1 << 30, None]
+    assert sh(*sargs[:5], None, *sargs[6:]) == lmh.LMH_ERR_INVALID_ARG  # no whole-vocab lse
+    assert sh(*sargs[:4], 16, 16, None, *sargs[7:]) == lmh.LMH_ERR_INVALID_ARG  # gH w/o entropy
+    assert sh(*sargs[:10], -1, *sargs[11:]) == lmh.LMH_ERR_INVALID_ARG
+    assert sh(*sargs[:12], 24, *sargs[13:]) == lmh.LMH_ERR_ALIGNMENT  # grad_hidden_part
+    sr = lib.lmhead_sum_ranks_bf16
+    assert sr(16, 0, 10, 16, None) == lmh.LMH_ERR_INVALID_ARG
+    assert sr(16, 2, -1, 16, None) == lmh.LMH_ERR_INVALID_ARG
+    assert sr(None, 2, 10, 16, None) == lmh.LMH_ERR_INVALID_ARG
+    assert sr(None, 2, 0, None, None) == lmh.LMH_OK
+    assert lib.lmhead_kernel_launches() == before
+
+
 def test_binding_refuses_a_missing_library(tmp_path):
     with pytest.raises(RuntimeError):
         lmh.library(str(tmp_path / "nope.so"))

@@ -6,10 +6,14 @@ order on every engine. Child processes force each engine (the choice is read
 once per process) on ragged shapes, including pairs whose second half lies
 wholly past the last row, and every output is compared bit for bit.
 
+Store contractions also run on narrower tiles (64, 128 or 192 columns on
+single CTAs, 128 on pairs) when a short launch would leave SMs idle; every
+width is forced in turn and compared too.
+
 grad_weight walks K downwards on a CTA's odd waves, so its summation order
 follows the engine's wave structure. The shapes here fit each grad_weight
-launch in one wave, where that order is the same, so grad_weight and the
-bare engine GEMM are compared bit for bit as well."""
+launch in one wave on the single and paired engines, where that order is the
+same, so grad_weight and the bare engine GEMM are compared bit for bit there."""
 
 import os
 import subprocess
@@ -56,24 +60,49 @@ torch.save(out, sys.argv[1])
 '''
 
 
-def test_pair_and_single_engines_give_identical_bits(tmp_path):
+def _run(tmp_path, name, env_extra):
     import torch
 
     child = tmp_path / "child.py"
-    child.write_text(CHILD)
-    got = {}
-    for mode in ("0", "1"):
-        path = tmp_path / f"out{mode}.pt"
-        env = dict(os.environ, LMH_GEMM_CTA_PAIRS=mode)
-        r = subprocess.run([sys.executable, str(child), str(path), ROOT], env=env, cwd=ROOT,
-                           capture_output=True, text=True, timeout=900)
-        assert r.returncode == 0, r.stderr[-2000:]
-        got[mode] = torch.load(path)
-    single, pair = got["0"], got["1"]
+    if not child.exists():
+        child.write_text(CHILD)
+    path = tmp_path / f"out_{name}.pt"
+    env = dict(os.environ, **env_extra)
+    r = subprocess.run([sys.executable, str(child), str(path), ROOT], env=env, cwd=ROOT,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return torch.load(path)
+
+
+def _same(a, b):
+    import torch
+
+    return a.shape == b.shape and torch.equal(
+        a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+        b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+
+
+@pytest.fixture(scope="module")
+def single(tmp_path_factory):
+    return _run(tmp_path_factory.mktemp("single"), "single", {"LMH_GEMM_CTA_PAIRS": "0"})
+
+
+def test_pair_and_single_engines_give_identical_bits(tmp_path, single):
+    pair = _run(tmp_path, "pair", {"LMH_GEMM_CTA_PAIRS": "1"})
     assert single.keys() == pair.keys()
     for k in single:
-        a, b = single[k], pair[k]
-        assert a.shape == b.shape, k
-        same = torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
-                           b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
-        assert same, f"{k}: the single-CTA and CTA-pair engines differ"
+        assert _same(single[k], pair[k]), f"{k}: the single-CTA and CTA-pair engines differ"
+
+
+# Every engine and tile width the store contractions can take (forced with
+# LMH_GEMM_STORE_ENGINE): grad_hidden (gh, gh2) and the bare engine GEMM must
+# keep their bits, and so must the forward outputs. grad_weight is left out
+# here: narrow tiles spread it over several waves, whose K direction differs.
+@pytest.mark.parametrize("engine", ["s64", "s128", "s192", "p128", "p256", "w"])
+def test_every_store_engine_and_width_gives_identical_bits(tmp_path, single, engine):
+    forced = _run(tmp_path, engine, {"LMH_GEMM_STORE_ENGINE": engine})
+    assert single.keys() == forced.keys()
+    for k in single:
+        if k.endswith("_gw") or k.endswith("_gw2"):
+            continue
+        assert _same(single[k], forced[k]), f"{k}: engine {engine} differs from single CTAs"

@@ -385,6 +385,41 @@ def test_logits_division_bad_row_temperature_is_nan_in_that_row_only(lmh):
     assert max_abs(lp[~bad], rlp) < ATOL_LOGPROB
 
 
+@pytest.mark.parametrize("V", [5000, 4999])
+def test_logits_division_by_a_power_of_two_is_the_multiplied_form_bit_for_bit(lmh, V):
+    """For t = 2^k, z = x / t is exact and z * log2(e) is the same real number
+    as x * (log2(e) / t), so every shifted value, and every output, must carry
+    the bits of the multiplied form with s = 1/t. The rows mix in what the
+    division's fast path treats apart: exact zeros of both signs, bf16
+    subnormals, tiny normals (|x| < 2^-100), huge values (2^110), a row of
+    tiny values only (its maximum is tiny too) and a row of zeros."""
+    import torch
+
+    T = 8
+    rng = np.random.default_rng(V)
+    x = rng.normal(0.0, 2.0, size=(T, V)).astype(np.float32)
+    x[0, rng.choice(V, V // 3, replace=False)] = 0.0
+    x[0, rng.choice(V, V // 8, replace=False)] = -0.0
+    sub = rng.choice(V, V // 8, replace=False)
+    x[1, sub] = np.float32(2.0 ** -130) * rng.integers(1, 100, size=sub.size)  # bf16 subnormals
+    tiny = rng.choice(V, V // 4, replace=False)
+    x[1, tiny] = np.float32(2.0 ** -110) * rng.normal(size=tiny.size).astype(np.float32)
+    x[2] = np.float32(2.0 ** -105) * rng.normal(size=V).astype(np.float32)  # tiny maximum
+    x[3] = 0.0
+    x[4, rng.choice(V, 5, replace=False)] = np.float32(2.0 ** 110)
+    x[5, :3] = -np.float32(2.0 ** 110)
+    bits = W.f32_to_bf16_bits(x)
+    labels = W.random_labels(3, T, V)
+    xd, lab = to_dev_bf16(bits), to_dev(labels)
+    for t in (2.0, 0.5, 0.25, 1.0):
+        div = lmh.logprob_from_logits_div(xd, lab, t, want_lse=True, want_sum_p2=True)
+        mul = lmh.logprob_from_logits_stats(xd, lab, 1.0 / t, want_lse=True)
+        torch.cuda.synchronize()
+        for a, b, name in zip(div, mul, ("logprob", "entropy", "lse", "sum_p2")):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), \
+                f"{name} at t={t}: division and multiplication differ"
+
+
 def test_logits_division_against_torch_sampler_formula(lmh):
     """Against torch's own fp32 sampler formula on the GPU (log_softmax of the
     fp32 logits divided by a per-row temperature tensor, then gather): the
