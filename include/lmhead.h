@@ -41,6 +41,14 @@
  *    last error of the calling thread is lmhead_last_error_string().
  *  - The current device must be sm_103 (GB300); any other device returns
  *    LMH_ERR_UNSUPPORTED_DEVICE. There is no fallback path.
+ *  - Range: the statistics fold the temperature into the max shift (one FMA,
+ *    d = x * c - m with m the rounded maximum), so the maximum's own shifted
+ *    value is the rounding residual of its product, up to half an ulp of it.
+ *    Outputs stay finite for temperature-scaled logits |z| < 2^30 (the
+ *    residual is below 2^-3 for |z| < 2^20); beyond that they may be inf or
+ *    NaN. A logit of -inf (a masked vocabulary entry) contributes nothing to
+ *    logprob and lse; entropy then comes out NaN (p log p = 0 * -inf), as
+ *    it does in an fp32 entropy of such logits.
  *  - Every wait inside the kernels is bounded; a wait that runs out sets a
  *    device status bit that lmhead_device_status() reports.
  *  - The environment variable LMH_GEMM_CTA_PAIRS, read once per process,

@@ -918,12 +918,12 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // Rows per raster group, per contraction (same-session sweep of 4/8/16/32
   // 128-row m tiles on the Qwen-like step; 1, 2 and 4 again for grad_hidden):
   // the N = V contractions (forward, dlogits) share W tiles across more m
-  // tiles, the K = V grad_hidden prefers small groups. A pair's m unit is two
-  // m tiles.
+  // tiles, the K = V grad_hidden (bf16 out, or its K halves in fp32) prefers
+  // small groups. A pair's m unit is two m tiles.
   const int group_tiles = (E == (int)Epi::FwdStats || E == (int)Epi::DLogits ||
                            E == (int)Epi::StoreF32T)
                               ? 32
-                              : (E == (int)Epi::StoreBf16 ? 4 : 8);
+                              : ((E == (int)Epi::StoreBf16 || p.k_split > 0) ? 4 : 8);
   p.group_m = g.mode != kSingle ? group_tiles / 2 : group_tiles;
   if (p.n_units <= 0) return cudaSuccess;
   return launch_mode<E>(a, b, c, p, g.mode, num_sms, stream);

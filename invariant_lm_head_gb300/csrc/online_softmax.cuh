@@ -199,6 +199,13 @@ struct ScaleMul {
                                               f32x2 (&d)[16]) const {
     shift_fast(w, neg_m, d);
   }
+  // The shifted pair of one 32-bit word, on either path.
+  __device__ __forceinline__ f32x2 shift1_fast(uint32_t w, f32x2 nm2) const {
+    return f2_fma(bf16x2_f2(w), f2_pack(c, c), nm2);
+  }
+  __device__ __forceinline__ f32x2 shift1_exact(uint32_t w, f32x2 nm2) const {
+    return shift1_fast(w, nm2);
+  }
 };
 
 // IEEE fp32 division, kept out of line so the rare callers add no code to the
@@ -301,6 +308,17 @@ struct ScaleDiv {
       }
     }
   }
+  // The shifted pair of one 32-bit word, on either path (same operations as
+  // shift_fast / shift_exact).
+  __device__ __forceinline__ f32x2 shift1_fast(uint32_t w, f32x2 nm2) const {
+    return f2_fma(fast_quotient2(bf16x2_f2(w)), f2_pack(kLog2e, kLog2e), nm2);
+  }
+  __device__ __forceinline__ f32x2 shift1_exact(uint32_t w, f32x2 nm2) const {
+    float lo, hi;
+    f2_unpack(nm2, lo, hi);
+    return f2_pack(__fmaf_rn(quotient(bf16_lo_f(w)), kLog2e, lo),
+                   __fmaf_rn(quotient(bf16_hi_f(w)), kLog2e, hi));
+  }
 };
 
 // Fold 32 bf16 values, given as 4 x 16-byte words (8 values each, of which
@@ -337,23 +355,35 @@ __device__ __forceinline__ void stat_fold_bf16x32(OnlineStat& st, const uint4 (&
   const float a = ex2(d0);
   const float u = (st.s > 0.f) ? __fmul_rn(a, __fmaf_rn(st.s, d0, st.u)) : 0.f;
   const float s = __fmul_rn(st.s, a);
-  f32x2 d[16];
-  if (sc.group_fast(w, nv, gmax, gmin, mn))
-    sc.shift_fast(w, -mn, d);
-  else
-    sc.shift_exact(w, nv, -mn, d);
+  // Each word's shifted pair is formed inside the fold (fewer live
+  // registers than forming all 16 first); the fast and exact paths are two
+  // copies of the same loop.
+  const f32x2 nm2 = f2_pack(-mn, -mn);
   f32x2 s2 = f2_pack(0.f, 0.f), u2 = s2, q2 = s2;
+  auto fold_pair = [&](const f32x2 d) {
+    float da, db;
+    f2_unpack(d, da, db);
+    const f32x2 e2 = f2_pack(ex2(da), ex2(db));
+    s2 = f2_add(s2, e2);
+    u2 = f2_fma(e2, d, u2);
+    if (kQ) q2 = f2_fma(e2, e2, q2);
+  };
+  if (sc.group_fast(w, nv, gmax, gmin, mn)) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    if (k < nv) {
+    for (int k = 0; k < 4; ++k) {
+      if (k < nv) {
+        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float da, db;
-        f2_unpack(d[4 * k + q], da, db);
-        const f32x2 e2 = f2_pack(ex2(da), ex2(db));
-        s2 = f2_add(s2, e2);
-        u2 = f2_fma(e2, d[4 * k + q], u2);
-        if (kQ) q2 = f2_fma(e2, e2, q2);
+        for (int q = 0; q < 4; ++q) fold_pair(sc.shift1_fast(ws[q], nm2));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < nv) {
+        const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) fold_pair(sc.shift1_exact(ws[q], nm2));
       }
     }
   }

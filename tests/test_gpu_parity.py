@@ -163,7 +163,7 @@ def test_fused_backward_matches_oracle(lmh, T, H, V, s, pass_lse):
     assert rel_frob(gw, rgw) < RTOL_FROB_GRAD
     # per-row check of grad_hidden (each row is its own reduction)
     for t in range(T):
-        assert rel_frob(gh[t], rgh[t]) < 3 * RTOL_FROB_GRAD
+        assert rel_frob(gh[t], rgh[t]) < RTOL_FROB_GRAD
 
 
 def test_fused_backward_several_row_chunks(lmh):
@@ -392,10 +392,13 @@ def test_logits_division_by_a_power_of_two_is_the_multiplied_form_bit_for_bit(lm
     the bits of the multiplied form with s = 1/t. The rows mix in what the
     division's fast path treats apart: exact zeros of both signs, bf16
     subnormals, tiny normals (|x| < 2^-100), huge values (2^110), a row of
-    tiny values only (its maximum is tiny too) and a row of zeros."""
+    tiny values only (its maximum is tiny too), a row of zeros, rows with -inf
+    entries (a masked sampler's logits), a row of huge negative values only,
+    and a row holding +inf. NaN outputs (entropy where a -inf logit makes
+    p * log p = 0 * -inf, every output of the +inf row) must be NaN in both."""
     import torch
 
-    T = 8
+    T = 11
     rng = np.random.default_rng(V)
     x = rng.normal(0.0, 2.0, size=(T, V)).astype(np.float32)
     x[0, rng.choice(V, V // 3, replace=False)] = 0.0
@@ -408,6 +411,10 @@ def test_logits_division_by_a_power_of_two_is_the_multiplied_form_bit_for_bit(lm
     x[3] = 0.0
     x[4, rng.choice(V, 5, replace=False)] = np.float32(2.0 ** 110)
     x[5, :3] = -np.float32(2.0 ** 110)
+    x[6, rng.choice(V, V // 3, replace=False)] = -np.inf
+    x[7] = -np.float32(2.0 ** 101) * (1.0 + rng.random(V).astype(np.float32))  # all huge negative
+    x[8, 7] = np.inf
+    x[9, :40] = -np.inf
     bits = W.f32_to_bf16_bits(x)
     labels = W.random_labels(3, T, V)
     xd, lab = to_dev_bf16(bits), to_dev(labels)
@@ -416,8 +423,12 @@ def test_logits_division_by_a_power_of_two_is_the_multiplied_form_bit_for_bit(lm
         mul = lmh.logprob_from_logits_stats(xd, lab, 1.0 / t, want_lse=True)
         torch.cuda.synchronize()
         for a, b, name in zip(div, mul, ("logprob", "entropy", "lse", "sum_p2")):
-            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), \
-                f"{name} at t={t}: division and multiplication differ"
+            same = (a.view(torch.int32) == b.view(torch.int32)) | (torch.isnan(a) & torch.isnan(b))
+            assert bool(same.all()), f"{name} at t={t}: division and multiplication differ"
+        # -inf logits (a masked sampler's) leave logprob finite. The huge rows
+        # (|z| >= 2^100) are outside the range the statistics hold finite
+        # (|z| < 2^30, include/lmhead.h); only their bits are compared above.
+        assert torch.isfinite(div[0][[0, 1, 2, 3, 6, 9, 10]]).all()
 
 
 def test_logits_division_against_torch_sampler_formula(lmh):
