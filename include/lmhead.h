@@ -56,7 +56,7 @@
  *    "1" CTA pairs (two SMs per MMA) wherever a launch has more than 128
  *    rows, unset the default (pairs for grad_weight and grad_hidden when
  *    they need enough fewer waves than single CTAs, and for the forward and
- *    dlogits over 2 to 32 row tiles of 128 in even number).
+ *    dlogits over an even number of 128-row tiles, or an odd number above 32).
  *    log-prob, entropy, lse, sum_p2 and grad_hidden are bit-identical
  *    whichever engine runs. grad_weight is deterministic for a given engine
  *    and SM count; its summation order follows the engine's waves.

@@ -511,6 +511,9 @@ def lmhead_logprob_merge(part_m, part_s, part_u, label_logit, labels, V: int, *,
 
 
 _LOGPROB_FN = None
+# Row chunk of the autograd backward (lmhead_logprob_bwd_chunked): at H = 3584,
+# V = 152064 its workspace is 1.4 GB instead of 5.6 GB for 16384 rows.
+AUTOGRAD_ROW_CHUNK = 4096
 
 
 def _logprob_function():
@@ -538,14 +541,18 @@ def _logprob_function():
                 return None, None, None, None
             s = ctx.inv_temperature
             g = None if grad_logprob is None else grad_logprob.float().contiguous()
-            if grad_entropy is None:
-                gh, gw = lmhead_logprob_bwd(hidden, weight, labels, g, s, lse=lse)
-            else:
-                gh, gw = lmhead_logprob_entropy_bwd(hidden, weight, labels, g,
-                                                    grad_entropy.float().contiguous(), s,
-                                                    lse=lse, entropy=ent)
-            return (gh if ctx.needs_input_grad[0] else None,
-                    gw.to(weight.dtype) if ctx.needs_input_grad[1] else None, None, None)
+            ge = None if grad_entropy is None else grad_entropy.float().contiguous()
+            # rows in chunks of AUTOGRAD_ROW_CHUNK: a quarter of the default
+            # backward's workspace, at no measurable cost in time
+            gh, gw = lmhead_logprob_bwd_chunked(hidden, weight, labels, g, s,
+                                                row_chunk=AUTOGRAD_ROW_CHUNK, grad_entropy=ge,
+                                                lse=lse, entropy=ent if ge is not None else None)
+            gw_out = None
+            if ctx.needs_input_grad[1]:
+                # the fp32 sum rounded once to the weight's bf16 by the library
+                gw_out = lmhead_sum_ranks_bf16(gw.view(1, *gw.shape))
+            del gw
+            return (gh if ctx.needs_input_grad[0] else None, gw_out, None, None)
 
     _LOGPROB_FN = _LMHeadLogprob
     return _LOGPROB_FN
@@ -558,8 +565,9 @@ def lmhead_logprob(hidden, weight, labels, inv_temperature: float = 1.0):
     lmhead_logprob_entropy_bwd when the entropy output also receives a
     gradient. hidden bf16 [T, H] and weight bf16 [V, H] get bf16 gradients
     (grad_weight is accumulated in fp32 by the library and rounded once to
-    the weight's dtype; call lmhead_logprob_bwd directly to keep it in fp32).
-    labels int32 [T] get none.
+    bf16 by it; call lmhead_logprob_bwd directly to keep it in fp32). The
+    backward runs in row chunks of AUTOGRAD_ROW_CHUNK. labels int32 [T] get
+    none.
     """
     return _logprob_function().apply(hidden, weight, labels, float(inv_temperature))
 

@@ -831,11 +831,15 @@ template <int E>
 cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
   // Engine per contraction. The forward and dlogits (K = H) run on pairs
-  // for an even number of m tiles up to 32 (T up to 4096; alone at H = 3584,
-  // V = 152064, forward: -8.5 % at 129 rows, -2 % at 2048, even at 4096;
-  // dlogits: -11 % at 512 rows, -3.5 % at 4096), where no pair half lies past
-  // the last row (forward on 3 m tiles: +14 %, on 9: +4.5 %), and on single
-  // CTAs above (16384 rows on pairs: forward +3 %, dlogits +0.6 %).
+  // for an even number of m tiles (alone at H = 3584, V = 152064, forward:
+  // -8.5 % at 129 rows, -2 % at 2048, even at 4096; dlogits: -11 % at 512
+  // rows, -3.5 % at 4096), and for an odd number above 32, where the pair
+  // half past the last row costs little (forward on 3 m tiles: +14 %, on 9:
+  // +4.5 %). At 16384 rows pairs were slower alone (forward +3 %, dlogits
+  // +0.6 %) but faster inside the step, which runs at the power cap: three
+  // same-session alternating runs, 40.02-40.21 against 40.35-40.59 ms per
+  // step (dlogits 10.38-10.44 against 10.87-10.91 ms), at a slightly higher
+  // clock: a pair loads half the B operand per flop into each SM.
   // grad_weight and grad_hidden take the engines below; at the 16384 x 3584 x
   // 152064 step, which runs at the power cap, both are on wide pairs (kernels
   // -6 % and -13 %, step -1.4 % and -1.8 %). A pair needs two m tiles: a
@@ -876,7 +880,7 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
       }
     }
   } else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles >= 2 &&
-             m_tiles <= 32 && m_tiles % 2 == 0) {
+             (m_tiles % 2 == 0 || m_tiles > 32)) {
     g.mode = kPairMode;
   }
   // LMH_GEMM_STORE_ENGINE forces the store contractions' engine and width

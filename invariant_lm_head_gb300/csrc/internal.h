@@ -144,10 +144,10 @@ size_t gemm_smem_bytes();
 // Which contractions run on CTA pairs (launches with two or more 128-row m
 // tiles only), from LMH_GEMM_CTA_PAIRS, read once: "0" none (0), "1" all (1;
 // the store epilogues as wide pairs), unset the per-contraction default (-1:
-// grad_hidden and grad_weight on wide pairs when they need enough fewer waves;
-// the forward and dlogits over an even number of m tiles up to 32 on pairs). The forward, dlogits and
-// grad_hidden give the same bits on every engine; grad_weight's summation
-// order follows the engine's waves.
+// grad_hidden and grad_weight by their measured engine choice; the forward
+// and dlogits on pairs over an even number of m tiles or an odd number above
+// 32). The forward, dlogits and grad_hidden give the same bits on every
+// engine; grad_weight's summation order follows the engine's waves.
 int gemm_pair_mode();
 // From LMH_GEMM_STORE_ENGINE, read once (a diagnostic, for tests and
 // measurements): the engine and tile width forced on the store contractions

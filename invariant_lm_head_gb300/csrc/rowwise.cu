@@ -4,7 +4,11 @@
 //     scalar or per-row temperature; online max / sum-exp / entropy
 //     accumulator, optionally sum p^2; label gather),
 //   * the fixed-order merge of the fused forward's per-vocab-chunk partials,
-//   * a self-test of the bounded wait (a barrier that nothing completes).
+//   * the transpose of a row chunk of hidden (grad_weight's K-major operand),
+//   * ordered sums of fp32 partials (grad_hidden's two K halves; a
+//     vocab-parallel head's per-rank shares),
+//   * self-tests of the bounded wait (a barrier that nothing completes) and
+//     of the division.
 //
 // The sampler formula is the one of the verl pull request "batch-invariant
 // actor forward and sampler log-prob formula" (fp32 log_softmax over the full
@@ -279,36 +283,67 @@ __global__ void __launch_bounds__(kRowThreads)
   }
 }
 
-// One thread per row: fold the per-chunk partials in ascending chunk order.
+// The fixed merge order of a row's per-chunk partials: the n chunks form
+// kMergeGroups consecutive groups of ceil(n / kMergeGroups) chunks (the last
+// ones shorter or empty); each group is folded in ascending chunk order, then
+// the group results in ascending group order. It depends on n (that is, on V)
+// alone, and it shortens a row's chain of dependent merges from n to about
+// n / 8 + 8.
+constexpr int kMergeGroups = 8;
+
+// kMergeGroups threads per row (consecutive lanes), one per group; the
+// group's first lane then folds the groups' results in order.
 template <bool kQ>
-__global__ void fwd_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
-                                 const float* __restrict__ pu, const float* __restrict__ pq,
-                                 const float* __restrict__ pzl, const int32_t* __restrict__ labels,
-                                 int64_t T, int n_vunits, int64_t V, float* __restrict__ out_lp,
-                                 float* __restrict__ out_ent, float* __restrict__ out_lse,
-                                 float* __restrict__ out_sum_p2) {
-  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= T) return;
+__global__ void __launch_bounds__(256)
+    fwd_merge_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                     const float* __restrict__ pu, const float* __restrict__ pq,
+                     const float* __restrict__ pzl, const int32_t* __restrict__ labels, int64_t T,
+                     int n_vunits, int64_t V, float* __restrict__ out_lp,
+                     float* __restrict__ out_ent, float* __restrict__ out_lse,
+                     float* __restrict__ out_sum_p2) {
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = gid / kMergeGroups;
+  const int grp = static_cast<int>(gid % kMergeGroups);
+  const bool live = row < T;  // whole rows per warp: 32 / kMergeGroups rows
+  const int per = (n_vunits + kMergeGroups - 1) / kMergeGroups;
+  const int c_begin = grp * per;
+  const int c_end = min(n_vunits, c_begin + per);
   OnlineStat st = stat_empty();
-  // Loads of kBatch chunks are issued before their merges, so a thread keeps
-  // several loads in flight; the merge order stays ascending.
-  constexpr int kBatch = 8;
-  for (int c0 = 0; c0 < n_vunits; c0 += kBatch) {
-    OnlineStat b[kBatch];
+  if (live) {
+    // Loads of kBatch chunks are issued before their merges, so a thread
+    // keeps several loads in flight; the merge order stays ascending.
+    constexpr int kBatch = 8;
+    for (int c0 = c_begin; c0 < c_end; c0 += kBatch) {
+      OnlineStat b[kBatch];
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      if (c0 + j < n_vunits) {
-        const int64_t o = (int64_t)(c0 + j) * T + row;
-        b[j] = OnlineStat{pm[o], ps[o], pu[o], kQ ? pq[o] : 0.f};
+      for (int j = 0; j < kBatch; ++j) {
+        if (c0 + j < c_end) {
+          const int64_t o = (int64_t)(c0 + j) * T + row;
+          b[j] = OnlineStat{pm[o], ps[o], pu[o], kQ ? pq[o] : 0.f};
+        }
       }
-    }
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j)
-      if (c0 + j < n_vunits) stat_merge<kQ>(st, b[j]);
+      for (int j = 0; j < kBatch; ++j)
+        if (c0 + j < c_end) stat_merge<kQ>(st, b[j]);
+    }
   }
+  // the row's groups, in ascending order, into the first lane of the row
+  const unsigned lane = threadIdx.x & 31u;
+  const unsigned first = lane - lane % kMergeGroups;
+  OnlineStat r = st;
+#pragma unroll
+  for (int g = 1; g < kMergeGroups; ++g) {
+    OnlineStat o;
+    o.m = __shfl_sync(0xffffffffu, st.m, first + g);
+    o.s = __shfl_sync(0xffffffffu, st.s, first + g);
+    o.u = __shfl_sync(0xffffffffu, st.u, first + g);
+    o.q = kQ ? __shfl_sync(0xffffffffu, st.q, first + g) : 0.f;
+    if (grp == 0) stat_merge<kQ>(r, o);
+  }
+  if (!live || grp != 0) return;
   const int lab = labels[row];
   const bool ok = lab >= 0 && (int64_t)lab < V;
-  write_row_outputs(row, st, ok ? pzl[row] : 0.f, ok, out_lp, out_ent, out_lse,
+  write_row_outputs(row, r, ok ? pzl[row] : 0.f, ok, out_lp, out_ent, out_lse,
                     kQ ? out_sum_p2 : nullptr);
 }
 
@@ -493,8 +528,8 @@ cudaError_t launch_fwd_merge(const float* pm, const float* ps, const float* pu, 
                              int64_t V, float* out_lp, float* out_ent, float* out_lse,
                              float* out_sum_p2, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  const int threads = 64;  // T = 16384 gives 256 blocks: every SM gets rows
-  const int64_t blocks = (T + threads - 1) / threads;
+  const int threads = 64;  // 8 rows per block: a 128-row batch still spreads over 16 SMs
+  const int64_t blocks = (T * kMergeGroups + threads - 1) / threads;
   if (pq && out_sum_p2)
     fwd_merge_kernel<true><<<(unsigned)blocks, threads, 0, stream>>>(
         pm, ps, pu, pq, pzl, labels, T, n_vunits, V, out_lp, out_ent, out_lse, out_sum_p2);

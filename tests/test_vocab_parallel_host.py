@@ -57,6 +57,37 @@ def _worker(rank, world, port, out):
         dist.destroy_process_group()
 
 
+def _three_rank_worker(rank, world, port, out):
+    import torch
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        V_total, T = 5000, 4  # 5 chunks over 3 ranks: 2, 2, 1
+        b0, b1 = vp.shard_bounds(V_total, world, rank)
+        counts = vp.exchange_layout(b0, b1 - b0, V_total)
+        n = -(-(b1 - b0) // vp.CHUNK)
+        planes = torch.full((3, n, T), float(rank))
+        whole = vp.gather_chunks(planes, counts)
+        out[rank] = (counts, whole[0, :, 0].tolist(), vp.gather_ranks(torch.tensor([rank])).tolist())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_exchange_on_three_gloo_ranks():
+    world = 3
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_three_rank_worker, args=(world, _free_port(), out), nprocs=world,
+                       start_method="spawn")
+    for r in range(world):
+        counts, chunk_owner, ranks = out[r]
+        assert counts == [2, 2, 1]
+        assert chunk_owner == [0.0, 0.0, 1.0, 1.0, 2.0]  # rank order along the vocabulary
+        assert ranks == [[0], [1], [2]]
+
+
 def test_exchange_on_two_gloo_ranks():
     world = 2
     mgr = mp.get_context("spawn").Manager()
