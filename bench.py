@@ -897,7 +897,8 @@ def run_gpu(args):
             "frac": round(T3 * V3 * 2 / (sq_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
         extras["logits_path"]["division_form"] = {
             "tokens_per_s": T3 / (d_ms * 1e-3), "ms": d_ms, "kernel_ms": dk_ms,
-            "achieved_gbs": round(dgbs, 1), "frac": round(dgbs / peaks["hbm_gbs"], 4)}
+            "achieved_gbs": round(dgbs, 1), "frac": round(dgbs / peaks["hbm_gbs"], 4),
+            "traffic": traffic_for("logits_rowwise_div")}
         extras["sampler_parity"] = sampler_parity(lmh, x[:4096], l3[:4096])
         if rank == 0 and not args.no_cpu_baseline:
             extras["logits_path"]["cpu_oracle"] = cpu_oracle_logits()

@@ -67,6 +67,16 @@
  *    process) forces the engine of grad_hidden and grad_weight: "w" wide
  *    pairs, "p256" / "p128" pairs, "s256" / "s192" / "s128" / "s64" single
  *    CTAs; it overrides LMH_GEMM_CTA_PAIRS for them.
+ *  - A contraction of several waves of output tiles (four or more; for
+ *    grad_weight, a row chunk of 8192 rows or more as well) hands its tiles
+ *    to the SMs in ascending order from a counter kept in the workspace
+ *    (zeroed in stream order before each launch), so tiles that share
+ *    operands run together; shorter ones, and calls without a workspace,
+ *    walk a fixed stride. No output bit depends on it. Two
+ *    diagnostics, read once per process: LMH_GEMM_SCHEDULE ("static" or
+ *    "dynamic") forces either order wherever a workspace is given, and
+ *    LMH_GEMM_GRID_CAP=n runs every contraction on at most n CTAs (or CTA
+ *    pairs).
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
@@ -98,7 +108,8 @@ struct CUstream_st; /* cudaStream_t */
 /*
  * Bytes of workspace that `op` needs for these sizes (0 for LMH_OP_LOGITS).
  * Returns SIZE_MAX for invalid arguments. The forward needs 16 bytes per row
- * per 1024 vocabulary columns (+4 per row); the backward adds 12 bytes per
+ * per 1024 vocabulary columns (+4 per row, and a 4-byte tile counter); the
+ * backward adds 12 bytes per
  * row, a bf16 dlogits buffer of min(T, 16384) x V, a bf16 transpose of one
  * 16384-row chunk of hidden (H x min(T, 16384)) and the fp32 partials of one
  * chunk's grad_hidden, one per half of the vocabulary (2 x min(T, 16384) x H,

@@ -170,6 +170,7 @@ int n_fwd_chunks(int64_t V) {
 
 struct FwdWs {
   float *pm, *ps, *pu, *pq, *pzl;
+  unsigned* sched;  // the GEMMs' unit counter (dynamic schedule)
 };
 
 FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
@@ -180,6 +181,7 @@ FwdWs carve_fwd(Carver& c, int64_t T, int64_t V) {
   w.pu = c.take<float>(n);
   w.pq = c.take<float>(n);
   w.pzl = c.take<float>(T);
+  w.sched = c.take<unsigned>(1);
   return w;
 }
 
@@ -315,6 +317,7 @@ int run_forward(const DeviceInfo& dev, const uint16_t* hidden, const uint16_t* w
   p.part_q = out_sum_p2 ? w.pq : nullptr;
   p.part_zl = w.pzl;
   p.part_ld = T;
+  p.sched = w.sched;
   if (!slices) {
     LMH_LAUNCH(lmh::K_FWD_GEMM, st,
                lmh::launch_gemm(lmh::Epi::FwdStats, ta, tb, p, lmh::kFwdTilesPerChunk, dev.sms, st),
@@ -542,6 +545,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
 
     lmh::GemmParams p{};
     p.status = dev->status;
+    p.sched = w.fwd.sched;
     p.M = static_cast<int>(rows);
     p.N = static_cast<int>(V);
     p.K = static_cast<int>(H);
@@ -571,6 +575,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     // gives a short batch two independent MMA chains on two SMs per tile.
     lmh::GemmParams q{};
     q.status = dev->status;
+    q.sched = w.fwd.sched;
     q.M = static_cast<int>(rows);
     q.N = static_cast<int>(H);
     q.K = static_cast<int>(V);
@@ -603,6 +608,7 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
 
     lmh::GemmParams r{};
     r.status = dev->status;
+    r.sched = w.fwd.sched;
     // grad_weight^T [H][V] = hidden^T * dl, stored transposed into grad_weight [V][H]
     r.M = static_cast<int>(H);
     r.N = static_cast<int>(V);

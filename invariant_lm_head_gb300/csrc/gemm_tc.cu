@@ -17,6 +17,18 @@
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
 //
+// Schedule: the output is cut into units (a row tile, or a pair's two, by one
+// or more column tiles), rastered in groups of row units so that concurrent
+// units share operand tiles in L2. A short launch walks them with a fixed
+// stride per CTA. A launch of several waves claims them from a counter in the
+// workspace in ascending order: one thread per CTA (per pair) claims and
+// passes each unit index to the CTA's other roles, and to the peer CTA,
+// through a 16-slot ring of shared-memory words and mbarriers. The claimed
+// order keeps concurrent units within about a wave of each other, which a
+// fixed stride does not (CTA pairs drifted apart by several units over a
+// 125-wave launch and lost the shared W tiles in L2), and it balances the
+// tail. Which CTA runs a unit changes none of its arithmetic.
+//
 // CTA pairs: a cluster of two CTAs owns a 256x256 tile. Each CTA stages its
 // own 128 A rows and one 128-row half of B (6 stages of 32 KB); CTA 0 issues
 // tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives its 128
@@ -64,6 +76,7 @@
 #include <cfloat>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 
 #include <cuda_bf16.h>
 
@@ -79,7 +92,14 @@ constexpr int kABytes = kBM * kBK * 2;           // one 128-row x 64-K A box
 constexpr int kBHalfBytes = kBBoxRows * kBK * 2;  // one 128-row x 64-K B box
 constexpr int kMnBoxBytes = 64 * kBK * 2;         // one 64(MN) x 64(K) bf16 box
 constexpr int kTmemCols = 512;
-constexpr int kBarrierBytes = 256;
+constexpr int kBarrierBytes = 512;
+// Slots of the ring through which a dynamic schedule's claimed unit indices
+// reach the CTA's other roles (and the peer CTA of a pair). Unit j + 1 is
+// published when the producer starts unit j, after it has issued every stage
+// of the units before; a role can trail it by at most the operand ring's
+// stages plus the two accumulators (every unit has at least one stage), about
+// 11 units, so 16 slots never lap.
+constexpr int kUnitSlots = 16;
 // Two staging buffers for the TMA-store epilogues: 128 rows x 128 bytes
 // (32 fp32 or, using half of it, 32 bf16 columns).
 constexpr int kStagingBytes = kBM * 128;
@@ -106,9 +126,11 @@ struct Ring {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
-  // full and empty per stage, two accumulator pairs, final; then the TMEM
-  // address, the abort flag, two epilogue go flags and the peer's load count
-  static_assert(8 * (2 * kMaxStages + 5) + 20 <= kBarrierBytes, "barrier area too small");
+  // full and empty per stage, two accumulator pairs, final, the unit ring's
+  // slots; then the TMEM address, the abort flag, two epilogue go flags, the
+  // peer's load count, two epilogue unit words and the unit ring
+  static_assert(8 * (2 * kMaxStages + 5 + kUnitSlots) + 4 * (7 + kUnitSlots) <= kBarrierBytes,
+                "barrier area too small");
 };
 constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
 
@@ -116,6 +138,12 @@ constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue thread
 // groups of group_m m units, unit-major inside a group, so concurrently
 // running CTAs share B tiles in L2. An m unit is one 128-row m tile, or two
 // for a CTA pair. The order changes no value.
+// Dynamic schedule: the next unit of the launch, -1 once all are claimed.
+__device__ __forceinline__ int claim_unit(const GemmParams& p) {
+  const unsigned v = atomicAdd(p.sched, 1u);
+  return v < static_cast<unsigned>(p.n_units) ? static_cast<int>(v) : -1;
+}
+
 __device__ __forceinline__ void unit_coords(const GemmParams& p, int u, int& m_tile, int& n_first,
                                             int& n_count, int& vunit, int& seg) {
   // with a K split, the second K segment's units follow all of the first's
@@ -201,19 +229,25 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   constexpr uint32_t kRingBytes = R::kStages * R::kStageBytes;
   const uint32_t staging = smem_base + kRingBytes;  // 2 x kStagingBytes
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRingBytes + 2 * kStagingBytes);
-  // barrier layout: full[kS], empty[kS], tfull[2], tempty[2], final
+  // barrier layout: full[kS], empty[kS], tfull[2], tempty[2], final, ufull[kUnitSlots]
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kS + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kS + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kS + 2 + a); };
   const uint32_t final_bar = bar0 + 8u * (2 * kS + 4);
+  // the unit ring: slot j % kUnitSlots holds the j-th unit of this CTA's walk
+  auto ufull_bar = [&](int j) {
+    return bar0 + 8u * static_cast<uint32_t>(2 * kS + 5 + (j & (kUnitSlots - 1)));
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) +
-                                                    8 * (2 * kS + 5));
+                                                    8 * (2 * kS + 5 + kUnitSlots));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_go = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
   // pair: the number of stage loads CTA 1 issued, published to CTA 0 at the end
   volatile uint32_t* peer_issued = tmem_slot + 4;
+  volatile int* epi_unit = reinterpret_cast<volatile int*>(tmem_slot + 5);  // [2]
+  volatile int* uring = reinterpret_cast<volatile int*>(tmem_slot + 7);     // [kUnitSlots]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -222,6 +256,25 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   const int first_unit = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int unit_stride = kPair ? static_cast<int>(cluster_nid_x()) : static_cast<int>(gridDim.x);
   auto cta_m_tile = [&](int m_unit) { return kPair ? 2 * m_unit + static_cast<int>(rank) : m_unit; };
+
+  // The j-th unit of this CTA's walk (-1 past the end). Static: a fixed
+  // stride over the units. Dynamic: one thread (CTA 0's producer in a pair)
+  // claims units from the launch's counter in ascending order and publishes
+  // each in slot j of the unit ring (and of the peer's ring), where every
+  // other role reads it; -1 ends the walk. Either way a unit's arithmetic is
+  // the same, so the schedule changes no bit.
+  const bool dyn = p.dynamic != 0;
+  auto static_unit = [&](int j) {
+    const long long u = first_unit + static_cast<long long>(j) * unit_stride;
+    return u < p.n_units ? static_cast<int>(u) : -1;
+  };
+  auto ring_unit = [&](int j, int& u) -> bool {  // bounded wait for slot j
+    if (!mbar_wait<kPair>(ufull_bar(j), static_cast<uint32_t>(j / kUnitSlots) & 1u, abort_flag,
+                          p.status))
+      return false;
+    u = uring[j & (kUnitSlots - 1)];
+    return true;
+  };
 
   // Output columns of a tile, and the B rows (of 64 K elements) this CTA
   // stages per stage: a wide pair's two 128-row halves, a pair's half of its
@@ -261,6 +314,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       mbar_init(tempty_bar(a), kPair ? 256 : 128);
     }
     mbar_init(final_bar, 1);
+    for (int j = 0; j < kUnitSlots; ++j) mbar_init(ufull_bar(j), 1);
     *abort_flag = 0;
     *peer_issued = 0;
     fence_barrier_init();
@@ -296,17 +350,54 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       // ------------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      int wave = 0;
-      for (int u = first_unit; ok && u < p.n_units; u += unit_stride, ++wave) {
+      const bool claims = dyn && (!kPair || rank == 0);
+      // Slot j of the ring (and of the peer's) gets unit u.
+      auto publish = [&](int j, int u) {
+        const int s = j & (kUnitSlots - 1);
+        uring[s] = u;
+        mbar_arrive(ufull_bar(j));  // release: the slot's store before the phase
+        if constexpr (kPair) {
+          st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(uring + s)), 1),
+                                static_cast<uint32_t>(u));
+          mbar_arrive_remote_release(mapa_shared(ufull_bar(j), 1));
+        }
+      };
+      // Each unit is published when the one before it starts, so the peer
+      // CTA's producer knows it a whole unit before its first load (publishing
+      // it at its own start cost short units, e.g. grad_weight at K = 512, a
+      // fifth of their time), and claimed one unit earlier still, so the
+      // atomic's latency hides behind the loads.
+      int cur = -1, nxt = -1;
+      if (claims) {
+        cur = claim_unit(p);
+        publish(0, cur);
+        nxt = cur >= 0 ? claim_unit(p) : -1;
+      }
+      for (int uj = 0; ok; ++uj) {
+        int u;
+        if (!dyn) {
+          u = static_unit(uj);
+        } else if (claims) {
+          u = cur;
+          if (u >= 0) {
+            publish(uj + 1, nxt);
+            cur = nxt;
+            nxt = cur >= 0 ? claim_unit(p) : -1;
+          }
+        } else if (!ring_unit(uj, u)) {
+          ok = false;
+          break;
+        }
+        if (u < 0) break;
         int m_unit, n_first, n_count, vunit, seg;
         unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
         const int m_tile = cta_m_tile(m_unit);
         const int kb0 = seg ? p.k_split : 0;
         const int kb_n = (p.k_split > 0 ? (seg ? kb_total : p.k_split) : kb_total) - kb0;
-        // grad_weight walks K (the rows) downwards on odd waves, so a wave
-        // starts on the operand rows the previous wave touched last, while
-        // they are still in L2.
-        const bool k_down = (E == (int)Epi::StoreF32T) && (wave & 1);
+        // grad_weight walks K (the rows) downwards on odd waves (a wave: one
+        // unit per CTA or pair of the grid), so a wave starts on the operand
+        // rows the previous wave touched last, while they are still in L2.
+        const bool k_down = (E == (int)Epi::StoreF32T) && ((u / unit_stride) & 1);
         for (int j = 0; ok && j < n_count; ++j) {
           const int n_tile = n_first + j;
           // first B row this CTA stages in each 256-column block: the whole
@@ -411,7 +502,15 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                                             p.a_mn != 0, p.b_mn != 0);
       uint32_t stage = 0, phase = 0, it = 0;
       bool ok = true;
-      for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
+      for (int uj = 0; ok; ++uj) {
+        int u;
+        if (!dyn) {
+          u = static_unit(uj);
+        } else if (!ring_unit(uj, u)) {
+          ok = false;
+          break;
+        }
+        if (u < 0) break;
         int m_unit, n_first, n_count, vunit, seg;
         unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
         const int kb_n =
@@ -497,7 +596,24 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     const int etid = threadIdx.x - 64;
     uint32_t it = 0, chunk_ctr = 0;
     bool ok = true;
-    for (int u = first_unit; ok && u < p.n_units; u += unit_stride) {
+    for (int uj = 0; ok; ++uj) {
+      int u;
+      if (!dyn) {
+        u = static_unit(uj);
+      } else {
+        // epilogue thread 0 reads the slot (bounded) and shares it: -2 = gave up
+        if (etid == 0) {
+          int v = -1;
+          epi_unit[uj & 1] = ring_unit(uj, v) ? v : -2;
+        }
+        named_barrier(kEpiBarrier, 128);
+        u = epi_unit[uj & 1];
+        if (u == -2) {
+          ok = false;
+          break;
+        }
+      }
+      if (u < 0) break;
       int m_unit, n_first, n_count, vunit, seg;
       unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
       const int m_tile = cta_m_tile(m_unit);
@@ -548,6 +664,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         for (int c = 0; c < tile_n / 32; ++c) {
           const int col0 = n_tile * tile_n + c * 32;
           if (col0 >= p.N) break;  // uniform over the CTA
+          // A store epilogue stages nothing for a tile wholly past the last
+          // row (a pair's second half): every staged chunk is then a
+          // committed store, which the staging buffers' reuse wait counts on.
+          // (Staging such a tile without storing it let its chunks overwrite
+          // a buffer that the last live store was still reading.)
+          if (E != (int)Epi::FwdStats && !tile_live) break;
           const int nvalid = min(32, p.N - col0);
           float v[32];
           tmem_ld32(taddr + c * 32, v);
@@ -620,7 +742,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
               stage_row_bf16(buf, row_in_tile, v);
             fence_proxy_async_smem();
             named_barrier(kEpiBarrier, 128);
-            if (etid == 0 && tile_live) {
+            if (etid == 0) {
               // (x, y) of the box in the output: transposed for StoreF32T
               const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
               const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM + seg * p.seg_rows;
@@ -745,25 +867,25 @@ int pair_slots(int num_sms) {
   return n;
 }
 
+// `lanes`: the most CTAs (single) or CTA pairs of the persistent grid.
 template <int E, int kMode>
 cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                       const GemmParams& p, int num_sms, cudaStream_t stream) {
+                       const GemmParams& p, int lanes, cudaStream_t stream) {
   cudaError_t e;
   if constexpr (kMode != kSingle) {
     // Set on every launch: the attribute belongs to the current device's context.
     e = cudaFuncSetAttribute(gemm_tc_pair_kernel<E, kMode>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Ring<kMode>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int slots = pair_slots<E, kMode>(num_sms);
-    if (slots <= 0) return cudaErrorInvalidConfiguration;  // launch_gemm checked it first
-    const int clusters = p.n_units < slots ? p.n_units : slots;  // persistent
+    if (lanes <= 0) return cudaErrorInvalidConfiguration;  // launch_gemm checked it first
+    const int clusters = p.n_units < lanes ? p.n_units : lanes;  // persistent
     gemm_tc_pair_kernel<E, kMode>
         <<<2 * clusters, kGemmThreads, Ring<kMode>::kSmemBytes, stream>>>(a, b, c, p);
   } else {
     e = cudaFuncSetAttribute(gemm_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Ring<kSingle>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = p.n_units < num_sms ? p.n_units : num_sms;  // persistent: <= one CTA per SM
+    const int grid = p.n_units < lanes ? p.n_units : lanes;  // persistent: <= one CTA per SM
     gemm_tc_kernel<E><<<grid, kGemmThreads, Ring<kSingle>::kSmemBytes, stream>>>(a, b, c, p);
   }
   e = cudaGetLastError();
@@ -788,11 +910,11 @@ int slots_for(int mode, int num_sms) {
 
 template <int E>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                        const GemmParams& p, int mode, int num_sms, cudaStream_t stream) {
-  if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, num_sms, stream);
+                        const GemmParams& p, int mode, int lanes, cudaStream_t stream) {
+  if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, lanes, stream);
   if constexpr (kHasWide<E>)
-    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, num_sms, stream);
-  return launch_one<E, kSingle>(a, b, c, p, num_sms, stream);
+    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, lanes, stream);
+  return launch_one<E, kSingle>(a, b, c, p, lanes, stream);
 }
 
 // An engine and tile width for one launch.
@@ -930,7 +1052,33 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
                               : ((E == (int)Epi::StoreBf16 || p.k_split > 0) ? 4 : 8);
   p.group_m = g.mode != kSingle ? group_tiles / 2 : group_tiles;
   if (p.n_units <= 0) return cudaSuccess;
-  return launch_mode<E>(a, b, c, p, g.mode, num_sms, stream);
+  // Schedule. A static stride lets CTA pairs drift apart: at 16384 x 3584 x
+  // 152064 the pairs sharing a W tile started 13-35 us apart in the first
+  // quarter of the forward and 140-300 us (2-4 units) apart in the last,
+  // where single CTAs stayed within 15 us; the forward read W about 12 times
+  // instead of once per raster group, and the slowest pair set the end. A
+  // launch of several waves therefore claims units from a counter in
+  // ascending order, which keeps concurrent units together and balances the
+  // tail.
+  // grad_weight keeps the fixed stride while K (the chunk's rows) is short:
+  // its units are then a few microseconds of MMAs behind a long fp32 store,
+  // and claimed units measured slower (alone at H = 3584, V = 152064, ms,
+  // fixed / claimed: 0.446 / 0.540 at 512 rows, 0.689 / 0.774 at 1024, 1.279 /
+  // 1.290 at 2048; 9.60-9.65 / 9.19-9.26 at 16384).
+  int sched_mode = -1, grid_cap = 0;
+  gemm_schedule(&sched_mode, &grid_cap);
+  int lanes = g.mode == kSingle ? num_sms : slots_for<E>(g.mode, num_sms);
+  if (grid_cap > 0 && grid_cap < lanes) lanes = grid_cap;
+  const bool claim_by_default =
+      p.n_units >= static_cast<long long>(kDynamicMinWaves) * lanes &&
+      !(E == (int)Epi::StoreF32T && p.K < kDynamicMinGradWeightK);
+  p.dynamic =
+      (p.sched != nullptr && (sched_mode == 1 || (sched_mode < 0 && claim_by_default))) ? 1 : 0;
+  if (p.dynamic) {
+    const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_mode<E>(a, b, c, p, g.mode, lanes, stream);
 }
 
 }  // namespace
@@ -971,6 +1119,22 @@ void gemm_store_engine(int* mode, int* tile_n) {
   }();
   *mode = forced.mode;
   *tile_n = forced.tile_n;
+}
+
+void gemm_schedule(int* schedule, int* grid_cap) {
+  static const int forced = [] {
+    const char* v = std::getenv("LMH_GEMM_SCHEDULE");
+    if (v && std::strcmp(v, "static") == 0) return 0;
+    if (v && std::strcmp(v, "dynamic") == 0) return 1;
+    return -1;
+  }();
+  static const int cap = [] {
+    const char* v = std::getenv("LMH_GEMM_GRID_CAP");
+    const int n = v ? std::atoi(v) : 0;
+    return n > 0 ? n : 0;
+  }();
+  *schedule = forced;
+  *grid_cap = cap;
 }
 
 int gemm_pair_mode() {

@@ -66,6 +66,12 @@ struct GemmParams {
   // row offset s * seg_rows, and a separate kernel adds the two in order.
   int k_split;
   int seg_rows;
+  // Dynamic schedule: a 32-bit unit counter in the caller's workspace (NULL =
+  // none). launch_gemm zeroes it and sets `dynamic` for launches of several
+  // waves; the CTAs (or CTA pairs) then claim units in ascending order instead
+  // of walking a fixed stride. A unit's arithmetic is the same either way.
+  unsigned* sched;
+  int dynamic;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -156,6 +162,16 @@ int gemm_pair_mode();
 // need two m tiles, and widths below 256 an MN-major B; *mode is -1 when
 // unset or not one of these (the cost model then decides).
 void gemm_store_engine(int* mode, int* tile_n);
+// From LMH_GEMM_SCHEDULE and LMH_GEMM_GRID_CAP, read once (diagnostics, for
+// tests and measurements): *schedule is 0 for "static" (every launch walks a
+// fixed stride), 1 for "dynamic" (every launch with a unit counter claims
+// units), -1 unset (dynamic from kDynamicMinWaves waves); *grid_cap is the
+// most CTAs (single) or CTA pairs a launch uses, 0 when unset (all SMs).
+void gemm_schedule(int* schedule, int* grid_cap);
+// A launch of at least this many waves of units claims them dynamically
+// (grad_weight only from this many rows of K).
+constexpr int kDynamicMinWaves = 4;
+constexpr int kDynamicMinGradWeightK = 8192;
 
 // a / b: operand maps with boxes of 64(K) x 128 rows (A, and B in kBBoxRows-row
 // boxes) when K-major, 64(MN) x 64(K) when MN-major. c is the output tensor map

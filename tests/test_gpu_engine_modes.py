@@ -13,7 +13,13 @@ width is forced in turn and compared too.
 grad_weight walks K downwards on a CTA's odd waves, so its summation order
 follows the engine's wave structure. The shapes here fit each grad_weight
 launch in one wave on the single and paired engines, where that order is the
-same, so grad_weight and the bare engine GEMM are compared bit for bit there."""
+same, so grad_weight and the bare engine GEMM are compared bit for bit there.
+
+The schedule (a fixed stride over the units, or units claimed from a counter
+in ascending order) must not change a bit either, grad_weight included: its K
+direction follows the unit's wave index, not the CTA that runs it. A grid cap
+of a few CTAs (or pairs) makes each walk dozens of units long, so the dynamic
+schedule's 16-slot unit ring wraps several times."""
 
 import os
 import subprocess
@@ -106,3 +112,65 @@ def test_every_store_engine_and_width_gives_identical_bits(tmp_path, single, eng
         if k.endswith("_gw") or k.endswith("_gw2"):
             continue
         assert _same(single[k], forced[k]), f"{k}: engine {engine} differs from single CTAs"
+
+
+@pytest.mark.parametrize("pairs,cap", [("0", "2"), ("1", "3")])
+def test_dynamic_schedule_gives_identical_bits(tmp_path, single, pairs, cap):
+    env = {"LMH_GEMM_CTA_PAIRS": pairs, "LMH_GEMM_GRID_CAP": cap}
+    fixed = _run(tmp_path, f"static_{pairs}", dict(env, LMH_GEMM_SCHEDULE="static"))
+    claimed = _run(tmp_path, f"dynamic_{pairs}", dict(env, LMH_GEMM_SCHEDULE="dynamic"))
+    assert fixed.keys() == claimed.keys() == single.keys()
+    for k in fixed:
+        assert _same(fixed[k], claimed[k]), f"{k}: the dynamic schedule changed bits"
+        if not (k.endswith("_gw") or k.endswith("_gw2")):
+            assert _same(single[k], claimed[k]), f"{k}: capped grid differs from single CTAs"
+
+
+# A ragged batch on CTA pairs: with 7 row tiles the last pair's second half
+# lies wholly past the last row and stores nothing. On a one-pair grid every
+# such half follows a live tile of the same CTA, whose last TMA store may
+# still be reading its staging buffer; the backward is repeated and must keep
+# its bits (and match single CTAs) every time.
+CHILD_REPEAT = r'''
+import sys
+import torch
+sys.path.insert(0, sys.argv[2])
+import workloads as W
+import invariant_lm_head_gb300 as lmh
+
+lmh.build()
+dev = torch.device("cuda:0")
+T, H, V, s = 777, 520, 3001, 1 / 0.7
+hidden = W.as_torch_bf16(W.random_bf16(T, (T, H), 1.0)).to(dev)
+weight = W.as_torch_bf16(W.random_bf16(T + 1, (V, H), 0.05)).to(dev)
+labels = torch.from_numpy(W.random_labels(T, T, V)).to(dev)
+grad = torch.from_numpy(W.random_f32(T, T)).to(dev)
+_, _, lse = lmh.lmhead_logprob_fwd(hidden, weight, labels, s, want_lse=True)
+out = {}
+for rep in range(int(sys.argv[3])):
+    gh, gw = lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse)
+    out[f"gh{rep}"] = gh.cpu()
+    out[f"gw{rep}"] = gw.cpu()
+torch.cuda.synchronize()
+assert lmh.lmhead_device_status() == 0
+torch.save(out, sys.argv[1])
+'''
+
+
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+def test_pair_halves_past_the_last_row_keep_live_stores_intact(tmp_path, single, schedule):
+    import torch
+
+    reps = 12
+    child = tmp_path / "repeat.py"
+    child.write_text(CHILD_REPEAT)
+    path = tmp_path / "rep.pt"
+    env = dict(os.environ, LMH_GEMM_CTA_PAIRS="1", LMH_GEMM_GRID_CAP="1",
+               LMH_GEMM_SCHEDULE=schedule)
+    r = subprocess.run([sys.executable, str(child), str(path), ROOT, str(reps)], env=env,
+                       cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    out = torch.load(path)
+    for rep in range(reps):
+        assert _same(out[f"gh{rep}"], single["777_gh"]), f"grad_hidden differs on repeat {rep}"
+        assert _same(out[f"gw{rep}"], out["gw0"]), f"grad_weight differs on repeat {rep}"
