@@ -76,7 +76,8 @@
  *    diagnostics, read once per process: LMH_GEMM_SCHEDULE ("static" or
  *    "dynamic") forces either order wherever a workspace is given, and
  *    LMH_GEMM_GRID_CAP=n runs every contraction on at most n CTAs (or CTA
- *    pairs).
+ *    pairs). LMH_GEMM_INTERLEAVE=0 (a diagnostic) stops the forward and
+ *    dlogits from overlapping consecutive tiles' K loops; bits are the same.
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H

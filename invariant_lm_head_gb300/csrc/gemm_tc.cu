@@ -16,6 +16,11 @@
 //   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
 //               and reads it 32 columns at a time with tcgen05.ld
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
+// In the forward and dlogits (K = H) consecutive tiles also overlap in K: a
+// tile's last K blocks alternate with the next tile's first ones in the
+// operand ring, so two independent accumulator chains feed the tensor pipe,
+// and each tile keeps a few blocks to itself while the epilogue drains the
+// other accumulator.
 //
 // Schedule: the output is cut into units (a row tile, or a pair's two, by one
 // or more column tiles), rastered in groups of row units so that concurrent
@@ -276,6 +281,72 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     return true;
   };
 
+  // The order in which the operand ring carries K blocks, which the producers
+  // and the MMA issuer follow alike. Tiles come in the walk's order (a unit's
+  // tiles, then the next unit's); tile t's blocks are issued in its own K
+  // order. With p.interleave = X > 0 (same K everywhere, two accumulators),
+  // tile t runs its blocks [lead, K - X) alone and then its last X blocks
+  // one-to-one with the next tile's first X: the two accumulators' MMA chains
+  // then overlap, while during a tile's solo blocks the epilogue drains the
+  // other accumulator. X = 0 runs the tiles one after another. The order of
+  // each tile's own MMAs, and so every bit, is the same either way.
+  const int kb_total = (p.K + kBK - 1) / kBK;
+  struct WalkTile {
+    int u, idx, m_unit, n_first, n_count, j, vunit, seg, kb0, kb_n;
+    bool k_down;
+  };
+  auto walk = [&](auto&& next_unit, auto&& on_stage) -> bool {
+    int uj = 0;
+    auto enter_unit = [&](WalkTile& t, int idx) -> bool {
+      int u = -1;
+      if (!next_unit(uj, u)) return false;
+      ++uj;
+      t.u = u;
+      t.idx = idx;
+      if (u < 0) return true;
+      unit_coords(p, u, t.m_unit, t.n_first, t.n_count, t.vunit, t.seg);
+      t.j = 0;
+      t.kb0 = t.seg ? p.k_split : 0;
+      t.kb_n = (p.k_split > 0 ? (t.seg ? kb_total : p.k_split) : kb_total) - t.kb0;
+      // grad_weight walks K (the rows) downwards on odd waves (a wave: one
+      // unit per CTA or pair of the grid), so a wave starts on the operand
+      // rows the previous wave touched last, while they are still in L2.
+      t.k_down = (E == (int)Epi::StoreF32T) && ((u / unit_stride) & 1);
+      return true;
+    };
+    auto next_tile = [&](const WalkTile& t, WalkTile& n) -> bool {
+      if (t.j + 1 < t.n_count) {
+        n = t;
+        ++n.j;
+        ++n.idx;
+        return true;
+      }
+      return enter_unit(n, t.idx + 1);
+    };
+    WalkTile a{}, b{};
+    if (!enter_unit(a, 0)) return false;
+    int lead = 0;  // blocks of tile a already issued beside its predecessor
+    const int X = p.interleave;
+    while (a.u >= 0) {
+      for (int i = lead; i < a.kb_n - X; ++i)
+        if (!on_stage(a, i)) return false;
+      if (!next_tile(a, b)) return false;
+      if (X > 0 && b.u >= 0) {
+        for (int i = 0; i < X; ++i) {
+          if (!on_stage(a, a.kb_n - X + i)) return false;
+          if (!on_stage(b, i)) return false;
+        }
+        lead = X;
+      } else {
+        for (int i = a.kb_n - X; i < a.kb_n; ++i)
+          if (!on_stage(a, i)) return false;
+        lead = 0;
+      }
+      a = b;
+    }
+    return true;
+  };
+
   // Output columns of a tile, and the B rows (of 64 K elements) this CTA
   // stages per stage: a wide pair's two 128-row halves, a pair's half of its
   // tile, or a single CTA's whole tile. A stage's bytes follow from them, and
@@ -342,7 +413,6 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int kb_total = (p.K + kBK - 1) / kBK;
   long long issued = 0;  // stage loads issued by this CTA's producer
 
   if (warp == 0) {
@@ -373,104 +443,90 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         publish(0, cur);
         nxt = cur >= 0 ? claim_unit(p) : -1;
       }
-      for (int uj = 0; ok; ++uj) {
-        int u;
+      auto next_unit = [&](int uj, int& u) -> bool {
         if (!dyn) {
           u = static_unit(uj);
-        } else if (claims) {
-          u = cur;
-          if (u >= 0) {
-            publish(uj + 1, nxt);
-            cur = nxt;
-            nxt = cur >= 0 ? claim_unit(p) : -1;
-          }
-        } else if (!ring_unit(uj, u)) {
-          ok = false;
-          break;
+          return true;
         }
-        if (u < 0) break;
-        int m_unit, n_first, n_count, vunit, seg;
-        unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
-        const int m_tile = cta_m_tile(m_unit);
-        const int kb0 = seg ? p.k_split : 0;
-        const int kb_n = (p.k_split > 0 ? (seg ? kb_total : p.k_split) : kb_total) - kb0;
-        // grad_weight walks K (the rows) downwards on odd waves (a wave: one
-        // unit per CTA or pair of the grid), so a wave starts on the operand
-        // rows the previous wave touched last, while they are still in L2.
-        const bool k_down = (E == (int)Epi::StoreF32T) && ((u / unit_stride) & 1);
-        for (int j = 0; ok && j < n_count; ++j) {
-          const int n_tile = n_first + j;
-          // first B row this CTA stages in each 256-column block: the whole
-          // block alone, its half in a pair
-          const int b_row0 = n_tile * tile_n +
-                             (kPair ? static_cast<int>(rank) * (b_rows / R::kNBlocks) : 0);
-          for (int kstep = 0; kstep < kb_n; ++kstep) {
-            const int kb = kb0 + (k_down ? kb_n - 1 - kstep : kstep);
-            if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            const uint32_t sA = smem_base + stage * stage_stride;
-            const uint32_t sB = sA + kABytes;
-            // One arrive per stage, by CTA 0, expecting both CTAs' bytes; both
-            // CTAs' boxes complete on CTA 0's barrier, issued in the pair form
-            // (measured: CTA 0 issuing the plain form made the pair 10 % slower).
-            if (rank == 0)
-              mbar_arrive_expect_tx(full_bar(stage),
-                                    (kPair ? 2u : 1u) * stage_tx - (kBM - a_rows) * 128);
-            const uint32_t fbar = kPair ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
-            auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
-              if constexpr (kPair)
-                tma_load_2d_pair(dst, map, fbar, x, y);
-              else
-                tma_load_2d(dst, map, fbar, x, y);
-            };
-            auto load_a = [&]() {
-              if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
+        if (!claims) return ring_unit(uj, u);
+        u = cur;
+        if (u >= 0) {
+          publish(uj + 1, nxt);
+          cur = nxt;
+          nxt = cur >= 0 ? claim_unit(p) : -1;
+        }
+        return true;
+      };
+      auto load_stage = [&](const WalkTile& t, int i) -> bool {
+        const int m_tile = cta_m_tile(t.m_unit);
+        const int n_tile = t.n_first + t.j;
+        const int kb = t.kb0 + (t.k_down ? t.kb_n - 1 - i : i);
+        // first B row this CTA stages in each 256-column block: the whole
+        // block alone, its half in a pair
+        const int b_row0 =
+            n_tile * tile_n + (kPair ? static_cast<int>(rank) * (b_rows / R::kNBlocks) : 0);
+        if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status)) return false;
+        const uint32_t sA = smem_base + stage * stage_stride;
+        const uint32_t sB = sA + kABytes;
+        // One arrive per stage, by CTA 0, expecting both CTAs' bytes; both
+        // CTAs' boxes complete on CTA 0's barrier, issued in the pair form
+        // (measured: CTA 0 issuing the plain form made the pair 10 % slower).
+        if (rank == 0)
+          mbar_arrive_expect_tx(full_bar(stage),
+                                (kPair ? 2u : 1u) * stage_tx - (kBM - a_rows) * 128);
+        const uint32_t fbar = kPair ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+        auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y) {
+          if constexpr (kPair)
+            tma_load_2d_pair(dst, map, fbar, x, y);
+          else
+            tma_load_2d(dst, map, fbar, x, y);
+        };
+        auto load_a = [&]() {
+          if (p.a_mn) {  // [K][M]: two 64(M) x 64(K) boxes
 #pragma unroll
-                for (int i = 0; i < kBM / 64; ++i)
-                  load(sA + i * kMnBoxBytes, &tmA, m_tile * kBM + 64 * i, kb * kBK);
-              } else {
-                load(sA, &tmA, kb * kBK, m_tile * kBM);
-              }
-            };
-            auto load_b = [&]() {
-              constexpr int kBlockBytes = R::kBBytes / R::kNBlocks;
-              // B rows of one N block this CTA stages (a multiple of 64, and
-              // of 128 when B is K-major)
-              const int block_rows = b_rows / R::kNBlocks;
+            for (int q = 0; q < kBM / 64; ++q)
+              load(sA + q * kMnBoxBytes, &tmA, m_tile * kBM + 64 * q, kb * kBK);
+          } else {
+            load(sA, &tmA, kb * kBK, m_tile * kBM);
+          }
+        };
+        auto load_b = [&]() {
+          constexpr int kBlockBytes = R::kBBytes / R::kNBlocks;
+          // B rows of one N block this CTA stages (a multiple of 64, and
+          // of 128 when B is K-major)
+          const int block_rows = b_rows / R::kNBlocks;
 #pragma unroll
-              for (int nb = 0; nb < R::kNBlocks; ++nb) {
-                const uint32_t dst = sB + nb * kBlockBytes;
-                const int row = b_row0 + nb * kBN;
-                if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
-                  for (int i = 0; i < block_rows / 64; ++i)
-                    load(dst + i * kMnBoxBytes, &tmB, row + 64 * i, kb * kBK);
-                } else {  // [N][K]: 128-row boxes
-                  for (int i = 0; i < block_rows / kBBoxRows; ++i)
-                    load(dst + i * kBHalfBytes, &tmB, kb * kBK, row + kBBoxRows * i);
-                }
-              }
-            };
-            // The forward and dlogits stream W as B: B first, so the DRAM
-            // loads start before A's (small, L2-resident, or for short batches
-            // mostly out-of-bounds zero fill). The other contractions stream
-            // A and measured faster with A first.
-            if (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
-              load_b();
-              load_a();
-            } else {
-              load_a();
-              load_b();
-            }
-            ++issued;
-            if (++stage == n_st) {
-              stage = 0;
-              phase ^= 1u;
+          for (int nb = 0; nb < R::kNBlocks; ++nb) {
+            const uint32_t dst = sB + nb * kBlockBytes;
+            const int row = b_row0 + nb * kBN;
+            if (p.b_mn) {  // [K][N]: 64(N) x 64(K) boxes
+              for (int q = 0; q < block_rows / 64; ++q)
+                load(dst + q * kMnBoxBytes, &tmB, row + 64 * q, kb * kBK);
+            } else {  // [N][K]: 128-row boxes
+              for (int q = 0; q < block_rows / kBBoxRows; ++q)
+                load(dst + q * kBHalfBytes, &tmB, kb * kBK, row + kBBoxRows * q);
             }
           }
+        };
+        // The forward and dlogits stream W as B: B first, so the DRAM
+        // loads start before A's (small, L2-resident, or for short batches
+        // mostly out-of-bounds zero fill). The other contractions stream
+        // A and measured faster with A first.
+        if (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) {
+          load_b();
+          load_a();
+        } else {
+          load_a();
+          load_b();
         }
-      }
+        ++issued;
+        if (++stage == n_st) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
+      ok = walk(next_unit, load_stage);
       if (kPair && rank != 0) {
         // CTA 0 drains this CTA's copies at the end; it needs their count
         st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<uint32_t*>(peer_issued)), 0),
@@ -500,78 +556,69 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBM : kBM,
                                             static_cast<uint32_t>(kMode == kWideMode ? kBN : tile_n),
                                             p.a_mn != 0, p.b_mn != 0);
-      uint32_t stage = 0, phase = 0, it = 0;
-      bool ok = true;
-      for (int uj = 0; ok; ++uj) {
-        int u;
+      uint32_t stage = 0, phase = 0;
+      auto next_unit = [&](int uj, int& u) -> bool {
         if (!dyn) {
           u = static_unit(uj);
-        } else if (!ring_unit(uj, u)) {
-          ok = false;
-          break;
+          return true;
         }
-        if (u < 0) break;
-        int m_unit, n_first, n_count, vunit, seg;
-        unit_coords(p, u, m_unit, n_first, n_count, vunit, seg);
-        const int kb_n =
-            p.k_split > 0 ? (seg ? kb_total - p.k_split : p.k_split) : kb_total;
-        for (int j = 0; ok && j < n_count; ++j, ++it) {
-          const uint32_t acc = it % R::kAccs;
-          const uint32_t aph = (it / R::kAccs) & 1u;
-          if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
+        return ring_unit(uj, u);
+      };
+      // One K block of tile t: its accumulator is t.idx % kAccs; the first
+      // block waits until the epilogue has released that accumulator, and
+      // the last hands it to the epilogue.
+      auto mma_stage = [&](const WalkTile& t, int i) -> bool {
+        const uint32_t acc = static_cast<uint32_t>(t.idx) % R::kAccs;
+        if (i == 0) {
+          const uint32_t aph = (static_cast<uint32_t>(t.idx) / R::kAccs) & 1u;
+          if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) return false;
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * kBN;
-          for (int kb = 0; kb < kb_n; ++kb) {
-            if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t sA = smem_base + stage * stage_stride;
-            const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
-            const uint64_t bdesc =
-                p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
-            // One K=16 step: +32 bytes inside a K-major 128-byte row, or +16
-            // rows of 128 bytes (two 8-row atoms) in an MN-major tile; in the
-            // descriptor's 16-byte address units that is +2 or +128.
-            const uint64_t astep = p.a_mn ? 128ull : 2ull;
-            const uint64_t bstep = p.b_mn ? 128ull : 2ull;
-            // a wide pair's second N block: its B half is the next kBlockBytes
-            // of the stage (>> 4 in descriptor units), its columns the next 256
-            constexpr uint64_t kBlockStep = (R::kBBytes / R::kNBlocks) >> 4;
+        }
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t sA = smem_base + stage * stage_stride;
+        const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
+        const uint64_t bdesc =
+            p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
+        // One K=16 step: +32 bytes inside a K-major 128-byte row, or +16
+        // rows of 128 bytes (two 8-row atoms) in an MN-major tile; in the
+        // descriptor's 16-byte address units that is +2 or +128.
+        const uint64_t astep = p.a_mn ? 128ull : 2ull;
+        const uint64_t bstep = p.b_mn ? 128ull : 2ull;
+        // a wide pair's second N block: its B half is the next kBlockBytes
+        // of the stage (>> 4 in descriptor units), its columns the next 256
+        constexpr uint64_t kBlockStep = (R::kBBytes / R::kNBlocks) >> 4;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint32_t accumulate = (kb > 0 || k > 0) ? 1u : 0u;
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint32_t accumulate = (i > 0 || k > 0) ? 1u : 0u;
 #pragma unroll
-              for (int nb = 0; nb < R::kNBlocks; ++nb) {
-                const uint64_t bd = bdesc + kBlockStep * nb + bstep * k;
-                if constexpr (kPair)
-                  tc_mma_bf16_pair(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
-                else
-                  tc_mma_bf16(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
-              }
-            }
-            // the stage is free in both CTAs once these MMAs have read it
+          for (int nb = 0; nb < R::kNBlocks; ++nb) {
+            const uint64_t bd = bdesc + kBlockStep * nb + bstep * k;
             if constexpr (kPair)
-              tc_commit_pair(empty_bar(stage), 0x3);
+              tc_mma_bf16_pair(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
             else
-              tc_commit(empty_bar(stage));
-            if (++stage == n_st) {
-              stage = 0;
-              phase ^= 1u;
-            }
-          }
-          if (ok) {
-            if constexpr (kPair)
-              tc_commit_pair(tfull_bar(acc), 0x3);
-            else
-              tc_commit(tfull_bar(acc));
+              tc_mma_bf16(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
           }
         }
-      }
+        // the stage is free in both CTAs once these MMAs have read it
+        if constexpr (kPair)
+          tc_commit_pair(empty_bar(stage), 0x3);
+        else
+          tc_commit(empty_bar(stage));
+        if (++stage == n_st) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (i == t.kb_n - 1) {
+          if constexpr (kPair)
+            tc_commit_pair(tfull_bar(acc), 0x3);
+          else
+            tc_commit(tfull_bar(acc));
+        }
+        return true;
+      };
+      walk(next_unit, mma_stage);
       // All MMAs issued by this thread must finish before TMEM is released
       // (in both CTAs of a pair).
       volatile int no_abort = 0;
@@ -1078,6 +1125,20 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
     const cudaError_t e = cudaMemsetAsync(p.sched, 0, sizeof(unsigned), stream);
     if (e != cudaSuccess) return e;
   }
+  // The forward and dlogits (K = H, two accumulators) overlap consecutive
+  // tiles: each tile runs kSoloBlocks of its K blocks alone, while the
+  // epilogue drains the other accumulator, and the rest one-to-one with its
+  // neighbours. Alone at 16384 x 3584 x 152064, two runs each (ms, forward /
+  // dlogits): not overlapped 10.32, 10.22 / 11.29, 11.39; 4 solo blocks 10.15,
+  // 10.11 / 11.26, 11.19; 8: 9.90, 10.14 / 10.99, 11.11; 12: 10.25, 10.13 /
+  // 10.95, 11.00; 16: 10.21, 10.04 / 11.03, 11.11; 24: 10.30, 10.23 / 11.16,
+  // 11.04. At V = 32000 the tensor pipe went from 76 % to 78-79 % busy.
+  p.interleave = 0;
+  if ((E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && g.mode != kWideMode &&
+      p.k_split == 0 && gemm_interleave_enabled()) {
+    const int kb = (p.K + kBK - 1) / kBK;
+    if (kb >= kSoloBlocks + 2) p.interleave = (kb - kSoloBlocks) / 2;
+  }
   return launch_mode<E>(a, b, c, p, g.mode, lanes, stream);
 }
 
@@ -1135,6 +1196,14 @@ void gemm_schedule(int* schedule, int* grid_cap) {
   }();
   *schedule = forced;
   *grid_cap = cap;
+}
+
+bool gemm_interleave_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("LMH_GEMM_INTERLEAVE");
+    return !(v && v[0] == '0');
+  }();
+  return on;
 }
 
 int gemm_pair_mode() {

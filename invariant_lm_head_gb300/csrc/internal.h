@@ -72,6 +72,9 @@ struct GemmParams {
   // of walking a fixed stride. A unit's arithmetic is the same either way.
   unsigned* sched;
   int dynamic;
+  // K blocks by which consecutive tiles overlap (set by launch_gemm; 0 = none):
+  // a tile's last `interleave` blocks alternate with the next tile's first.
+  int interleave;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -168,6 +171,11 @@ void gemm_store_engine(int* mode, int* tile_n);
 // units), -1 unset (dynamic from kDynamicMinWaves waves); *grid_cap is the
 // most CTAs (single) or CTA pairs a launch uses, 0 when unset (all SMs).
 void gemm_schedule(int* schedule, int* grid_cap);
+// Whether the forward and dlogits overlap consecutive tiles' K loops
+// (LMH_GEMM_INTERLEAVE, read once: "0" off, a diagnostic; on by default), and
+// how many K blocks each tile then runs alone.
+bool gemm_interleave_enabled();
+constexpr int kSoloBlocks = 10;
 // A launch of at least this many waves of units claims them dynamically
 // (grad_weight only from this many rows of K).
 constexpr int kDynamicMinWaves = 4;

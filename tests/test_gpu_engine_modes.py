@@ -174,3 +174,15 @@ def test_pair_halves_past_the_last_row_keep_live_stores_intact(tmp_path, single,
     for rep in range(reps):
         assert _same(out[f"gh{rep}"], single["777_gh"]), f"grad_hidden differs on repeat {rep}"
         assert _same(out[f"gw{rep}"], out["gw0"]), f"grad_weight differs on repeat {rep}"
+
+
+# The forward and dlogits overlap consecutive tiles' K loops by default (the
+# operand ring then alternates between two tiles); each tile's own MMAs keep
+# their order, so turning the overlap off must change no bit on either engine.
+@pytest.mark.parametrize("pairs", ["0", "1"])
+def test_overlapped_tiles_give_identical_bits(tmp_path, single, pairs):
+    on = single if pairs == "0" else _run(tmp_path, "pairs_on", {"LMH_GEMM_CTA_PAIRS": pairs})
+    off = _run(tmp_path, f"off_{pairs}", {"LMH_GEMM_CTA_PAIRS": pairs, "LMH_GEMM_INTERLEAVE": "0"})
+    assert on.keys() == off.keys()
+    for k in on:
+        assert _same(on[k], off[k]), f"{k}: overlapping the tiles changed bits"
