@@ -53,10 +53,11 @@
  *    device status bit that lmhead_device_status() reports.
  *  - The environment variable LMH_GEMM_CTA_PAIRS, read once per process,
  *    picks the tensor-core engine: "0" single CTAs for every contraction,
- *    "1" CTA pairs (two SMs per MMA) wherever a launch has more than 128
- *    rows, unset the default (pairs for grad_weight and grad_hidden when
- *    they need enough fewer waves than single CTAs, and for the forward and
- *    dlogits over an even number of 128-row tiles, or an odd number above 32).
+ *    "1" wide CTA pairs (two SMs per pair of MMAs, 256 x 512 tiles) wherever
+ *    a launch has more than 128 rows, "2" 256 x 256 pairs there, unset the
+ *    default (wide pairs for the forward and dlogits over an even number of
+ *    128-row tiles, or an odd number above 32; for grad_weight and
+ *    grad_hidden the engine that needs the fewest waves by measured cost).
  *    log-prob, entropy, lse, sum_p2 and grad_hidden are bit-identical
  *    whichever engine runs. grad_weight is deterministic for a given engine
  *    and SM count; its summation order follows the engine's waves.

@@ -122,7 +122,9 @@ int make_out_tmap(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, ui
                   bool f32, bool transposed = false) {
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {32, 128};
+  // fp32: the 128 x 32 chunk of an epilogue group; bf16: one epilogue warp's
+  // 32 x 32 box
+  cuuint32_t box[2] = {32, f32 ? 128u : 32u};
   if (transposed) {  // StoreF32T: 128 columns x 32 rows of fp32, no swizzle
     box[0] = 128;
     box[1] = 32;

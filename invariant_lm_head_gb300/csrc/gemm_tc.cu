@@ -13,8 +13,10 @@
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=256, K=16, four per 64-wide stage) into one of two
 //               256-column accumulators, and tcgen05.commit frees the stage
-//   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM lane)
-//               and reads it 32 columns at a time with tcgen05.ld
+//   warps 2..9  epilogue, two groups of four: each thread owns one
+//               accumulator row (its TMEM lane) and reads it 32 columns at a
+//               time with tcgen05.ld; on a wide tile each group drains one
+//               256-column half
 // The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
 // In the forward and dlogits (K = H) consecutive tiles also overlap in K: a
 // tile's last K blocks alternate with the next tile's first ones in the
@@ -37,13 +39,15 @@
 // CTA pairs: a cluster of two CTAs owns a 256x256 tile. Each CTA stages its
 // own 128 A rows and one 128-row half of B (6 stages of 32 KB); CTA 0 issues
 // tcgen05.mma.cta_group::2 (M=256), and each CTA's TMEM receives its 128
-// accumulator rows, so the epilogue is the same. Wide pairs (grad_hidden,
-// grad_weight) own 256x512 tiles: two N=256 pair MMAs per K step into one
-// 512-column accumulator per CTA, which halves how often an operand is
-// re-read; the epilogue no longer overlaps the next tile, which their K
-// (V or 16384 rows) mostly hides. Every engine walks K in the same MMA order
-// for the forward, dlogits and grad_hidden, so their bits do not depend on
-// the engine.
+// accumulator rows, so the epilogue is the same. Wide pairs own 256x512
+// tiles: two N=256 pair MMAs per K step into one 512-column accumulator per
+// CTA, two independent chains that share each A stage, so a CTA stages a
+// quarter fewer operand bytes per flop and an operand is re-read half as
+// often. Their epilogue no longer overlaps the next tile; a long K (grad_hidden,
+// grad_weight) hides it, and for the forward and dlogits (K = H) the saved
+// operand traffic outweighs it. Every engine walks K in the same MMA order for
+// the forward, dlogits and grad_hidden, so their bits do not depend on the
+// engine.
 //
 // Narrow tiles: single CTAs and pairs also take tiles of fewer columns (64,
 // 128 or 192 alone, 128 in a pair; MN-major B only), so a short grad_hidden
@@ -105,9 +109,11 @@ constexpr int kBarrierBytes = 512;
 // stages plus the two accumulators (every unit has at least one stage), about
 // 11 units, so 16 slots never lap.
 constexpr int kUnitSlots = 16;
-// Two staging buffers for the TMA-store epilogues: 128 rows x 128 bytes
-// (32 fp32 or, using half of it, 32 bf16 columns).
+// Staging for the TMA-store epilogues, 32 KB: two 16 KB buffers of a 128 x 32
+// fp32 chunk, or per epilogue warp a share of 2 KB buffers of its 32 x 32 bf16
+// boxes.
 constexpr int kStagingBytes = kBM * 128;
+constexpr uint32_t kStagingTotal = 2 * kStagingBytes;
 
 // Engine modes: one CTA per 128 x 256 tile; a CTA pair per 256 x 256 tile;
 // a CTA pair per 256 x 512 tile ("wide": two N=256 pair MMAs per K step into
@@ -132,12 +138,25 @@ struct Ring {
   static constexpr int kSmemBytes = kStages * kStageBytes + 2 * kStagingBytes + kBarrierBytes + 1024;
   static_assert(kSmemBytes <= 232448, "exceeds the 227 KB shared-memory limit per CTA");
   // full and empty per stage, two accumulator pairs, final, the unit ring's
-  // slots; then the TMEM address, the abort flag, two epilogue go flags, the
-  // peer's load count, two epilogue unit words and the unit ring
-  static_assert(8 * (2 * kMaxStages + 5 + kUnitSlots) + 4 * (7 + kUnitSlots) <= kBarrierBytes,
+  // slots, the forward's two exchange buffers' full and empty; then the TMEM
+  // address, the abort flag, the peer's load count, two go flags and two unit
+  // words per epilogue group, two exchange go flags and the unit ring
+  static_assert(8 * (2 * kMaxStages + 5 + kUnitSlots + 4) + 4 * (13 + kUnitSlots) <=
+                    kBarrierBytes,
                 "barrier area too small");
 };
-constexpr uint32_t kEpiBarrier = 1;  // named barrier of the 128 epilogue threads
+constexpr uint32_t kEpiBarrier = 1;  // named barriers 1 and 2: one per epilogue group of 128
+
+// Two epilogue groups drain a wide tile's two halves at the same time for the
+// forward and the bf16 stores. The fp32 stores keep one group (their long K
+// leaves little to overlap, and a 320-thread CTA measured 2.5 % slower for
+// grad_hidden and grad_weight even with the second group idle).
+template <int E, int kMode>
+constexpr bool kSplitHalvesFor =
+    kMode == kWideMode &&
+    (E == (int)Epi::FwdStats || E == (int)Epi::DLogits || E == (int)Epi::StoreBf16);
+template <int E, int kMode>
+constexpr int kThreadsFor = kSplitHalvesFor<E, kMode> ? kGemmThreadsTwoGroups : kGemmThreadsOneGroup;
 
 // Unit u -> (m unit, N tiles). Units enumerate (m unit, vocab unit) pairs in
 // groups of group_m m units, unit-major inside a group, so concurrently
@@ -183,9 +202,10 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 }
 
 // One row's 32 columns into a staging buffer laid out as the TMA store reads
-// it. fp32: 128-byte rows with 128-byte swizzle (16-byte chunk j of row r at
-// chunk j ^ (r % 8)). bf16: 64-byte rows with 64-byte swizzle (chunk j at
-// j ^ ((r / 2) % 4)). Either way a warp's 32 rows spread evenly over the banks.
+// it (128 rows for fp32, a warp's 32 rows for bf16). fp32: 128-byte rows with
+// 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)). bf16:
+// 64-byte rows with 64-byte swizzle (chunk j at j ^ ((r / 2) % 4)). Either
+// way a warp's 32 rows spread evenly over the banks.
 __device__ __forceinline__ void stage_row_f32(uint32_t buf, int r, const float (&v)[32]) {
   const uint32_t row = buf + static_cast<uint32_t>(r) * 128u;
 #pragma unroll
@@ -245,14 +265,21 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   auto ufull_bar = [&](int j) {
     return bar0 + 8u * static_cast<uint32_t>(2 * kS + 5 + (j & (kUnitSlots - 1)));
   };
+  // the forward's group exchange: buffer b's full (group 1 wrote) and empty
+  // (group 0 read) barriers
+  auto xfull_bar = [&](int b) { return bar0 + 8u * static_cast<uint32_t>(2 * kS + 5 + kUnitSlots + b); };
+  auto xempty_bar = [&](int b) {
+    return bar0 + 8u * static_cast<uint32_t>(2 * kS + 7 + kUnitSlots + b);
+  };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(bars) +
-                                                    8 * (2 * kS + 5 + kUnitSlots));
+                                                    8 * (2 * kS + 9 + kUnitSlots));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* epi_go = reinterpret_cast<volatile int*>(tmem_slot + 2);  // [2]
   // pair: the number of stage loads CTA 1 issued, published to CTA 0 at the end
-  volatile uint32_t* peer_issued = tmem_slot + 4;
-  volatile int* epi_unit = reinterpret_cast<volatile int*>(tmem_slot + 5);  // [2]
-  volatile int* uring = reinterpret_cast<volatile int*>(tmem_slot + 7);     // [kUnitSlots]
+  volatile uint32_t* peer_issued = tmem_slot + 2;
+  volatile int* epi_go = reinterpret_cast<volatile int*>(tmem_slot + 3);     // [group][2]
+  volatile int* epi_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);   // [group][2]
+  volatile int* x_go = reinterpret_cast<volatile int*>(tmem_slot + 11);      // [group]
+  volatile int* uring = reinterpret_cast<volatile int*>(tmem_slot + 13);     // [kUnitSlots]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -386,6 +413,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     }
     mbar_init(final_bar, 1);
     for (int j = 0; j < kUnitSlots; ++j) mbar_init(ufull_bar(j), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(xfull_bar(b), 128);
+      mbar_init(xempty_bar(b), 128);
+    }
     *abort_flag = 0;
     *peer_issued = 0;
     fence_barrier_init();
@@ -564,20 +595,10 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         return ring_unit(uj, u);
       };
-      // One K block of tile t: its accumulator is t.idx % kAccs; the first
-      // block waits until the epilogue has released that accumulator, and
-      // the last hands it to the epilogue.
-      auto mma_stage = [&](const WalkTile& t, int i) -> bool {
-        const uint32_t acc = static_cast<uint32_t>(t.idx) % R::kAccs;
-        if (i == 0) {
-          const uint32_t aph = (static_cast<uint32_t>(t.idx) / R::kAccs) & 1u;
-          if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) return false;
-          tc_fence_after();
-        }
-        const uint32_t d_tmem = tmem_base + acc * kBN;
-        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t sA = smem_base + stage * stage_stride;
+      // The MMAs of N block nb (one 256-column chain, into TMEM columns from
+      // d_tmem) over the K block in stage st, block i of its tile.
+      auto issue_chain = [&](uint32_t st, int i, int nb, uint32_t d_tmem) {
+        const uint32_t sA = smem_base + st * stage_stride;
         const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
         const uint64_t bdesc =
             p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
@@ -592,20 +613,126 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 #pragma unroll
         for (int k = 0; k < kBK / 16; ++k) {
           const uint32_t accumulate = (i > 0 || k > 0) ? 1u : 0u;
+          const uint64_t bd = bdesc + kBlockStep * nb + bstep * k;
+          if constexpr (kPair)
+            tc_mma_bf16_pair(d_tmem, adesc + astep * k, bd, idesc, accumulate);
+          else
+            tc_mma_bf16(d_tmem, adesc + astep * k, bd, idesc, accumulate);
+        }
+      };
+      // Both N blocks of a wide tile over the K block in stage st, the two
+      // chains alternating at every K step so that each MMA's predecessor in
+      // its chain was issued two MMAs earlier.
+      auto issue_both = [&](uint32_t st, int i) {
+        const uint32_t sA = smem_base + st * stage_stride;
+        const uint64_t adesc = p.a_mn ? sw128_mnmajor_desc(sA) : sw128_kmajor_desc(sA);
+        const uint64_t bdesc =
+            p.b_mn ? sw128_mnmajor_desc(sA + kABytes) : sw128_kmajor_desc(sA + kABytes);
+        const uint64_t astep = p.a_mn ? 128ull : 2ull;
+        const uint64_t bstep = p.b_mn ? 128ull : 2ull;
+        constexpr uint64_t kBlockStep = (R::kBBytes / R::kNBlocks) >> 4;
 #pragma unroll
-          for (int nb = 0; nb < R::kNBlocks; ++nb) {
+        for (int k = 0; k < kBK / 16; ++k) {
+          const uint32_t accumulate = (i > 0 || k > 0) ? 1u : 0u;
+#pragma unroll
+          for (int nb = 0; nb < 2; ++nb) {
             const uint64_t bd = bdesc + kBlockStep * nb + bstep * k;
             if constexpr (kPair)
-              tc_mma_bf16_pair(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
+              tc_mma_bf16_pair(tmem_base + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
             else
-              tc_mma_bf16(d_tmem + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
+              tc_mma_bf16(tmem_base + nb * kBN, adesc + astep * k, bd, idesc, accumulate);
           }
         }
-        // the stage is free in both CTAs once these MMAs have read it
+      };
+      auto free_stage = [&](uint32_t st) {  // free in both CTAs once its MMAs have read it
         if constexpr (kPair)
-          tc_commit_pair(empty_bar(stage), 0x3);
+          tc_commit_pair(empty_bar(st), 0x3);
         else
-          tc_commit(empty_bar(stage));
+          tc_commit(empty_bar(st));
+      };
+      // Wide tiles: the epilogue releases the accumulator's two 256-column
+      // halves one after the other (tempty 0, then 1). A tile's N block 0
+      // starts as soon as half 0 is free; while half 1 is still being
+      // drained, its stages are held after block 0's MMAs (at most the ring
+      // less one) and block 1 catches up on them once half 1 is free.
+      bool half1_free = false;
+      int n_held = 0;
+      uint32_t held_stage[kMaxStages];
+      int held_block[kMaxStages];
+      auto wide_stage = [&](const WalkTile& t, int i) -> bool {
+        const uint32_t aph = static_cast<uint32_t>(t.idx) & 1u;
+        if (i == 0) {
+          if (!mbar_wait(tempty_bar(0), aph ^ 1u, abort_flag, p.status)) return false;
+          half1_free = mbar_try_wait(tempty_bar(1), aph ^ 1u);
+          tc_fence_after();
+          n_held = 0;
+        }
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) return false;
+        tc_fence_after();
+        if (half1_free) {  // steady state: both chains, interleaved
+          issue_both(stage, i);
+          free_stage(stage);
+          if (++stage == n_st) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (i == t.kb_n - 1) {
+            if constexpr (kPair)
+              tc_commit_pair(tfull_bar(0), 0x3);
+            else
+              tc_commit(tfull_bar(0));
+          }
+          return true;
+        }
+        // half 1 still draining: N block 0 alone, the stage held for block 1
+        issue_chain(stage, i, 0, tmem_base);
+        if (mbar_try_wait(tempty_bar(1), aph ^ 1u)) {
+          half1_free = true;
+        } else if (n_held + 1 >= static_cast<int>(n_st) || i == t.kb_n - 1) {
+          if (!mbar_wait(tempty_bar(1), aph ^ 1u, abort_flag, p.status)) return false;
+          half1_free = true;
+        }
+        if (half1_free) tc_fence_after();
+        if (half1_free) {
+          for (int h = 0; h < n_held; ++h) {
+            issue_chain(held_stage[h], held_block[h], 1, tmem_base + kBN);
+            free_stage(held_stage[h]);
+          }
+          n_held = 0;
+          issue_chain(stage, i, 1, tmem_base + kBN);
+          free_stage(stage);
+        } else {
+          held_stage[n_held] = stage;
+          held_block[n_held] = i;
+          ++n_held;
+        }
+        if (++stage == n_st) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (i == t.kb_n - 1) {
+          if constexpr (kPair)
+            tc_commit_pair(tfull_bar(0), 0x3);
+          else
+            tc_commit(tfull_bar(0));
+        }
+        return true;
+      };
+      // One K block of tile t: its accumulator is t.idx % kAccs; the first
+      // block waits until the epilogue has released that accumulator, and
+      // the last hands it to the epilogue.
+      auto mma_stage = [&](const WalkTile& t, int i) -> bool {
+        if constexpr (kMode == kWideMode) return wide_stage(t, i);
+        const uint32_t acc = static_cast<uint32_t>(t.idx) % R::kAccs;
+        if (i == 0) {
+          const uint32_t aph = (static_cast<uint32_t>(t.idx) / R::kAccs) & 1u;
+          if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) return false;
+          tc_fence_after();
+        }
+        if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) return false;
+        tc_fence_after();
+        issue_chain(stage, i, 0, tmem_base + acc * kBN);
+        free_stage(stage);
         if (++stage == n_st) {
           stage = 0;
           phase ^= 1u;
@@ -635,26 +762,40 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // Control flow is uniform over the 128 epilogue threads: epilogue thread 0
-    // does the bounded wait for each accumulator and publishes the outcome,
-    // so no thread can be left waiting at a named barrier the others skipped.
+    // Two groups of four warps (threads 64-191 and 192-319). On a wide tile
+    // of the forward or a bf16 store, group g drains the accumulator's
+    // 256-column half g and hands it back to the MMA issuer on its own, so
+    // the halves drain at the same time. Otherwise group 0 drains every tile
+    // (on a wide tile, half 0 first, handed back as soon as it is read) and
+    // group 1 has no work: the fp32 stores keep two staging buffers per warp
+    // that way, and their long K leaves little to overlap.
+    // Control flow is uniform within a group: the group's thread 0 does the
+    // bounded wait for each accumulator and publishes the outcome, so no
+    // thread can be left waiting at a named barrier the others skipped.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
-    const int etid = threadIdx.x - 64;
+    const int grp = (warp - 2) >> 2;
+    const int gtid = (threadIdx.x - 64) & 127;  // thread within the group
+    const uint32_t grp_bar = kEpiBarrier + static_cast<uint32_t>(grp);
+    constexpr bool kSplitHalves = kSplitHalvesFor<E, kMode>;
+    constexpr int kGroups = kSplitHalves ? 2 : 1;
+    // each warp's staging: a quarter of a group's share of the 32 KB
+    const uint32_t warp_staging =
+        staging + static_cast<uint32_t>(grp * 4 + q) * (kStagingTotal / (4 * kGroups));
     uint32_t it = 0, chunk_ctr = 0;
-    bool ok = true;
+    bool ok = grp < kGroups;
     for (int uj = 0; ok; ++uj) {
       int u;
       if (!dyn) {
         u = static_unit(uj);
       } else {
-        // epilogue thread 0 reads the slot (bounded) and shares it: -2 = gave up
-        if (etid == 0) {
+        // the group's thread 0 reads the slot (bounded) and shares it: -2 = gave up
+        if (gtid == 0) {
           int v = -1;
-          epi_unit[uj & 1] = ring_unit(uj, v) ? v : -2;
+          epi_unit[grp * 2 + (uj & 1)] = ring_unit(uj, v) ? v : -2;
         }
-        named_barrier(kEpiBarrier, 128);
-        u = epi_unit[uj & 1];
+        named_barrier(grp_bar, 128);
+        u = epi_unit[grp * 2 + (uj & 1)];
         if (u == -2) {
           ok = false;
           break;
@@ -692,23 +833,52 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           c1 = __fmul_rn(__fmul_rn(p.inv_temp, ge), kLn2);
         }
       }
-      OnlineStat st = stat_empty();
+      // The forward folds a row's vocabulary unit as two streams, the even
+      // and the odd 256-column blocks (on a wide tile, its two halves), and
+      // merges them at the unit's end: the same on every engine. sb is the
+      // stream being folded; on 256-column tiles the two swap at each tile
+      // (register moves, so neither lives in local memory).
+      OnlineStat sb = stat_empty(), sb_other = stat_empty();
       float zl = __int_as_float(0x7fc00000);  // NaN until the label column is seen
 
       for (int j = 0; j < n_count; ++j, ++it) {
         const int n_tile = n_first + j;
         const uint32_t acc = it % R::kAccs;
         const uint32_t aph = (it / R::kAccs) & 1u;
-        if (etid == 0) epi_go[it & 1u] = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
-        named_barrier(kEpiBarrier, 128);
-        if (!epi_go[it & 1u]) {
+        volatile int* go = epi_go + grp * 2;
+        if (gtid == 0) go[it & 1u] = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
+        named_barrier(grp_bar, 128);
+        if (!go[it & 1u]) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
+        // this group's 32-column chunks: a wide tile's half, or a whole tile
+        const int c_first = kSplitHalves ? grp * (kBN / 32) : 0;
+        const int c_end = kSplitHalves ? c_first + kBN / 32 : tile_n / 32;
+        // hand columns back to the MMA issuer (CTA 0 of a pair): the
+        // accumulator, or one 256-column half of a wide one
+        auto release = [&](uint32_t bar) {
+          tc_fence_before();
+          if constexpr (kPair)
+            mbar_arrive_remote(mapa_shared(tempty_bar(bar), 0));
+          else
+            mbar_arrive(tempty_bar(bar));
+        };
+        bool half0_released = false;
+        // the forward's stream: on 256-column tiles the tile's block parity
+        // in the unit (a unit starts on a block), on a wide tile the group's
+        // own (half g of tile j is block 2j + g)
+        if constexpr (E == (int)Epi::FwdStats && kMode != kWideMode) {
+          if (j > 0) {
+            const OnlineStat t = sb;
+            sb = sb_other;
+            sb_other = t;
+          }
+        }
 #pragma unroll 1
-        for (int c = 0; c < tile_n / 32; ++c) {
+        for (int c = c_first; c < c_end; ++c) {
           const int col0 = n_tile * tile_n + c * 32;
           if (col0 >= p.N) break;  // uniform over the CTA
           // A store epilogue stages nothing for a tile wholly past the last
@@ -720,6 +890,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const int nvalid = min(32, p.N - col0);
           float v[32];
           tmem_ld32(taddr + c * 32, v);
+          if constexpr (kMode == kWideMode && !kSplitHalves) {
+            if (c == kBN / 32 - 1) {  // the first half has been read
+              release(0);
+              half0_released = true;
+            }
+          }
 
           if constexpr (E == (int)Epi::FwdStats) {
             // y = acc * scale2 (the temperature and log2(e)), folded into
@@ -728,14 +904,14 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             // (m, s and u do not depend on it).
             if (p.part_q) {
               if (nvalid == 32)
-                stat_fold_scaled<32, true>(st, v, p.scale2);
+                stat_fold_scaled<32, true>(sb, v, p.scale2);
               else
-                stat_fold_scaled<32, true>(st, v, p.scale2, nvalid);
+                stat_fold_scaled<32, true>(sb, v, p.scale2, nvalid);
             } else {
               if (nvalid == 32)
-                stat_fold_scaled<32, false>(st, v, p.scale2);
+                stat_fold_scaled<32, false>(sb, v, p.scale2);
               else
-                stat_fold_scaled<32, false>(st, v, p.scale2, nvalid);
+                stat_fold_scaled<32, false>(sb, v, p.scale2, nvalid);
             }
             const int rel = lab - col0;
             if (__any_sync(0xffffffffu, rel >= 0 && rel < nvalid)) {
@@ -776,54 +952,121 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
                   if (i == rel) v[i] = __fadd_rn(v[i], gs);
               }
             }
-            // Stage the 128 x 32 chunk and store it with one TMA bulk store
-            // (or reduce-add); rows and columns outside the output are clipped.
-            const uint32_t buf = staging + (chunk_ctr & 1u) * kStagingBytes;
-            if (etid == 0) bulk_wait_group_read<1>();  // this buffer's last store has read it
-            named_barrier(kEpiBarrier, 128);
-            if constexpr (E == (int)Epi::StoreF32)
-              stage_row_f32(buf, row_in_tile, v);
-            else if constexpr (E == (int)Epi::StoreF32T)
-              stage_col_f32(buf, row_in_tile, v);
-            else
-              stage_row_bf16(buf, row_in_tile, v);
-            fence_proxy_async_smem();
-            named_barrier(kEpiBarrier, 128);
-            if (etid == 0) {
-              // (x, y) of the box in the output: transposed for StoreF32T
-              const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
-              const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM + seg * p.seg_rows;
-              if ((E == (int)Epi::StoreF32 || E == (int)Epi::StoreF32T) && p.accumulate)
-                tma_reduce_add_2d(&tmC, buf, ox, oy);
+            // Each warp stages its 32 rows of the chunk and its lane 0 stores
+            // them with one TMA bulk store (or reduce-add) of a 32 x 32 box;
+            // rows and columns outside the output are clipped. No barrier
+            // across the warps: a warp reuses a buffer once its own store from
+            // that buffer (kBufs chunks back) has read it.
+            // bf16: each warp stages its 32 rows of the chunk and its lane 0
+            // stores them with one TMA bulk store of a 32 x 32 box, with no
+            // barrier across the warps (a warp reuses a buffer once its own
+            // store from it, kBufs chunks back, has read it). fp32: the group
+            // stages the whole 128 x 32 chunk in one of two buffers and its
+            // thread 0 stores (or reduce-adds) it, which measured 5 % faster
+            // than 32-row boxes for a short grad_weight. Rows and columns
+            // outside the output are clipped.
+            constexpr bool kBf16Out = E == (int)Epi::DLogits || E == (int)Epi::StoreBf16;
+            if constexpr (kBf16Out) {
+              constexpr uint32_t kBufBytes = 32 * 64;
+              constexpr uint32_t kBufs = kStagingTotal / (4 * kGroups) / kBufBytes;
+              const uint32_t buf = warp_staging + (chunk_ctr % kBufs) * kBufBytes;
+              if (lane == 0) bulk_wait_group_read<kBufs - 1>();
+              __syncwarp();
+              stage_row_bf16(buf, lane, v);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                const int r0 = m_tile * kBM + q * 32;
+                tma_store_2d(&tmC, buf, col0, r0 + seg * p.seg_rows);
+                bulk_commit_group();
+              }
+            } else {
+              const uint32_t buf = staging + (chunk_ctr & 1u) * kStagingBytes;
+              if (gtid == 0) bulk_wait_group_read<1>();  // this buffer's last store has read it
+              named_barrier(grp_bar, 128);
+              if constexpr (E == (int)Epi::StoreF32)
+                stage_row_f32(buf, row_in_tile, v);
               else
-                tma_store_2d(&tmC, buf, ox, oy);
-              bulk_commit_group();
+                stage_col_f32(buf, row_in_tile, v);
+              fence_proxy_async_smem();
+              named_barrier(grp_bar, 128);
+              if (gtid == 0) {
+                // (x, y) of the box in the output: transposed for StoreF32T
+                const int ox = E == (int)Epi::StoreF32T ? m_tile * kBM : col0;
+                const int oy = E == (int)Epi::StoreF32T ? col0 : m_tile * kBM + seg * p.seg_rows;
+                if (p.accumulate)
+                  tma_reduce_add_2d(&tmC, buf, ox, oy);
+                else
+                  tma_store_2d(&tmC, buf, ox, oy);
+                bulk_commit_group();
+              }
             }
             ++chunk_ctr;
           }
         }
-        tc_fence_before();
-        if constexpr (kPair)
-          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));  // CTA 0 reissues the MMAs
-        else
-          mbar_arrive(tempty_bar(acc));
+        if constexpr (kSplitHalves) {
+          release(static_cast<uint32_t>(grp));
+        } else if constexpr (kMode == kWideMode) {
+          if (!half0_released) release(0);
+          release(1);
+        } else {
+          release(acc);
+        }
       }
       if (!ok) break;
 
       if constexpr (E == (int)Epi::FwdStats) {
+        // on 256-column tiles sb holds the last tile's stream
+        const bool last_odd = kMode != kWideMode && ((n_count - 1) & 1);
+        OnlineStat all = last_odd ? sb_other : sb;
+        OnlineStat odd = last_odd ? sb : sb_other;
+        if constexpr (kSplitHalves) {
+          // Group 1 (the odd blocks) hands its stream to group 0 through one
+          // of two shared-memory buffers (in the staging area, which the
+          // forward does not store through). Each buffer has a full and an
+          // empty barrier; a group's thread 0 waits on it (bounded) and
+          // shares the outcome over the group's named barrier.
+          const int b = uj & 1;
+          const uint32_t xph = static_cast<uint32_t>(uj >> 1) & 1u;
+          float* xrow = reinterpret_cast<float*>(smem + kRingBytes) + b * (kBM * 5) + row_in_tile * 5;
+          if (grp == 1) {
+            if (gtid == 0) x_go[1] = mbar_wait(xempty_bar(b), xph ^ 1u, abort_flag, p.status) ? 1 : 0;
+            named_barrier(grp_bar, 128);
+            if (!x_go[1]) break;
+            xrow[0] = sb.m;
+            xrow[1] = sb.s;
+            xrow[2] = sb.u;
+            xrow[3] = sb.q;
+            xrow[4] = zl;
+            mbar_arrive(xfull_bar(b));  // release: this thread's row is written
+            continue;
+          }
+          if (gtid == 0) x_go[0] = mbar_wait(xfull_bar(b), xph, abort_flag, p.status) ? 1 : 0;
+          named_barrier(grp_bar, 128);
+          if (!x_go[0]) break;
+          odd = OnlineStat{xrow[0], xrow[1], xrow[2], xrow[3]};
+          const float zl_odd = xrow[4];
+          mbar_arrive(xempty_bar(b));  // this thread has read its row
+          // the label's 256-column block decides whose capture holds its logit
+          if (lab >= 0 && ((lab / kBN) & 1)) zl = zl_odd;
+        }
+        if (p.part_q)
+          stat_merge<true>(all, odd);
+        else
+          stat_merge<false>(all, odd);
         if (row_ok) {
           const int64_t o = static_cast<int64_t>(vunit) * p.part_ld + row;
-          p.part_m[o] = st.m;
-          p.part_s[o] = st.s;
-          p.part_u[o] = st.u;
-          if (p.part_q) p.part_q[o] = st.q;
+          p.part_m[o] = all.m;
+          p.part_s[o] = all.s;
+          p.part_u[o] = all.u;
+          if (p.part_q) p.part_q[o] = all.q;
           const int c0 = n_first * tile_n;
           const int c1 = min(p.N, (n_first + n_count) * tile_n);
           if (lab >= c0 && lab < c1) p.part_zl[row] = zl;
         }
       }
     }
-    if (etid == 0) bulk_wait_group<0>();  // every output store has completed
+    if (lane == 0) bulk_wait_group<0>();  // every output store of this warp has completed
   }
 
   tc_fence_before();
@@ -867,7 +1110,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
 }
 
 template <int E>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kGemmThreadsOneGroup, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   gemm_body<E, kSingle>(tmA, tmB, tmC, p);
@@ -875,7 +1118,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // kMode: kPairMode or kWideMode
 template <int E, int kMode>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreadsFor<E, kMode>, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
@@ -902,7 +1145,7 @@ int pair_slots(int num_sms) {
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-  cfg.blockDim = dim3(kGemmThreads);
+  cfg.blockDim = dim3(kThreadsFor<E, kMode>);
   cfg.dynamicSmemBytes = Ring<kMode>::kSmemBytes;
   int n = 0;
   if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_pair_kernel<E, kMode>, &cfg) != cudaSuccess) {
@@ -927,31 +1170,28 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtenso
     if (lanes <= 0) return cudaErrorInvalidConfiguration;  // launch_gemm checked it first
     const int clusters = p.n_units < lanes ? p.n_units : lanes;  // persistent
     gemm_tc_pair_kernel<E, kMode>
-        <<<2 * clusters, kGemmThreads, Ring<kMode>::kSmemBytes, stream>>>(a, b, c, p);
+        <<<2 * clusters, kThreadsFor<E, kMode>, Ring<kMode>::kSmemBytes, stream>>>(a, b, c, p);
   } else {
     e = cudaFuncSetAttribute(gemm_tc_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Ring<kSingle>::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = p.n_units < lanes ? p.n_units : lanes;  // persistent: <= one CTA per SM
-    gemm_tc_kernel<E><<<grid, kGemmThreads, Ring<kSingle>::kSmemBytes, stream>>>(a, b, c, p);
+    gemm_tc_kernel<E><<<grid, kGemmThreadsOneGroup, Ring<kSingle>::kSmemBytes, stream>>>(a, b, c, p);
   }
   e = cudaGetLastError();
   if (e == cudaSuccess) note_launch();
   return e;
 }
 
-// Engines each contraction is built for besides single CTAs: pairs for all;
-// wide pairs for the store epilogues (not the forward, whose chunk grid is
-// 256-column tiles, nor dlogits, whose K = H is too short to hide an epilogue
-// that no longer overlaps the next tile).
+// The store epilogues (grad_hidden, grad_weight, the bare engine GEMM), whose
+// engine and tile width are chosen by cost and can be forced.
 template <int E>
-constexpr bool kHasWide = !(E == (int)Epi::FwdStats || E == (int)Epi::DLogits);
+constexpr bool kStoreEpi = !(E == (int)Epi::FwdStats || E == (int)Epi::DLogits);
 
 template <int E>
 int slots_for(int mode, int num_sms) {
   if (mode == kPairMode) return pair_slots<E, kPairMode>(num_sms);
-  if constexpr (kHasWide<E>)
-    if (mode == kWideMode) return pair_slots<E, kWideMode>(num_sms);
+  if (mode == kWideMode) return pair_slots<E, kWideMode>(num_sms);
   return 0;
 }
 
@@ -959,8 +1199,7 @@ template <int E>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                         const GemmParams& p, int mode, int lanes, cudaStream_t stream) {
   if (mode == kPairMode) return launch_one<E, kPairMode>(a, b, c, p, lanes, stream);
-  if constexpr (kHasWide<E>)
-    if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, lanes, stream);
+  if (mode == kWideMode) return launch_one<E, kWideMode>(a, b, c, p, lanes, stream);
   return launch_one<E, kSingle>(a, b, c, p, lanes, stream);
 }
 
@@ -999,16 +1238,21 @@ double engine_cost(const Engine& g, long long m_tiles, long long n, int num_sms,
 template <int E>
 cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
-  // Engine per contraction. The forward and dlogits (K = H) run on pairs
-  // for an even number of m tiles (alone at H = 3584, V = 152064, forward:
-  // -8.5 % at 129 rows, -2 % at 2048, even at 4096; dlogits: -11 % at 512
-  // rows, -3.5 % at 4096), and for an odd number above 32, where the pair
-  // half past the last row costs little (forward on 3 m tiles: +14 %, on 9:
-  // +4.5 %). At 16384 rows pairs were slower alone (forward +3 %, dlogits
-  // +0.6 %) but faster inside the step, which runs at the power cap: three
-  // same-session alternating runs, 40.02-40.21 against 40.35-40.59 ms per
-  // step (dlogits 10.38-10.44 against 10.87-10.91 ms), at a slightly higher
-  // clock: a pair loads half the B operand per flop into each SM.
+  // Engine per contraction. The forward and dlogits (K = H) run on CTA
+  // pairs for an even number of m tiles (alone at H = 3584, V = 152064,
+  // 256-wide pairs against single CTAs, forward: -8.5 % at 129 rows, -2 % at
+  // 2048; dlogits: -11 % at 512 rows, -3.5 % at 4096), and for an odd number
+  // above 32, where the pair half past the last row costs little (forward on
+  // 3 m tiles: +14 %, on 9: +4.5 %). Among pairs they take wide ones: a wide
+  // pair stages a quarter fewer operand bytes per flop, which the 256-wide
+  // pairs' tensor pipe was waiting on (76-79 % busy at V = 32000 against 87 %
+  // wide), and that outweighs its epilogue no longer overlapping the next
+  // tile. Alone, 256-wide / wide (ms): forward 0.335 / 0.315 at 512 rows,
+  // 1.237 / 1.147 at 2048, 2.434 / 2.247 at 4096, 9.86-10.03 / 9.24-9.30 at
+  // 16384, 0.618 / 0.571 at 4096 x 4096 x 32000, even at 256 rows; dlogits
+  // 0.347 / 0.343 at 512, 1.242 / 1.220 at 2048, 2.59 / 2.52 at 4096,
+  // 10.97-11.09 / 10.63-10.75 at 16384; the short step 396-402k / 408-417k
+  // tokens/s.
   // grad_weight and grad_hidden take the engines below; at the 16384 x 3584 x
   // 152064 step, which runs at the power cap, both are on wide pairs (kernels
   // -6 % and -13 %, step -1.4 % and -1.8 %). A pair needs two m tiles: a
@@ -1018,7 +1262,9 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   const int env = gemm_pair_mode();
   Engine g{kSingle, kBN};
   if (env == 1 && m_tiles >= 2) {
-    g.mode = kHasWide<E> ? kWideMode : kPairMode;
+    g = Engine{kWideMode, 2 * kBN};
+  } else if (env == 2 && m_tiles >= 2) {
+    g = Engine{kPairMode, kBN};
   } else if (env < 0 && E == (int)Epi::StoreF32T) {
     // grad_weight (K = the chunk's rows): 256-wide pairs, whose epilogue
     // overlaps the next tile's MMAs, while K is short enough for the fp32
@@ -1027,7 +1273,7 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
     // 0.54 at 512, 0.69 / 0.79 at 1024, 1.29 / 1.28 at 2048, 2.62 / 2.50 at
     // 4096, 5.47 / 5.01 at 8192.
     if (m_tiles >= 2) g = p.K < 2048 ? Engine{kPairMode, kBN} : Engine{kWideMode, 2 * kBN};
-  } else if (env < 0 && kHasWide<E>) {
+  } else if (env < 0 && kStoreEpi<E>) {
     // grad_hidden and the bare engine GEMM: the cheapest engine by
     // engine_cost (pairs only over two or more m tiles). Narrower tiles need
     // an MN-major B (64-column boxes); each output element's K walk is the
@@ -1050,10 +1296,10 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
     }
   } else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles >= 2 &&
              (m_tiles % 2 == 0 || m_tiles > 32)) {
-    g.mode = kPairMode;
+    g = Engine{kWideMode, 2 * kBN};
   }
   // LMH_GEMM_STORE_ENGINE forces the store contractions' engine and width
-  if constexpr (kHasWide<E>) {
+  if constexpr (kStoreEpi<E>) {
     int fm = -1, fn = 0;
     gemm_store_engine(&fm, &fn);
     if (fm == kSingle || (fm >= 0 && m_tiles >= 2)) {
@@ -1065,7 +1311,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // give the same bits
   if (g.mode != kSingle && slots_for<E>(g.mode, num_sms) <= 0) g = Engine{kSingle, kBN};
   if (g.mode == kWideMode) g.tile_n = 2 * kBN;
-  if (E == (int)Epi::FwdStats && g.tile_n != kBN) return cudaErrorInvalidValue;  // chunk grid
+  if (E == (int)Epi::FwdStats && g.tile_n != kBN && !(g.mode == kWideMode && g.tile_n == 2 * kBN))
+    return cudaErrorInvalidValue;  // chunk grid: 1024-column chunks of whole tiles
   const int kb_total = (p.K + kBK - 1) / kBK;
   if (p.k_split != 0 && (!(E == (int)Epi::StoreF32 || E == (int)Epi::StoreBf16) || p.k_split < 0 ||
                          p.k_split >= kb_total || p.seg_rows < (p.M + kBM - 1) / kBM * kBM))
@@ -1077,6 +1324,10 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   p.tile_n = g.mode == kWideMode ? 0 : g.tile_n;
   p.n_m_tiles = (p.M + m_rows - 1) / m_rows;
   p.n_n_tiles = (p.N + g.tile_n - 1) / g.tile_n;
+  // a vocab unit keeps its columns on wider tiles (the forward's 1024-column
+  // chunk is two 512-column wide tiles)
+  if (tiles_per_unit * kBN % g.tile_n == 0 && g.tile_n > kBN)
+    tiles_per_unit = tiles_per_unit * kBN / g.tile_n;
   p.tiles_per_unit = tiles_per_unit;
   const int all_vunits = (p.n_n_tiles + tiles_per_unit - 1) / tiles_per_unit;
   const int vu_end = (p.vunit_end > 0 && p.vunit_end < all_vunits) ? p.vunit_end : all_vunits;
@@ -1211,6 +1462,7 @@ int gemm_pair_mode() {
     const char* v = std::getenv("LMH_GEMM_CTA_PAIRS");
     if (v && v[0] == '0') return 0;
     if (v && v[0] == '1') return 1;
+    if (v && v[0] == '2') return 2;
     return -1;
   }();
   return mode;

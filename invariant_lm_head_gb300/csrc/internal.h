@@ -17,7 +17,10 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
 constexpr int kBBoxRows = kBN / 2;
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+// Engine CTA: warp 0 TMA, warp 1 MMA, then one or two epilogue groups of four
+// warps (two only where a wide tile's halves drain in parallel).
+constexpr int kGemmThreadsOneGroup = 192;
+constexpr int kGemmThreadsTwoGroups = 320;
 
 // Forward: a vocab chunk is kFwdTilesPerChunk N-tiles (1024 columns). The
 // chunk grid depends only on V, so per-row partials and their merge order
@@ -151,12 +154,13 @@ int api_make_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t o
 
 size_t gemm_smem_bytes();
 // Which contractions run on CTA pairs (launches with two or more 128-row m
-// tiles only), from LMH_GEMM_CTA_PAIRS, read once: "0" none (0), "1" all (1;
-// the store epilogues as wide pairs), unset the per-contraction default (-1:
-// grad_hidden and grad_weight by their measured engine choice; the forward
-// and dlogits on pairs over an even number of m tiles or an odd number above
-// 32). The forward, dlogits and grad_hidden give the same bits on every
-// engine; grad_weight's summation order follows the engine's waves.
+// tiles only), from LMH_GEMM_CTA_PAIRS, read once: "0" none (0), "1" all on
+// wide pairs (1), "2" all on 256-wide pairs (2), unset the per-contraction
+// default (-1: grad_hidden and grad_weight by their measured engine choice;
+// the forward and dlogits on wide pairs over an even number of m tiles or an
+// odd number above 32). The forward, dlogits and grad_hidden give the same
+// bits on every engine; grad_weight's summation order follows the engine's
+// waves.
 int gemm_pair_mode();
 // From LMH_GEMM_STORE_ENGINE, read once (a diagnostic, for tests and
 // measurements): the engine and tile width forced on the store contractions

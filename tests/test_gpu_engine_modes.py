@@ -93,8 +93,10 @@ def single(tmp_path_factory):
     return _run(tmp_path_factory.mktemp("single"), "single", {"LMH_GEMM_CTA_PAIRS": "0"})
 
 
-def test_pair_and_single_engines_give_identical_bits(tmp_path, single):
-    pair = _run(tmp_path, "pair", {"LMH_GEMM_CTA_PAIRS": "1"})
+# "1": every contraction on wide pairs; "2": every contraction on 256-wide pairs.
+@pytest.mark.parametrize("pairs", ["1", "2"])
+def test_pair_and_single_engines_give_identical_bits(tmp_path, single, pairs):
+    pair = _run(tmp_path, f"pair{pairs}", {"LMH_GEMM_CTA_PAIRS": pairs})
     assert single.keys() == pair.keys()
     for k in single:
         assert _same(single[k], pair[k]), f"{k}: the single-CTA and CTA-pair engines differ"
@@ -114,7 +116,7 @@ def test_every_store_engine_and_width_gives_identical_bits(tmp_path, single, eng
         assert _same(single[k], forced[k]), f"{k}: engine {engine} differs from single CTAs"
 
 
-@pytest.mark.parametrize("pairs,cap", [("0", "2"), ("1", "3")])
+@pytest.mark.parametrize("pairs,cap", [("0", "2"), ("1", "3"), ("2", "3")])
 def test_dynamic_schedule_gives_identical_bits(tmp_path, single, pairs, cap):
     env = {"LMH_GEMM_CTA_PAIRS": pairs, "LMH_GEMM_GRID_CAP": cap}
     fixed = _run(tmp_path, f"static_{pairs}", dict(env, LMH_GEMM_SCHEDULE="static"))
@@ -157,15 +159,16 @@ torch.save(out, sys.argv[1])
 '''
 
 
+@pytest.mark.parametrize("pairs", ["1", "2"])
 @pytest.mark.parametrize("schedule", ["static", "dynamic"])
-def test_pair_halves_past_the_last_row_keep_live_stores_intact(tmp_path, single, schedule):
+def test_pair_halves_past_the_last_row_keep_live_stores_intact(tmp_path, single, schedule, pairs):
     import torch
 
     reps = 12
     child = tmp_path / "repeat.py"
     child.write_text(CHILD_REPEAT)
     path = tmp_path / "rep.pt"
-    env = dict(os.environ, LMH_GEMM_CTA_PAIRS="1", LMH_GEMM_GRID_CAP="1",
+    env = dict(os.environ, LMH_GEMM_CTA_PAIRS=pairs, LMH_GEMM_GRID_CAP="1",
                LMH_GEMM_SCHEDULE=schedule)
     r = subprocess.run([sys.executable, str(child), str(path), ROOT, str(reps)], env=env,
                        cwd=ROOT, capture_output=True, text=True, timeout=900)
@@ -176,10 +179,11 @@ def test_pair_halves_past_the_last_row_keep_live_stores_intact(tmp_path, single,
         assert _same(out[f"gw{rep}"], out["gw0"]), f"grad_weight differs on repeat {rep}"
 
 
-# The forward and dlogits overlap consecutive tiles' K loops by default (the
-# operand ring then alternates between two tiles); each tile's own MMAs keep
-# their order, so turning the overlap off must change no bit on either engine.
-@pytest.mark.parametrize("pairs", ["0", "1"])
+# On single CTAs and 256-wide pairs the forward and dlogits overlap
+# consecutive tiles' K loops (the operand ring then alternates between two
+# tiles); each tile's own MMAs keep their order, so turning the overlap off
+# must change no bit on either engine.
+@pytest.mark.parametrize("pairs", ["0", "2"])
 def test_overlapped_tiles_give_identical_bits(tmp_path, single, pairs):
     on = single if pairs == "0" else _run(tmp_path, "pairs_on", {"LMH_GEMM_CTA_PAIRS": pairs})
     off = _run(tmp_path, f"off_{pairs}", {"LMH_GEMM_CTA_PAIRS": pairs, "LMH_GEMM_INTERLEAVE": "0"})
