@@ -75,9 +75,11 @@
 //   StoreF32   D = A * B^T in fp32, row-major (the bare engine GEMM).
 //
 // Batch invariance: the work split depends only on N (vocab) and never on M
-// (rows), each row is reduced by one thread in a fixed column order, there are
-// no atomics, and the forward, dlogits and grad_hidden contractions walk K in
-// ascending order for every tile. Which engine runs depends on M (a pair
+// (rows); a row's forward statistics over a 1024-column unit are folded as two
+// streams (its even and odd 256-column blocks, each in column order) merged
+// in that order, the same on every engine; there are no atomics; and the
+// forward, dlogits and grad_hidden contractions walk K in ascending order for
+// every tile. Which engine runs depends on M (a pair
 // needs two m tiles), and changes none of their bits. grad_weight, a sum over rows that no row's
 // output depends on, walks K downwards on a CTA's odd waves for L2 reuse; its
 // bits are fixed by the inputs, the row chunking, the SM count and the engine.
