@@ -149,8 +149,9 @@ struct Ring {
 };
 constexpr uint32_t kEpiBarrier = 1;  // named barriers 1 and 2: one per epilogue group of 128
 
-// Two epilogue groups drain a wide tile's two halves at the same time for the
-// forward and the bf16 stores. The fp32 stores keep one group (their long K
+// Two epilogue groups share the drain of a wide tile for the forward and the
+// bf16 stores: both read half 0 first, so it is handed back after half the
+// drain. The fp32 stores keep one group (their long K
 // leaves little to overlap, and a 320-thread CTA measured 2.5 % slower for
 // grad_hidden and grad_weight even with the second group idle).
 template <int E, int kMode>
@@ -411,7 +412,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
       // every epilogue thread of the pair releases the accumulator to CTA 0
-      mbar_init(tempty_bar(a), kPair ? 256 : 128);
+      // every epilogue thread of the pair (of each group) releases it
+      mbar_init(tempty_bar(a), (kPair ? 256 : 128) * (kSplitHalvesFor<E, kMode> ? 2 : 1));
     }
     mbar_init(final_bar, 1);
     for (int j = 0; j < kUnitSlots; ++j) mbar_init(ufull_bar(j), 1);
@@ -836,11 +838,12 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
       }
       // The forward folds a row's vocabulary unit as two streams, the even
-      // and the odd 256-column blocks (on a wide tile, its two halves), and
-      // merges them at the unit's end: the same on every engine. sb is the
-      // stream being folded; on 256-column tiles the two swap at each tile
-      // (register moves, so neither lives in local memory).
+      // and the odd 128-column blocks, and merges them at the unit's end: the
+      // same on every engine. sb is the stream being folded (parity cur_par);
+      // a single group swaps the two as the parity changes (register moves,
+      // so neither lives in local memory).
       OnlineStat sb = stat_empty(), sb_other = stat_empty();
+      int cur_par = 0;
       float zl = __int_as_float(0x7fc00000);  // NaN until the label column is seen
 
       for (int j = 0; j < n_count; ++j, ++it) {
@@ -856,9 +859,11 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         tc_fence_after();
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBN;
-        // this group's 32-column chunks: a wide tile's half, or a whole tile
-        const int c_first = kSplitHalves ? grp * (kBN / 32) : 0;
-        const int c_end = kSplitHalves ? c_first + kBN / 32 : tile_n / 32;
+        // This group's 32-column chunks, in order: on a wide tile split
+        // between two groups, four of half 0 (group g: chunks 4g..4g+3) and
+        // then the matching four of half 1, so that half 0 is read, and
+        // handed back, after half the drain; otherwise every chunk.
+        const int n_iter = kSplitHalves ? 8 : tile_n / 32;
         // hand columns back to the MMA issuer (CTA 0 of a pair): the
         // accumulator, or one 256-column half of a wide one
         auto release = [&](uint32_t bar) {
@@ -872,15 +877,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         // the forward's stream: on 256-column tiles the tile's block parity
         // in the unit (a unit starts on a block), on a wide tile the group's
         // own (half g of tile j is block 2j + g)
-        if constexpr (E == (int)Epi::FwdStats && kMode != kWideMode) {
-          if (j > 0) {
-            const OnlineStat t = sb;
-            sb = sb_other;
-            sb_other = t;
-          }
-        }
 #pragma unroll 1
-        for (int c = c_first; c < c_end; ++c) {
+        for (int ci = 0; ci < n_iter; ++ci) {
+          const int c = kSplitHalves ? (ci >> 2) * (kBN / 32) + 4 * grp + (ci & 3) : ci;
           const int col0 = n_tile * tile_n + c * 32;
           if (col0 >= p.N) break;  // uniform over the CTA
           // A store epilogue stages nothing for a tile wholly past the last
@@ -892,14 +891,26 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           const int nvalid = min(32, p.N - col0);
           float v[32];
           tmem_ld32(taddr + c * 32, v);
-          if constexpr (kMode == kWideMode && !kSplitHalves) {
-            if (c == kBN / 32 - 1) {  // the first half has been read
+          if constexpr (kMode == kWideMode) {
+            // the first half has been read (by this group)
+            if (kSplitHalves ? ci == 3 : c == kBN / 32 - 1) {
               release(0);
               half0_released = true;
             }
           }
 
           if constexpr (E == (int)Epi::FwdStats) {
+            // The stream of this chunk: its 128-column block's parity in the
+            // unit. A group of a split wide tile sees one parity only.
+            if constexpr (!kSplitHalves) {
+              const int par = ((col0 - n_first * tile_n) >> 7) & 1;
+              if (par != cur_par) {
+                const OnlineStat t = sb;
+                sb = sb_other;
+                sb_other = t;
+                cur_par = par;
+              }
+            }
             // y = acc * scale2 (the temperature and log2(e)), folded into
             // the statistics' shift; the label's y is formed on its own. The
             // sum of p^2 is accumulated only when a plane for it was given
@@ -1006,9 +1017,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             ++chunk_ctr;
           }
         }
-        if constexpr (kSplitHalves) {
-          release(static_cast<uint32_t>(grp));
-        } else if constexpr (kMode == kWideMode) {
+        if constexpr (kMode == kWideMode) {
           if (!half0_released) release(0);
           release(1);
         } else {
@@ -1018,10 +1027,9 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
       if (!ok) break;
 
       if constexpr (E == (int)Epi::FwdStats) {
-        // on 256-column tiles sb holds the last tile's stream
-        const bool last_odd = kMode != kWideMode && ((n_count - 1) & 1);
-        OnlineStat all = last_odd ? sb_other : sb;
-        OnlineStat odd = last_odd ? sb : sb_other;
+        // a single group: sb holds the stream of parity cur_par
+        OnlineStat all = cur_par ? sb_other : sb;
+        OnlineStat odd = cur_par ? sb : sb_other;
         if constexpr (kSplitHalves) {
           // Group 1 (the odd blocks) hands its stream to group 0 through one
           // of two shared-memory buffers (in the staging area, which the
@@ -1049,8 +1057,8 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           odd = OnlineStat{xrow[0], xrow[1], xrow[2], xrow[3]};
           const float zl_odd = xrow[4];
           mbar_arrive(xempty_bar(b));  // this thread has read its row
-          // the label's 256-column block decides whose capture holds its logit
-          if (lab >= 0 && ((lab / kBN) & 1)) zl = zl_odd;
+          // the label's 128-column block decides whose capture holds its logit
+          if (lab >= 0 && ((lab >> 7) & 1)) zl = zl_odd;
         }
         if (p.part_q)
           stat_merge<true>(all, odd);
