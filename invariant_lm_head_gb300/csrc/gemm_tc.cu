@@ -13,16 +13,17 @@
 //   warp 1      allocates 512 TMEM columns; one thread issues tcgen05.mma
 //               (M=128, N=256, K=16, four per 64-wide stage) into one of two
 //               256-column accumulators, and tcgen05.commit frees the stage
-//   warps 2..9  epilogue, two groups of four: each thread owns one
-//               accumulator row (its TMEM lane) and reads it 32 columns at a
-//               time with tcgen05.ld; on a wide tile each group drains one
-//               256-column half
-// The epilogue of tile i overlaps the MMAs of tile i+1 (double-buffered TMEM).
-// In the forward and dlogits (K = H) consecutive tiles also overlap in K: a
-// tile's last K blocks alternate with the next tile's first ones in the
-// operand ring, so two independent accumulator chains feed the tensor pipe,
-// and each tile keeps a few blocks to itself while the epilogue drains the
-// other accumulator.
+//   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM
+//               lane) and reads it 32 columns at a time with tcgen05.ld; a
+//               second group (warps 6..9) shares the drain of the forward's
+//               and dlogits' wide tiles
+// On 256-column tiles the epilogue of tile i overlaps the MMAs of tile i+1
+// (double-buffered TMEM), and in the forward and dlogits (K = H) consecutive
+// tiles also overlap in K: a tile's last K blocks alternate with the next
+// tile's first ones in the operand ring, so two independent accumulator
+// chains feed the tensor pipe while each tile keeps a few blocks to itself
+// for the other accumulator's drain. A wide tile's one 512-column
+// accumulator goes back to the MMA issuer in two halves (below).
 //
 // Schedule: the output is cut into units (a row tile, or a pair's two, by one
 // or more column tiles), rastered in groups of row units so that concurrent
@@ -43,9 +44,12 @@
 // tiles: two N=256 pair MMAs per K step into one 512-column accumulator per
 // CTA, two independent chains that share each A stage, so a CTA stages a
 // quarter fewer operand bytes per flop and an operand is re-read half as
-// often. Their epilogue no longer overlaps the next tile; a long K (grad_hidden,
-// grad_weight) hides it, and for the forward and dlogits (K = H) the saved
-// operand traffic outweighs it. Every engine walks K in the same MMA order for
+// often. The accumulator goes back to the MMA issuer in two 256-column
+// halves: the next tile's first N block starts once half 0 has been read
+// (holding its stages for the second block until half 1 is free), and for
+// the forward and dlogits two epilogue groups read half 0 first. A long K
+// (grad_hidden, grad_weight) hides the rest of the drain; for the forward and
+// dlogits (K = H) the saved operand traffic outweighs it. Every engine walks K in the same MMA order for
 // the forward, dlogits and grad_hidden, so their bits do not depend on the
 // engine.
 //
