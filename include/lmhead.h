@@ -34,8 +34,10 @@
  *    buffers of lmhead_logprob_fwd_host. The library never allocates device
  *    memory, and outside the diagnostics that say so it never synchronises or
  *    reads results back: everything is enqueued on `stream` (NULL = legacy
- *    default stream) of the current device. A whole step can therefore be
- *    captured into a CUDA graph once a first call has set up the device.
+ *    default stream) of the current device, or on a stream of the library's
+ *    own that forks from `stream` and joins back into it within the call. A
+ *    whole step can therefore be captured into a CUDA graph once a first call
+ *    has set up the device.
  *  - Return value: LMH_OK, or an error code with nothing launched (argument
  *    errors) or with the launch failing (LMH_ERR_LAUNCH). The message of the
  *    last error of the calling thread is lmhead_last_error_string().
@@ -79,6 +81,19 @@
  *    LMH_GEMM_GRID_CAP=n runs every contraction on at most n CTAs (or CTA
  *    pairs). LMH_GEMM_INTERLEAVE=0 (a diagnostic) stops the forward and
  *    dlogits from overlapping consecutive tiles' K loops; bits are the same.
+ *  - The backward of a row chunk of up to 1024 rows runs grad_hidden beside
+ *    grad_weight: grad_hidden on a second stream that the library keeps per
+ *    device, forked from `stream` after dlogits and joined back before the
+ *    call returns (an event record and a stream wait each way, so the call
+ *    stays ordered on `stream` as a whole, and stream capture records the
+ *    two as parallel branches). grad_hidden then takes an engine that leaves
+ *    at least half the SMs free when one costs at most twice the fastest
+ *    (its bits do not change), and grad_weight runs on wide pairs whose CTAs
+ *    claim their tiles as SMs come free (deterministic; its summation order
+ *    is that of the wide pairs, not of the 256-wide pairs it takes alone).
+ *    Concurrent backward calls from several host threads on one device take
+ *    turns while enqueuing. LMH_BWD_OVERLAP (a diagnostic, read once per
+ *    process) forces it off ("0") or on for every chunk ("1").
  */
 #ifndef LMHEAD_H
 #define LMHEAD_H
@@ -115,7 +130,7 @@ struct CUstream_st; /* cudaStream_t */
  * row, a bf16 dlogits buffer of min(T, 16384) x V, a bf16 transpose of one
  * 16384-row chunk of hidden (H x min(T, 16384)) and the fp32 partials of one
  * chunk's grad_hidden, one per half of the vocabulary (2 x min(T, 16384) x H,
- * rows rounded up to 128).
+ * rows rounded up to 128), and a second 4-byte tile counter.
  */
 size_t lmhead_workspace_size(int op, int64_t T, int64_t H, int64_t V);
 

@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <atomic>
 #include <mutex>
@@ -195,6 +196,7 @@ struct BwdWs {
   uint16_t* dl;  // [Tc][Vpad] bf16 dlogits of one row chunk
   uint16_t* ht;  // [H][Tcpad] bf16 transpose of one row chunk of hidden
   float* ghp;    // [2][ghp_rows][H] fp32 partials of grad_hidden, one per K segment
+  unsigned* sched2;  // grad_hidden's unit counter when it runs beside grad_weight
   int64_t vpad, tc, tcpad, ghp_rows;
 };
 
@@ -212,6 +214,7 @@ BwdWs carve_bwd(Carver& c, int64_t T, int64_t H, int64_t V,
   w.ht = c.take<uint16_t>(H * w.tcpad);
   w.ghp_rows = round_up(w.tc, lmh::kBM);
   w.ghp = c.take<float>(2 * w.ghp_rows * H);
+  w.sched2 = c.take<unsigned>(1);
   return w;
 }
 
@@ -479,6 +482,80 @@ struct BwdOpts {
 //                          into grad_hidden_f32 (a vocab shard's partial)
 //   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
 //   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
+// ------------------------------------------------------------ backward side stream
+// Per device: a second stream of the library's own (non-blocking, created on
+// first use) and two events. The backward runs grad_hidden on it beside
+// grad_weight: both read the chunk's dl and write different outputs. Fork and
+// join are an event record plus a stream wait each way, so under stream
+// capture the two become parallel branches of the graph. The mutex keeps one
+// call's records and waits together when several host threads call at once.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+SideStream g_side[kMaxDevices];
+
+int side_stream_init(SideStream& sd) {
+  cudaError_t e = cudaSuccess;
+  if (!sd.st && (e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaStreamCreate: %s", cudaGetErrorString(e));
+  if (!sd.fork && (e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
+  if (!sd.join && (e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
+  return LMH_OK;
+}
+
+// One fork of the side stream from `main`; the destructor joins a fork that
+// an error left open, so `main` never runs ahead of the side stream's work.
+struct SideBranch {
+  SideStream* sd;
+  cudaStream_t main;
+  bool open = false;
+  int fork() {
+    cudaError_t e;
+    if ((e = cudaEventRecord(sd->fork, main)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(sd->st, sd->fork, 0)) != cudaSuccess)
+      return fail(LMH_ERR_LAUNCH, "side stream fork: %s", cudaGetErrorString(e));
+    open = true;
+    return LMH_OK;
+  }
+  int join() {
+    open = false;
+    cudaError_t e;
+    if ((e = cudaEventRecord(sd->join, sd->st)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(main, sd->join, 0)) != cudaSuccess)
+      return fail(LMH_ERR_LAUNCH, "side stream join: %s", cudaGetErrorString(e));
+    return LMH_OK;
+  }
+  ~SideBranch() {
+    if (open && cudaEventRecord(sd->join, sd->st) == cudaSuccess)
+      cudaStreamWaitEvent(main, sd->join, 0);
+  }
+};
+
+// Row chunks up to this many rows run grad_hidden beside grad_weight. Alone
+// at H = 3584, V = 152064, whole backward, one after the other / side by side
+// (ms): 128 rows 0.935 / 0.743, 512 1.214 / 1.130, 1024 2.001 / 1.921, 2048
+// 3.745 / 3.68, 4096 7.03 / 7.00, 16384 28.9 / 29.3; inside a long run at the
+// power cap: 128 rows 1.065 / 0.785, 512 1.198 / 1.137, 1024 2.165 / 2.171,
+// 2048 4.109 / 4.188. From 2048 rows grad_hidden spans more than one wave,
+// and grad_weight then only fills its tail while disturbing its reads.
+constexpr int64_t kBwdOverlapMaxRows = 1024;
+
+// LMH_BWD_OVERLAP, read once (a diagnostic): "0" runs grad_hidden and
+// grad_weight one after the other, "1" side by side; -1 when unset.
+int bwd_overlap_mode() {
+  static const int mode = [] {
+    const char* v = std::getenv("LMH_BWD_OVERLAP");
+    if (v && v[0] == '0') return 0;
+    if (v && v[0] == '1') return 1;
+    return -1;
+  }();
+  return mode;
+}
+
 int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                  const float* grad_lp, const float* grad_ent, const float* lse, const float* ent,
                  int64_t T, int64_t H, int64_t V, float s, uint16_t* grad_hidden,
@@ -526,6 +603,25 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   LMH_TRY(device_info(&dev));
   Carver c{static_cast<char*>(workspace)};
   const BwdWs w = carve_bwd(c, T, H, V, o.row_chunk);
+  // grad_hidden beside grad_weight, on the side stream, for chunks of up to
+  // kBwdOverlapMaxRows rows (LMH_BWD_OVERLAP forces it off or on)
+  const int ov_mode = bwd_overlap_mode();
+  auto overlap_for = [&](int64_t rows) {
+    return ov_mode == 1 || (ov_mode < 0 && rows <= kBwdOverlapMaxRows);
+  };
+  const int64_t first_rows = T < o.row_chunk ? T : o.row_chunk;
+  const int64_t last_rows = T % o.row_chunk == 0 ? first_rows : T % o.row_chunk;
+  // The side stream is set up by every backward call, used or not, so that a
+  // later call under stream capture creates nothing.
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);  // in range: device_info accepted it
+  SideStream* side = &g_side[dev_id];
+  std::unique_lock<std::mutex> side_lock(side->mu);
+  LMH_TRY(side_stream_init(*side));
+  if (!overlap_for(first_rows) && !overlap_for(last_rows)) {
+    side_lock.unlock();
+    side = nullptr;
+  }
 
   if (!lse || (grad_ent && !ent)) {
     LMH_TRY(run_forward(*dev, hidden, weight, labels, T, H, V, s, w.lp, w.ent, w.lse, w.fwd, st));
@@ -575,9 +671,17 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     // order, then bf16(P0 + P1) (one K block: P0 alone). The split depends on
     // V only, so every row and every batch gets the same association; it
     // gives a short batch two independent MMA chains on two SMs per tile.
+    const bool beside = side && overlap_for(rows);
+    SideBranch branch{side, st};
+    cudaStream_t gs = st;  // grad_hidden's stream
+    if (beside) {
+      LMH_TRY(branch.fork());
+      gs = side->st;
+    }
     lmh::GemmParams q{};
     q.status = dev->status;
-    q.sched = w.fwd.sched;
+    q.sched = beside ? w.sched2 : w.fwd.sched;
+    q.corun = beside ? 1 : 0;
     q.M = static_cast<int>(rows);
     q.N = static_cast<int>(H);
     q.K = static_cast<int>(V);
@@ -588,19 +692,19 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
       q.seg_rows = static_cast<int>(w.ghp_rows);
       CUtensorMap o_ghp;
       LMH_TRY(make_out_tmap(&o_ghp, w.ghp, H, 2 * w.ghp_rows, H * 4, true));
-      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
-                 lmh::launch_gemm(lmh::Epi::StoreF32, t_dl, t_w_mn, q, 1, dev->sms, st, &o_ghp),
+      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, gs,
+                 lmh::launch_gemm(lmh::Epi::StoreF32, t_dl, t_w_mn, q, 1, dev->sms, gs, &o_ghp),
                  "grad_hidden");
       void* gh_out = grad_hidden_f32 ? static_cast<void*>(grad_hidden_f32 + c0 * H)
                                      : static_cast<void*>(grad_hidden + c0 * H);
-      LMH_LAUNCH(lmh::K_DHIDDEN_SUM, st,
+      LMH_LAUNCH(lmh::K_DHIDDEN_SUM, gs,
                  lmh::launch_sum_parts(w.ghp, 2, w.ghp_rows * H, rows * H, gh_out,
-                                       grad_hidden_f32 == nullptr, dev->sms, st),
+                                       grad_hidden_f32 == nullptr, dev->sms, gs),
                  "grad_hidden segments");
     } else {
-      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, st,
+      LMH_LAUNCH(lmh::K_DHIDDEN_GEMM, gs,
                  lmh::launch_gemm(grad_hidden_f32 ? lmh::Epi::StoreF32 : lmh::Epi::StoreBf16,
-                                  t_dl, t_w_mn, q, 1, dev->sms, st, &o_gh),
+                                  t_dl, t_w_mn, q, 1, dev->sms, gs, &o_gh),
                  "grad_hidden");
     }
 
@@ -618,9 +722,17 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
     r.a_mn = 0;
     r.b_mn = 1;
     r.accumulate = c0 > 0 ? 1 : 0;  // later chunks: TMA reduce-add into grad_weight
+    // Beside grad_hidden, grad_weight's CTAs start as SMs come free: claimed
+    // units let the early ones take the work of those that start late. It
+    // also takes wide pairs then, which changes its summation order (and so
+    // its bits) against the run alone on 256-wide pairs.
+    r.claim = beside ? 1 : 0;
+    r.corun = beside ? 1 : 0;
     LMH_LAUNCH(lmh::K_DWEIGHT_GEMM, st,
                lmh::launch_gemm(lmh::Epi::StoreF32T, t_ht, t_dl_mn, r, 1, dev->sms, st, &o_gw),
                "grad_weight");
+    // the next chunk overwrites dl and the partials
+    if (beside) LMH_TRY(branch.join());
   }
   return ok();
 }

@@ -1249,6 +1249,17 @@ double engine_cost(const Engine& g, long long m_tiles, long long n, int num_sms,
   return static_cast<double>(waves) * wave / segs;
 }
 
+// CTAs that a launch of engine g keeps busy: one per unit (two per pair
+// unit), at most one wave.
+long long engine_ctas(const Engine& g, long long m_tiles, long long n, int num_sms, int slots,
+                      int segs = 1) {
+  const long long rows = g.mode == kSingle ? 1 : 2;
+  const long long m_units = (m_tiles + rows - 1) / rows;
+  const long long units = m_units * ((n + g.tile_n - 1) / g.tile_n) * segs;
+  const long long lanes = g.mode == kSingle ? num_sms : slots;
+  return (units < lanes ? units : lanes) * rows;
+}
+
 template <int E>
 cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                           GemmParams p, int tiles_per_unit, int num_sms, cudaStream_t stream) {
@@ -1285,8 +1296,11 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
     // output's stores to matter; wide pairs from 2048 rows. Alone at H =
     // 3584, V = 152064 (ms, pairs / wide): 0.34 / 0.36 at 128 rows, 0.44 /
     // 0.54 at 512, 0.69 / 0.79 at 1024, 1.29 / 1.28 at 2048, 2.62 / 2.50 at
-    // 4096, 5.47 / 5.01 at 8192.
-    if (m_tiles >= 2) g = p.K < 2048 ? Engine{kPairMode, kBN} : Engine{kWideMode, 2 * kBN};
+    // 4096, 5.47 / 5.01 at 8192. Beside grad_hidden (corun) wide pairs
+    // again: whole backward 0.741 / 0.737 ms at 128 rows, 1.154 / 1.131 at
+    // 512, 1.960 / 1.931 at 1024.
+    if (m_tiles >= 2)
+      g = (p.K < 2048 && !p.corun) ? Engine{kPairMode, kBN} : Engine{kWideMode, 2 * kBN};
   } else if (env < 0 && kStoreEpi<E>) {
     // grad_hidden and the bare engine GEMM: the cheapest engine by
     // engine_cost (pairs only over two or more m tiles). Narrower tiles need
@@ -1298,16 +1312,29 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
                             {kPairMode, 128},     {kSingle, 192},  {kSingle, 128},
                             {kSingle, 64}};
     const int n_cand = p.b_mn ? 7 : 3;
-    double best = 1e30;
+    const int segs = p.k_split > 0 ? 2 : 1;
+    double best = 1e30, best_half = 1e30;
+    Engine half = g;
     for (int i = 0; i < n_cand; ++i) {
       const int slots = cand[i].mode == kWideMode ? wide_slots : pair_slots_n;
-      const double cost =
-          engine_cost(cand[i], m_tiles, p.N, num_sms, slots, p.k_split > 0 ? 2 : 1);
+      const double cost = engine_cost(cand[i], m_tiles, p.N, num_sms, slots, segs);
       if (cost < best * 0.999) {
         best = cost;
         g = cand[i];
       }
+      if (cost < best_half * 0.999 &&
+          2 * engine_ctas(cand[i], m_tiles, p.N, num_sms, slots, segs) <= num_sms) {
+        best_half = cost;
+        half = cand[i];
+      }
     }
+    // Beside grad_weight (corun), grad_hidden of a short batch gives up some
+    // speed for SMs: alone at H = 3584, V = 152064, whole backward with the
+    // two side by side (ms): 128 rows, 64-column tiles on 112 CTAs 0.826,
+    // 128-column on 56 CTAs 0.766; 512 rows, 256-wide pairs on 112 SMs 1.185,
+    // wide pairs on 56 SMs 1.101 (alone the wide pairs take 0.644 ms against
+    // 0.418).
+    if (p.corun && best_half <= 2.0 * best) g = half;
   } else if (env < 0 && (E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && m_tiles >= 2 &&
              (m_tiles % 2 == 0 || m_tiles > 32)) {
     g = Engine{kWideMode, 2 * kBN};
@@ -1382,8 +1409,8 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   int lanes = g.mode == kSingle ? num_sms : slots_for<E>(g.mode, num_sms);
   if (grid_cap > 0 && grid_cap < lanes) lanes = grid_cap;
   const bool claim_by_default =
-      p.n_units >= static_cast<long long>(kDynamicMinWaves) * lanes &&
-      !(E == (int)Epi::StoreF32T && p.K < kDynamicMinGradWeightK);
+      p.claim != 0 || (p.n_units >= static_cast<long long>(kDynamicMinWaves) * lanes &&
+                       !(E == (int)Epi::StoreF32T && p.K < kDynamicMinGradWeightK));
   p.dynamic =
       (p.sched != nullptr && (sched_mode == 1 || (sched_mode < 0 && claim_by_default))) ? 1 : 0;
   if (p.dynamic) {

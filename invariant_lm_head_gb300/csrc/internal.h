@@ -75,6 +75,13 @@ struct GemmParams {
   // of walking a fixed stride. A unit's arithmetic is the same either way.
   unsigned* sched;
   int dynamic;
+  // Host hints for a launch that shares the GPU with another. claim: claim
+  // units whatever the wave count (its CTAs start as SMs come free). corun:
+  // grad_hidden (and the bare engine GEMM) leaves at least half the SMs to
+  // the other launch when an engine that does so costs at most twice the
+  // cheapest; grad_weight takes wide pairs whatever its K.
+  int claim;
+  int corun;
   // K blocks by which consecutive tiles overlap (set by launch_gemm; 0 = none):
   // a tile's last `interleave` blocks alternate with the next tile's first.
   int interleave;

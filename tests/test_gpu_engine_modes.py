@@ -190,3 +190,74 @@ def test_overlapped_tiles_give_identical_bits(tmp_path, single, pairs):
     assert on.keys() == off.keys()
     for k in on:
         assert _same(on[k], off[k]), f"{k}: overlapping the tiles changed bits"
+
+
+# grad_hidden and grad_weight of a row chunk may run side by side, grad_hidden
+# on a second stream of the library's own (LMH_BWD_OVERLAP forces it off or
+# on), over one chunk and over seven 128-row chunks, where the next chunk's
+# dlogits must wait for the side stream before it overwrites dl and
+# grad_weight's reduce-adds must keep chunk order. grad_hidden keeps its bits.
+# Side by side, grad_weight runs on wide pairs, whose summation order differs
+# from the 256-wide pairs it takes alone: with every store contraction forced
+# onto wide pairs the two modes must agree bit for bit, and by default each
+# mode must repeat its own bits and agree with the other to fp32 rounding. A
+# grid cap makes grad_weight claim several units per CTA meanwhile.
+CHILD_CHUNKS = r'''
+import sys
+import torch
+sys.path.insert(0, sys.argv[2])
+import workloads as W
+import invariant_lm_head_gb300 as lmh
+
+lmh.build()
+dev = torch.device("cuda:0")
+out = {}
+for (T, H, V, s) in [(777, 520, 3001, 1 / 0.7), (300, 264, 517, 2.0)]:
+    hidden = W.as_torch_bf16(W.random_bf16(T, (T, H), 1.0)).to(dev)
+    weight = W.as_torch_bf16(W.random_bf16(T + 1, (V, H), 0.05)).to(dev)
+    labels = torch.from_numpy(W.random_labels(T, T, V)).to(dev)
+    grad = torch.from_numpy(W.random_f32(T, T)).to(dev)
+    grad_e = torch.from_numpy(W.random_f32(T + 2, T)).to(dev)
+    _, ent, lse = lmh.lmhead_logprob_fwd(hidden, weight, labels, s, want_lse=True)
+    for rep in range(3):
+        gh, gw = lmh.lmhead_logprob_bwd(hidden, weight, labels, grad, s, lse=lse)
+        gh_c, gw_c = lmh.lmhead_logprob_bwd_chunked(hidden, weight, labels, grad, s, row_chunk=128,
+                                                    grad_entropy=grad_e, lse=lse, entropy=ent)
+        for k, v in dict(gh=gh, gw=gw, gh_c=gh_c, gw_c=gw_c).items():
+            out[f"{T}_{k}_{rep}"] = v.cpu()
+torch.cuda.synchronize()
+assert lmh.lmhead_device_status() == 0
+torch.save(out, sys.argv[1])
+'''
+
+
+@pytest.mark.parametrize("engine", ["", "w"])
+@pytest.mark.parametrize("cap", ["", "4"])
+def test_grad_hidden_beside_grad_weight(tmp_path, engine, cap):
+    import torch
+
+    child = tmp_path / "chunks.py"
+    child.write_text(CHILD_CHUNKS)
+    res = {}
+    for mode in ("0", "1"):
+        path = tmp_path / f"ov{mode}.pt"
+        env = dict(os.environ, LMH_BWD_OVERLAP=mode)
+        if cap:
+            env["LMH_GEMM_GRID_CAP"] = cap
+        if engine:
+            env["LMH_GEMM_STORE_ENGINE"] = engine
+        r = subprocess.run([sys.executable, str(child), str(path), ROOT], env=env, cwd=ROOT,
+                           capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0, r.stderr[-2000:]
+        res[mode] = torch.load(path)
+    assert res["0"].keys() == res["1"].keys()
+    for k in res["0"]:
+        base = k.rsplit("_", 1)[0] + "_0"
+        for mode in ("0", "1"):
+            assert _same(res[mode][k], res[mode][base]), f"{k}: repeats differ (mode {mode})"
+        a, b = res["0"][k], res["1"][k]
+        if engine or "_gh" in k:
+            assert _same(a, b), f"{k}: running grad_hidden beside grad_weight changed bits"
+        else:
+            err = (a.double() - b.double()).norm() / a.double().norm()
+            assert err < 1e-5, f"{k}: side by side, grad_weight moved by {float(err):.2e}"
