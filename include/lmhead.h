@@ -81,6 +81,10 @@
  *    LMH_GEMM_GRID_CAP=n runs every contraction on at most n CTAs (or CTA
  *    pairs). LMH_GEMM_INTERLEAVE=0 (a diagnostic) stops the forward and
  *    dlogits from overlapping consecutive tiles' K loops; bits are the same.
+ *    LMH_GEMM_WIDE_SKEW=n (a diagnostic) sets how many K blocks at the end of
+ *    a wide tile run its first 256 columns ahead of the second (default 3,
+ *    at most the operand ring less one; 0 runs the two together to the
+ *    end); bits are the same.
  *  - The backward of a row chunk of up to 1024 rows runs grad_hidden beside
  *    grad_weight: grad_hidden on a second stream that the library keeps per
  *    device, forked from `stream` after dlogits and joined back before the

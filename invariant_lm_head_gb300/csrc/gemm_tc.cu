@@ -47,11 +47,13 @@
 // often. The accumulator goes back to the MMA issuer in two 256-column
 // halves: the next tile's first N block starts once half 0 has been read
 // (holding its stages for the second block until half 1 is free), and for
-// the forward and dlogits two epilogue groups read half 0 first. A long K
+// the forward and dlogits two epilogue groups read half 0 first. The halves
+// also reach the epilogue one after the other: a tile's last few K blocks run
+// N block 0 first, so half 0 drains while block 1 finishes. A long K
 // (grad_hidden, grad_weight) hides the rest of the drain; for the forward and
-// dlogits (K = H) the saved operand traffic outweighs it. Every engine walks K in the same MMA order for
-// the forward, dlogits and grad_hidden, so their bits do not depend on the
-// engine.
+// dlogits (K = H) the saved operand traffic outweighs it. Every engine walks
+// K in the same MMA order for the forward, dlogits and grad_hidden, so their
+// bits do not depend on the engine.
 //
 // Narrow tiles: single CTAs and pairs also take tiles of fewer columns (64,
 // 128 or 192 alone, 128 in a pair; MN-major B only), so a short grad_hidden
@@ -146,8 +148,9 @@ struct Ring {
   // full and empty per stage, two accumulator pairs, final, the unit ring's
   // slots, the forward's two exchange buffers' full and empty; then the TMEM
   // address, the abort flag, the peer's load count, two go flags and two unit
-  // words per epilogue group, two exchange go flags and the unit ring
-  static_assert(8 * (2 * kMaxStages + 5 + kUnitSlots + 4) + 4 * (13 + kUnitSlots) <=
+  // words per epilogue group, two exchange go flags, the unit ring and two
+  // second-half go flags per epilogue group
+  static_assert(8 * (2 * kMaxStages + 5 + kUnitSlots + 4) + 4 * (13 + kUnitSlots + 4) <=
                     kBarrierBytes,
                 "barrier area too small");
 };
@@ -287,6 +290,7 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
   volatile int* epi_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);   // [group][2]
   volatile int* x_go = reinterpret_cast<volatile int*>(tmem_slot + 11);      // [group]
   volatile int* uring = reinterpret_cast<volatile int*>(tmem_slot + 13);     // [kUnitSlots]
+  volatile int* epi_go1 = reinterpret_cast<volatile int*>(tmem_slot + 13 + kUnitSlots);  // [group][2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -659,14 +663,25 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           tc_commit(empty_bar(st));
       };
       // Wide tiles: the epilogue releases the accumulator's two 256-column
-      // halves one after the other (tempty 0, then 1). A tile's N block 0
-      // starts as soon as half 0 is free; while half 1 is still being
-      // drained, its stages are held after block 0's MMAs (at most the ring
-      // less one) and block 1 catches up on them once half 1 is free.
+      // halves one after the other (tempty 0, then 1), and each half is handed
+      // to it on its own (tfull 0, then 1). A tile's N block 0 starts as soon
+      // as half 0 is free; while half 1 is still being drained, its stages
+      // are held after block 0's MMAs (at most the whole ring) and block 1
+      // catches up on them once half 1 is free. A tile's last `skew` K blocks
+      // also run block 0 first, their stages held: half 0 is handed over while
+      // block 1's last MMAs run, so its drain overlaps them. Each chain keeps
+      // its K order, so no value depends on it.
+      const int skew = min(p.wide_skew, static_cast<int>(n_st) - 1);
       bool half1_free = false;
       int n_held = 0;
       uint32_t held_stage[kMaxStages];
       int held_block[kMaxStages];
+      auto commit_half = [&](int h) {
+        if constexpr (kPair)
+          tc_commit_pair(tfull_bar(h), 0x3);
+        else
+          tc_commit(tfull_bar(h));
+      };
       auto wide_stage = [&](const WalkTile& t, int i) -> bool {
         const uint32_t aph = static_cast<uint32_t>(t.idx) & 1u;
         if (i == 0) {
@@ -677,53 +692,50 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
         }
         if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) return false;
         tc_fence_after();
-        if (half1_free) {  // steady state: both chains, interleaved
+        const bool last = i == t.kb_n - 1;
+        const bool tail = i >= t.kb_n - skew;
+        if (half1_free && !tail) {  // steady state: both chains, interleaved
           issue_both(stage, i);
           free_stage(stage);
           if (++stage == n_st) {
             stage = 0;
             phase ^= 1u;
           }
-          if (i == t.kb_n - 1) {
-            if constexpr (kPair)
-              tc_commit_pair(tfull_bar(0), 0x3);
-            else
-              tc_commit(tfull_bar(0));
+          if (last) {
+            commit_half(0);
+            commit_half(1);
           }
           return true;
         }
-        // half 1 still draining: N block 0 alone, the stage held for block 1
+        // N block 0 alone, the stage held for block 1
         issue_chain(stage, i, 0, tmem_base);
-        if (mbar_try_wait(tempty_bar(1), aph ^ 1u)) {
-          half1_free = true;
-        } else if (n_held + 1 >= static_cast<int>(n_st) || i == t.kb_n - 1) {
-          if (!mbar_wait(tempty_bar(1), aph ^ 1u, abort_flag, p.status)) return false;
-          half1_free = true;
+        held_stage[n_held] = stage;
+        held_block[n_held] = i;
+        ++n_held;
+        if (++stage == n_st) {
+          stage = 0;
+          phase ^= 1u;
         }
-        if (half1_free) tc_fence_after();
-        if (half1_free) {
+        if (last) commit_half(0);
+        // block 1 must catch up at the tile's end, or when every stage is held
+        const bool must = last || n_held >= static_cast<int>(n_st);
+        if (!half1_free) {
+          if (mbar_try_wait(tempty_bar(1), aph ^ 1u)) {
+            half1_free = true;
+          } else if (must) {
+            if (!mbar_wait(tempty_bar(1), aph ^ 1u, abort_flag, p.status)) return false;
+            half1_free = true;
+          }
+          if (half1_free) tc_fence_after();
+        }
+        if (half1_free && (!tail || must)) {
           for (int h = 0; h < n_held; ++h) {
             issue_chain(held_stage[h], held_block[h], 1, tmem_base + kBN);
             free_stage(held_stage[h]);
           }
           n_held = 0;
-          issue_chain(stage, i, 1, tmem_base + kBN);
-          free_stage(stage);
-        } else {
-          held_stage[n_held] = stage;
-          held_block[n_held] = i;
-          ++n_held;
         }
-        if (++stage == n_st) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (i == t.kb_n - 1) {
-          if constexpr (kPair)
-            tc_commit_pair(tfull_bar(0), 0x3);
-          else
-            tc_commit(tfull_bar(0));
-        }
+        if (last) commit_half(1);
         return true;
       };
       // One K block of tile t: its accumulator is t.idx % kAccs; the first
@@ -878,6 +890,17 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
             mbar_arrive(tempty_bar(bar));
         };
         bool half0_released = false;
+        bool half1_handed = false;  // this tile's tfull(1) has been waited for
+        // wait (the group's thread 0, bounded) for half 1's hand-over
+        auto wait_half1 = [&]() -> bool {
+          volatile int* go1 = epi_go1 + grp * 2;
+          if (gtid == 0) go1[it & 1u] = mbar_wait(tfull_bar(1), aph, abort_flag, p.status) ? 1 : 0;
+          named_barrier(grp_bar, 128);
+          half1_handed = true;
+          if (!go1[it & 1u]) return false;
+          tc_fence_after();
+          return true;
+        };
         // the forward's stream: on 256-column tiles the tile's block parity
         // in the unit (a unit starts on a block), on a wide tile the group's
         // own (half g of tile j is block 2j + g)
@@ -892,6 +915,13 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           // (Staging such a tile without storing it let its chunks overwrite
           // a buffer that the last live store was still reading.)
           if (E != (int)Epi::FwdStats && !tile_live) break;
+          if constexpr (kMode == kWideMode) {
+            // half 1 is handed over on its own, after half 0
+            if ((kSplitHalves ? ci == 4 : c == kBN / 32) && !wait_half1()) {
+              ok = false;
+              break;
+            }
+          }
           const int nvalid = min(32, p.N - col0);
           float v[32];
           tmem_ld32(taddr + c * 32, v);
@@ -1022,11 +1052,19 @@ __device__ __forceinline__ void gemm_body(const CUtensorMap& tmA, const CUtensor
           }
         }
         if constexpr (kMode == kWideMode) {
+          // Half 1 goes back only after its own hand-over, read or not. A
+          // group that read none of it (a pair half past the last row, or
+          // columns past N) could otherwise reach the next tile, whose half 0
+          // may be handed over before this tile's half 1 is free, and arrive
+          // on tempty 1 again before its peer CTA arrived for this tile: the
+          // two arrivals would complete the phase while the peer still reads.
+          if (ok && !half1_handed && !wait_half1()) ok = false;
           if (!half0_released) release(0);
           release(1);
         } else {
           release(acc);
         }
+        if (!ok) break;
       }
       if (!ok) break;
 
@@ -1425,6 +1463,7 @@ cudaError_t launch_gemm_e(const CUtensorMap& a, const CUtensorMap& b, const CUte
   // 10.11 / 11.26, 11.19; 8: 9.90, 10.14 / 10.99, 11.11; 12: 10.25, 10.13 /
   // 10.95, 11.00; 16: 10.21, 10.04 / 11.03, 11.11; 24: 10.30, 10.23 / 11.16,
   // 11.04. At V = 32000 the tensor pipe went from 76 % to 78-79 % busy.
+  p.wide_skew = g.mode == kWideMode ? gemm_wide_skew() : 0;
   p.interleave = 0;
   if ((E == (int)Epi::FwdStats || E == (int)Epi::DLogits) && g.mode != kWideMode &&
       p.k_split == 0 && gemm_interleave_enabled()) {
@@ -1488,6 +1527,16 @@ void gemm_schedule(int* schedule, int* grid_cap) {
   }();
   *schedule = forced;
   *grid_cap = cap;
+}
+
+int gemm_wide_skew() {
+  static const int skew = [] {
+    const char* v = std::getenv("LMH_GEMM_WIDE_SKEW");
+    if (!v || !*v) return kWideSkewBlocks;
+    const int n = std::atoi(v);
+    return n < 0 ? 0 : (n > kMaxStages ? kMaxStages : n);
+  }();
+  return skew;
 }
 
 bool gemm_interleave_enabled() {

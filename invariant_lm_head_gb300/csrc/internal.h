@@ -85,6 +85,9 @@ struct GemmParams {
   // K blocks by which consecutive tiles overlap (set by launch_gemm; 0 = none):
   // a tile's last `interleave` blocks alternate with the next tile's first.
   int interleave;
+  // Wide tiles: K blocks at a tile's end that run N block 0 before block 1
+  // (set by launch_gemm; capped by the ring), so that half 0 drains early.
+  int wide_skew;
   unsigned* status;
   // FwdStats / DLogits
   float scale2;    // inv_temperature * log2(e)
@@ -187,6 +190,10 @@ void gemm_schedule(int* schedule, int* grid_cap);
 // how many K blocks each tile then runs alone.
 bool gemm_interleave_enabled();
 constexpr int kSoloBlocks = 10;
+// K blocks at a wide tile's end that run N block 0 first (LMH_GEMM_WIDE_SKEW,
+// read once, overrides it: a diagnostic; 0 runs both blocks to the end).
+constexpr int kWideSkewBlocks = 3;
+int gemm_wide_skew();
 // A launch of at least this many waves of units claims them dynamically
 // (grad_weight only from this many rows of K).
 constexpr int kDynamicMinWaves = 4;
