@@ -66,3 +66,25 @@ def test_traffic_lookup_ignores_stale_counters(tmp_path, monkeypatch):
     (tmp_path / "b.cu").write_text("changed")
     assert bench.traffic_for("k") is None
     assert bench.sources_sha(["a.cu", "missing.cu"]) is None
+
+
+def test_backward_rooflines():
+    # the joint bound of a backward whose kernels may overlap: the three
+    # GEMMs' 6THV flops at the tensor peak or their algorithmic bytes at HBM
+    # speed, whichever is longer; never above the serial sum of per-kernel
+    # bounds, and equal to the flop term once the batch is compute-bound
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}
+    H, V = 3584, 152064
+    for T in (1, 128, 512, 2048, 16384):
+        joint = bench.bwd_joint_roofline_ms(T, H, V, peaks)
+        serial = sum(bench.bwd_roofline_ms(T, H, V, peaks).values())
+        flop_ms = 6.0 * T * H * V / 2000e12 * 1e3
+        byte_ms = (2.0 * V * H * 2 + 4.0 * V * H + 6.0 * T * H + 6.0 * T * V) / 8000e9 * 1e3
+        assert joint == pytest.approx(max(flop_ms, byte_ms), rel=1e-12)
+        assert joint <= serial * (1 + 1e-12)
+    # one row: all bytes (W read twice, grad_weight written in fp32)
+    assert bench.bwd_joint_roofline_ms(1, H, V, peaks) == pytest.approx(
+        (8.0 * V * H + 6.0 * H + 6.0 * V) / 8000e9 * 1e3, rel=1e-12)
+    # a long batch: all flops
+    assert bench.bwd_joint_roofline_ms(16384, H, V, peaks) == pytest.approx(
+        6.0 * 16384 * H * V / 2000e12 * 1e3, rel=1e-12)

@@ -261,3 +261,15 @@ def test_grad_hidden_beside_grad_weight(tmp_path, engine, cap):
         else:
             err = (a.double() - b.double()).norm() / a.double().norm()
             assert err < 1e-5, f"{k}: side by side, grad_weight moved by {float(err):.2e}"
+
+
+# A wide tile's last K blocks run its first 256 columns ahead of the second
+# (LMH_GEMM_WIDE_SKEW; 0 runs the two together to the end). Each chain keeps
+# its K order, so with every contraction on wide pairs no output may change a
+# bit, grad_weight included (same engine, same waves).
+def test_skewed_tile_ends_give_identical_bits(tmp_path):
+    on = _run(tmp_path, "skew_on", {"LMH_GEMM_CTA_PAIRS": "1"})
+    off = _run(tmp_path, "skew_off", {"LMH_GEMM_CTA_PAIRS": "1", "LMH_GEMM_WIDE_SKEW": "0"})
+    assert on.keys() == off.keys()
+    for k in on:
+        assert _same(on[k], off[k]), f"{k}: the skewed tile ends changed bits"
