@@ -321,15 +321,78 @@ def make_inputs(T, H, V, seed, dev):
     return hidden, weight, labels, grad
 
 
-def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
+def invariance_cases(run, T, subs, window=1024, shifts=(1, 63, 127), seeds=(11, 12, 13),
+                     embed=4096, dev=None):
+    """Bit-mismatch counts of a row-wise result under re-batching. run(rows)
+    computes it on exactly these rows (an index tensor, in that order) and
+    returns its per-row outputs; each case is compared with the whole batch's
+    rows, in fp32 or bf16 bits. The cases: sub-batches ((size, starts) pairs),
+    windows of `window` rows shifted by 1..127, shuffled packings of the
+    whole batch, and the batch as the first T rows of a larger one (rows on
+    `dev`, the current CUDA device by default)."""
     import torch
 
     def bits(t):
-        return t.view(torch.int32)
+        return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
 
-    lmh.lmhead_logprob_fwd(hidden, weight, labels, s, out_logprob=lp, out_entropy=ent, out_lse=lse)
-    full = [x.clone() for x in (lp, ent, lse)]
+    if dev is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    full = [x.clone() for x in run(torch.arange(T, device=dev))]
+    out = {"rows_compared": 0, "mismatched_values": 0, "cases": []}
+
+    def compare(rows, part):
+        n = sum(int((bits(a[:rows.numel()]) != bits(b[rows])).sum().item())
+                for a, b in zip(part, full))
+        out["rows_compared"] += int(rows.numel())
+        out["mismatched_values"] += n
+        return n
+
+    for bs, starts in subs:
+        for r0 in starts:
+            rows = torch.arange(r0, r0 + bs, device=dev)
+            out["cases"].append({"batch": bs, "start": r0, "mismatched": compare(rows, run(rows))})
+    for shift in shifts:
+        rows = torch.arange(shift, min(T, shift + window), device=dev)
+        out["cases"].append({"batch": int(rows.numel()), "shift": shift,
+                             "mismatched": compare(rows, run(rows))})
+    for seed in seeds:
+        perm = torch.randperm(T, generator=torch.Generator().manual_seed(seed)).to(dev)
+        out["cases"].append({"batch": T, "shuffled": seed, "mismatched": compare(perm, run(perm))})
+    if embed:
+        rows = torch.arange(T, device=dev)
+        bigger = torch.cat([rows, torch.arange(0, min(T, embed), device=dev)])
+        out["cases"].append({"batch": int(bigger.numel()), "embedded_rows": T,
+                             "mismatched": compare(rows, run(bigger))})
+    return out
+
+
+def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
+    """The fused forward's invariance cases on the main workload."""
     T = hidden.shape[0]
+
+    def run(rows):
+        return lmh.lmhead_logprob_fwd(hidden[rows].contiguous(), weight, labels[rows].contiguous(),
+                                      s, want_lse=True)
+
+    return invariance_cases(run, T, ((1, (0, 1, T - 1)), (7, (0, 4093)), (256, (0, 8000))))
+
+
+def packed_invariance(run, lengths, seeds=(21, 22, 23), alone=(0, 7, 31), dev=None):
+    """Bit-mismatch counts of a row-wise result on a packed batch of
+    sequences: the sequences re-packed in shuffled orders, and single
+    sequences run alone, each compared with the original packing's rows."""
+    import torch
+
+    def bits(t):
+        return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
+
+    if dev is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    offs = [0]
+    for n in lengths:
+        offs.append(offs[-1] + int(n))
+    T = offs[-1]
+    full = [x.clone() for x in run(torch.arange(T, device=dev))]
     out = {"rows_compared": 0, "mismatched_values": 0, "cases": []}
 
     def compare(rows, part):
@@ -338,34 +401,14 @@ def invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse):
         out["mismatched_values"] += n
         return n
 
-    dev = hidden.device
-    for bs, starts in ((1, (0, 1, T - 1)), (7, (0, 4093)), (256, (0, 8000))):
-        for r0 in starts:
-            rows = torch.arange(r0, r0 + bs, device=dev)
-            part = lmh.lmhead_logprob_fwd(hidden[r0:r0 + bs], weight, labels[r0:r0 + bs], s,
-                                          want_lse=True)
-            out["cases"].append({"batch": bs, "start": r0, "mismatched": compare(rows, part)})
-    for shift in (1, 63, 127):
-        rows = torch.arange(shift, min(T, shift + 1024), device=dev)
-        part = lmh.lmhead_logprob_fwd(hidden[rows].contiguous(), weight, labels[rows].contiguous(),
-                                      s, want_lse=True)
-        out["cases"].append({"batch": int(rows.numel()), "shift": shift,
-                             "mismatched": compare(rows, part)})
-    for seed in (11, 12, 13):  # three shuffled packings of the whole batch
-        perm = torch.randperm(T, generator=torch.Generator().manual_seed(seed)).to(dev)
-        part = lmh.lmhead_logprob_fwd(hidden[perm].contiguous(), weight,
-                                      labels[perm].contiguous(), s, want_lse=True)
-        out["cases"].append({"batch": T, "shuffled": seed, "mismatched": compare(perm, part)})
-    # the batch as T rows of a larger one: one more copy of the first 4096 rows after it
-    extra = torch.arange(0, min(T, 4096), device=dev)
-    rows = torch.cat([torch.arange(T, device=dev), extra])
-    part = lmh.lmhead_logprob_fwd(hidden[rows].contiguous(), weight, labels[rows].contiguous(), s,
-                                  want_lse=True)
-    n = sum(int((bits(a[:T]) != bits(b)).sum().item()) for a, b in zip(part, full))
-    out["rows_compared"] += T
-    out["mismatched_values"] += n
-    out["cases"].append({"batch": int(rows.numel()), "embedded_rows": T, "mismatched": n})
-    torch.cuda.synchronize()
+    for seed in seeds:
+        order = torch.randperm(len(lengths), generator=torch.Generator().manual_seed(seed)).tolist()
+        rows = torch.cat([torch.arange(offs[i], offs[i + 1], device=dev) for i in order])
+        out["cases"].append({"sequences_shuffled": seed, "mismatched": compare(rows, run(rows))})
+    for i in alone:
+        rows = torch.arange(offs[i], offs[i + 1], device=dev)
+        out["cases"].append({"sequence_alone": i, "rows": int(rows.numel()),
+                             "mismatched": compare(rows, run(rows))})
     return out
 
 
@@ -634,10 +677,23 @@ def run_gpu(args):
 
     # ------------------------------------------------- batch invariance (bit mismatches)
     # Forward outputs of the full batch against the same rows run as
-    # sub-batches of 1, 7 and 256 rows, shifted by 1..127 rows and in one
-    # shuffled packing; counted in fp32 bits (target 0).
+    # sub-batches of 1, 7 and 256 rows, shifted by 1..127 rows, in three
+    # shuffled packings and inside a larger batch; counted in fp32 bits
+    # (target 0). The backward's grad_hidden rows the same way, in bf16 bits
+    # (grad_weight sums over the batch's rows, so it has no per-row bits).
     if not args.no_extras:
         line["invariance"] = invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse)
+        lse_full = lse.clone()
+
+        def bwd_rows(rows):
+            gh_r, _ = lmh.lmhead_logprob_bwd(hidden[rows].contiguous(), weight,
+                                             labels[rows].contiguous(), grad[rows].contiguous(), s,
+                                             lse=lse_full[rows].contiguous())
+            return (gh_r,)
+
+        line["invariance_grad_hidden"] = invariance_cases(
+            bwd_rows, T, ((1, (0, T - 1)), (7, (4093,)), (256, (8000,))))
+        torch.cuda.empty_cache()
 
     # ------------------------------------------------------------- e2e (host buffers)
     h_host = hidden.cpu().pin_memory()
@@ -811,6 +867,10 @@ def run_gpu(args):
             "tflops_kernels": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12,
             "frac_of_burst_peak": 2.0 * T2 * H2 * V2 / (fk2 * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "peak_mem": peak_mem(ws2.numel())}
+        extras["fwd_only"]["T=4096 H=4096 V=32000"]["invariance"] = invariance_cases(
+            lambda rows: lmh.lmhead_logprob_fwd(h2[rows].contiguous(), w2, l2[rows].contiguous(),
+                                                1.0, want_lse=True),
+            T2, ((1, (0, T2 - 1)), (7, (0, 2045)), (256, (0, 3840))))
         del h2, w2
         # tiny fused forward T=64 H=256 V=4096: a latency figure, no roofline
         Tt, Ht, Vt = 64, 256, 4096
@@ -825,6 +885,11 @@ def run_gpu(args):
                               "ms_per_call": timed(fwdt, 50, 5),
                               "ms_kernels": kernel_ms(lmh, fwdt, 50, 5, fwd_kernels),
                               "peak_mem": peak_mem(wst.numel())}
+        # sub-batches of 1, 7 and the whole 64, windows shifted by 1..15
+        extras["tiny_fwd"]["invariance"] = invariance_cases(
+            lambda rows: lmh.lmhead_logprob_fwd(ht_[rows].contiguous(), wt_, lt_[rows].contiguous(),
+                                                1.0, want_lse=True),
+            Tt, ((1, (0, 1, 63)), (7, (0, 57)), (64, (0,))), window=48, shifts=(1, 7, 15), embed=64)
         del ht_, wt_
         # packed variable-length batch: 32 sequences of seeded lengths in
         # [128, 4096], concatenated; H=5120 V=152064; one fwd+bwd step
@@ -854,7 +919,19 @@ def run_gpu(args):
             "ms_kernels_per_step": p_ms, "tokens_per_s": Tp / (p_ms * 1e-3),
             "tflops_as_executed": p_tf, "frac_of_sustained": p_tf / peak,
             "peak_mem": peak_mem(wsfp.numel() + wsbp.numel())}
-        del hp, wp, ghp, gwp, wsfp, wsbp
+        del ghp, gwp, wsfp, wsbp
+        torch.cuda.empty_cache()
+
+        # the same rows re-packed: sequences in shuffled orders, and alone
+        def packed_rows(rows):
+            h_r, l_r = hp[rows].contiguous(), lbp[rows].contiguous()
+            lp_r, ent_r, lse_r = lmh.lmhead_logprob_fwd(h_r, wp, l_r, 1.0, want_lse=True)
+            gh_r, _ = lmh.lmhead_logprob_bwd(h_r, wp, l_r, gp[rows].contiguous(), 1.0, lse=lse_r)
+            return lp_r, ent_r, lse_r, gh_r
+
+        extras["packed_varlen_fwd_bwd"]["invariance"] = packed_invariance(
+            packed_rows, W.packed_lengths())
+        del hp, wp
         torch.cuda.empty_cache()
         # logits path: bf16 logits [8192, 152064] (2.49 GB > L2)
         T3, V3 = 8192, 152064
@@ -896,6 +973,10 @@ def run_gpu(args):
                          "traffic": traffic_for("logits_rowwise"),
                          "algorithmic_bytes_per_launch": T3 * V3 * 2},
             "clocks": l_clk, "peak_mem": peak_mem(0)}
+        extras["logits_path"]["invariance"] = invariance_cases(
+            lambda rows: lmh.logprob_from_logits(x[rows].contiguous(), l3[rows].contiguous(), 1.0,
+                                                 want_lse=True),
+            T3, ((1, (0, T3 - 1)), (7, (0, 4093)), (256, (0, 7936))))
         # sampler-parity (division) form on the same logits, and the mismatch
         # counts against torch's own fp32 sampler formula on the GPU
         temps = torch.full((T3,), 0.7, dtype=torch.float32, device=dev)

@@ -88,3 +88,45 @@ def test_backward_rooflines():
     # a long batch: all flops
     assert bench.bwd_joint_roofline_ms(16384, H, V, peaks) == pytest.approx(
         6.0 * 16384 * H * V / 2000e12 * 1e3, rel=1e-12)
+
+
+def test_invariance_cases_count_only_real_mismatches():
+    # a row-wise map has no mismatch in any case; one that depends on the
+    # batch size (a per-batch offset) is caught in every case but the whole
+    # batch, and so is one whose rows see their position in the batch
+    import torch
+
+    x = torch.randn(300, 5, generator=torch.Generator().manual_seed(3))
+    cpu = torch.device("cpu")
+    subs = ((1, (0, 299)), (7, (0, 100)), (64, (5,)))
+    row_wise = bench.invariance_cases(lambda r: (x[r] * 2.0, (x[r] + 1).to(torch.bfloat16)), 300,
+                                      subs, window=128, dev=cpu)
+    assert row_wise["mismatched_values"] == 0
+    assert len(row_wise["cases"]) == 5 + 3 + 3 + 1
+    assert row_wise["rows_compared"] == 2 + 14 + 64 + 3 * 128 + 3 * 300 + 300
+    by_size = bench.invariance_cases(lambda r: (x[r] + float(r.numel()),), 300, subs,
+                                     window=128, dev=cpu)
+    assert all(c["mismatched"] > 0 for c in by_size["cases"]
+               if c.get("batch") not in (300, None) or "embedded_rows" in c)
+    assert all(c["mismatched"] == 0 for c in by_size["cases"] if "shuffled" in c)
+    by_pos = bench.invariance_cases(lambda r: (x[r] + torch.arange(r.numel()).float()[:, None],),
+                                    300, subs, window=128, dev=cpu)
+    # (the embedded case keeps every row's position, so it cannot show this one)
+    assert all(c["mismatched"] > 0 for c in by_pos["cases"]
+               if c.get("start", 1) != 0 and "embedded_rows" not in c)
+
+
+def test_packed_invariance_over_sequences():
+    import torch
+
+    lengths = (5, 9, 3, 12, 7, 4, 8, 6)
+    T = sum(lengths)
+    x = torch.randn(T, 3, generator=torch.Generator().manual_seed(4))
+    cpu = torch.device("cpu")
+    ok = bench.packed_invariance(lambda r: (x[r].exp(),), lengths, seeds=(1, 2), alone=(0, 3, 7),
+                                 dev=cpu)
+    assert ok["mismatched_values"] == 0 and ok["rows_compared"] == 2 * T + 5 + 12 + 6
+    # a result that depends on the packing (each row plus the batch mean) is caught
+    bad = bench.packed_invariance(lambda r: (x[r] + x[r].mean(),), lengths, seeds=(1,),
+                                  alone=(3,), dev=cpu)
+    assert bad["cases"][-1]["mismatched"] > 0
