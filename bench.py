@@ -217,6 +217,29 @@ def oracle_step(sample):
     oracle.fused_backward(h, w, lab, g, s)
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it: the model name where the kernel
+    gives one (x86), else the architecture with the Arm implementer and part
+    numbers of the first core."""
+    import platform
+
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = (x.strip() for x in line.split(":", 1))
+                    fields.setdefault(k, v)
+    except OSError:
+        pass
+    if fields.get("model name"):
+        return fields["model name"]
+    if "CPU implementer" in fields:
+        return (f"{platform.machine()} (implementer {fields['CPU implementer']}, "
+                f"part {fields.get('CPU part', '?')})")
+    return platform.machine() or "unknown"
+
+
 def cpu_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -237,7 +260,8 @@ def cpu_baseline(target_s: float = 15.0, rows: int = 128):
         dt = time.perf_counter() - t0
         if dt >= target_s or n >= 50:
             break
-    return {"value": rows * n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+    return {"value": rows * n / dt, "unit": "tokens/s", "cores": cpu_cores(), "cpu": cpu_model(),
+            "kind": "oracle",
             "sample": f"{rows} rows of the workload (full H={H_}, V={V_}), fp64 forward+backward "
                       f"incl. grad_weight over the sampled rows, repeated {n}x in {dt:.1f} s"}
 
@@ -267,7 +291,8 @@ def cpu_oracle_logits(target_s: float = 3.0, rows: int = 64, divide: bool = Fals
         dt = time.perf_counter() - t0
         if dt >= target_s or n >= 100:
             break
-    return {"value": rows * n / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+    return {"value": rows * n / dt, "unit": "tokens/s", "cores": cpu_cores(), "cpu": cpu_model(),
+            "kind": "oracle",
             "sample": f"{rows} rows of the logits workload (V={W.LOGITS.V}), fp64, "
                       f"repeated {n}x in {dt:.1f} s"}
 
@@ -298,7 +323,8 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "T": T_, "H": H_, "V": V_,
                    "inv_temperature": inv_temperature(),
                    "sample_rows_per_step": rows, "l2": "host run; not applicable"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "cpu": cpu_model(), "kind": "oracle",
                          "sample": f"{rows} rows per step of the workload (full H, V), fp64 "
                                    f"forward+backward"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -130,3 +130,8 @@ def test_packed_invariance_over_sequences():
     bad = bench.packed_invariance(lambda r: (x[r] + x[r].mean(),), lengths, seeds=(1,),
                                   alone=(3,), dev=cpu)
     assert bad["cases"][-1]["mismatched"] > 0
+
+
+def test_cpu_model_names_the_host():
+    name = bench.cpu_model()
+    assert isinstance(name, str) and name and name != "unknown"
