@@ -701,27 +701,9 @@ def run_gpu(args):
                                                     / peak, 4)},
     }
 
-    # ------------------------------------------------- batch invariance (bit mismatches)
-    # Forward outputs of the full batch against the same rows run as
-    # sub-batches of 1, 7 and 256 rows, shifted by 1..127 rows, in three
-    # shuffled packings and inside a larger batch; counted in fp32 bits
-    # (target 0). The backward's grad_hidden rows the same way, in bf16 bits
-    # (grad_weight sums over the batch's rows, so it has no per-row bits).
-    if not args.no_extras:
-        line["invariance"] = invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse)
-        lse_full = lse.clone()
-
-        def bwd_rows(rows):
-            gh_r, _ = lmh.lmhead_logprob_bwd(hidden[rows].contiguous(), weight,
-                                             labels[rows].contiguous(), grad[rows].contiguous(), s,
-                                             lse=lse_full[rows].contiguous())
-            return (gh_r,)
-
-        line["invariance_grad_hidden"] = invariance_cases(
-            bwd_rows, T, ((1, (0, T - 1)), (7, (4093,)), (256, (8000,))))
-        torch.cuda.empty_cache()
-
     # ------------------------------------------------------------- e2e (host buffers)
+    # Timed right after the device-resident step, before any other leg, so
+    # that both see the same clocks under the power cap.
     h_host = hidden.cpu().pin_memory()
     w_host = weight.cpu().pin_memory()
     l_host = labels.cpu().pin_memory()
@@ -756,6 +738,26 @@ def run_gpu(args):
                            "the forward) + lmhead_logprob_bwd; logprob and entropy to host",
                    "h2d_copy_gbs": round(h2d_gbs, 1)}
     del h_host, w_host
+
+    # ------------------------------------------------- batch invariance (bit mismatches)
+    # Forward outputs of the full batch against the same rows run as
+    # sub-batches of 1, 7 and 256 rows, shifted by 1..127 rows, in three
+    # shuffled packings and inside a larger batch; counted in fp32 bits
+    # (target 0). The backward's grad_hidden rows the same way, in bf16 bits
+    # (grad_weight sums over the batch's rows, so it has no per-row bits).
+    if not args.no_extras:
+        line["invariance"] = invariance_counts(lmh, hidden, weight, labels, s, lp, ent, lse)
+        lse_full = lse.clone()
+
+        def bwd_rows(rows):
+            gh_r, _ = lmh.lmhead_logprob_bwd(hidden[rows].contiguous(), weight,
+                                             labels[rows].contiguous(), grad[rows].contiguous(), s,
+                                             lse=lse_full[rows].contiguous())
+            return (gh_r,)
+
+        line["invariance_grad_hidden"] = invariance_cases(
+            bwd_rows, T, ((1, (0, T - 1)), (7, (4093,)), (256, (8000,))))
+        torch.cuda.empty_cache()
 
     if ws == 1 and not args.no_extras:
         # forward only, same workload
