@@ -306,7 +306,9 @@ int logprob_from_logits_div(const uint16_t* logits, const int32_t* labels, int64
  * work already enqueued on `stream` (an event recorded on `stream` at entry),
  * and `stream` waits for every copy before the kernels that read it, so all of
  * the call is ordered on `stream` as if it ran there. Nothing is allocated on
- * the device; the library keeps a copy stream and a few events per device.
+ * the device; the library keeps a copy stream and a few events per device,
+ * created by this entry point's first call (which therefore comes before any
+ * stream capture of it).
  * Everything else (workspace, sizes, errors) as lmhead_logprob_fwd.
  */
 int lmhead_logprob_fwd_host(const uint16_t* hidden_host, const uint16_t* weight_host,

@@ -57,6 +57,32 @@ std::atomic<unsigned long long> g_launches{0};
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// ------------------------------------------------------------ backward side stream
+// Per device: a second stream of the library's own (non-blocking, created by
+// the device's first call of any entry point, so that no later call under
+// stream capture creates it) and two events. The backward runs grad_hidden on it beside
+// grad_weight: both read the chunk's dl and write different outputs. Fork and
+// join are an event record plus a stream wait each way, so under stream
+// capture the two become parallel branches of the graph. The mutex keeps one
+// call's records and waits together when several host threads call at once.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+SideStream g_side[kMaxDevices];
+
+int side_stream_init(SideStream& sd) {
+  cudaError_t e = cudaSuccess;
+  if (!sd.st && (e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaStreamCreate: %s", cudaGetErrorString(e));
+  if (!sd.fork && (e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
+  if (!sd.join && (e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess)
+    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
+  return LMH_OK;
+}
+
 // Per-device facts, queried once with that device current.
 int device_info(DeviceInfo** out) {
   int dev = 0;
@@ -90,6 +116,8 @@ int device_info(DeviceInfo** out) {
         return fail(LMH_ERR_LAUNCH, "cuTensorMapEncodeTiled unavailable");
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
+    const int rc_side = side_stream_init(g_side[dev]);
+    if (rc_side != LMH_OK) return rc_side;
     d.ready = true;
   }
   *out = &d;
@@ -482,31 +510,6 @@ struct BwdOpts {
 //                          into grad_hidden_f32 (a vocab shard's partial)
 //   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
 //   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
-// ------------------------------------------------------------ backward side stream
-// Per device: a second stream of the library's own (non-blocking, created on
-// first use) and two events. The backward runs grad_hidden on it beside
-// grad_weight: both read the chunk's dl and write different outputs. Fork and
-// join are an event record plus a stream wait each way, so under stream
-// capture the two become parallel branches of the graph. The mutex keeps one
-// call's records and waits together when several host threads call at once.
-struct SideStream {
-  cudaStream_t st = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  std::mutex mu;
-};
-SideStream g_side[kMaxDevices];
-
-int side_stream_init(SideStream& sd) {
-  cudaError_t e = cudaSuccess;
-  if (!sd.st && (e = cudaStreamCreateWithFlags(&sd.st, cudaStreamNonBlocking)) != cudaSuccess)
-    return fail(LMH_ERR_LAUNCH, "cudaStreamCreate: %s", cudaGetErrorString(e));
-  if (!sd.fork && (e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)) != cudaSuccess)
-    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
-  if (!sd.join && (e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)) != cudaSuccess)
-    return fail(LMH_ERR_LAUNCH, "cudaEventCreate: %s", cudaGetErrorString(e));
-  return LMH_OK;
-}
-
 // One fork of the side stream from `main`; the destructor joins a fork that
 // an error left open, so `main` never runs ahead of the side stream's work.
 struct SideBranch {
@@ -611,10 +614,8 @@ int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* 
   };
   const int64_t first_rows = T < o.row_chunk ? T : o.row_chunk;
   const int64_t last_rows = T % o.row_chunk == 0 ? first_rows : T % o.row_chunk;
-  // The side stream is set up by every backward call, used or not, so that a
-  // later call under stream capture creates nothing.
   int dev_id = 0;
-  cudaGetDevice(&dev_id);  // in range: device_info accepted it
+  cudaGetDevice(&dev_id);  // in range: device_info accepted it (and made the side stream)
   SideStream* side = &g_side[dev_id];
   std::unique_lock<std::mutex> side_lock(side->mu);
   LMH_TRY(side_stream_init(*side));
