@@ -60,11 +60,12 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // ------------------------------------------------------------ backward side stream
 // Per device: a second stream of the library's own (non-blocking, created by
 // the device's first call of any entry point, so that no later call under
-// stream capture creates it) and two events. The backward runs grad_hidden on it beside
-// grad_weight: both read the chunk's dl and write different outputs. Fork and
-// join are an event record plus a stream wait each way, so under stream
-// capture the two become parallel branches of the graph. The mutex keeps one
-// call's records and waits together when several host threads call at once.
+// stream capture creates it) and two events. The backward runs grad_hidden
+// on it beside grad_weight: both read the chunk's dl and write different
+// outputs. Fork and join are an event record plus a stream wait each way, so
+// under stream capture the two become parallel branches of the graph. The
+// mutex keeps one call's records and waits together when several host
+// threads call at once.
 struct SideStream {
   cudaStream_t st = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
@@ -503,13 +504,6 @@ struct BwdOpts {
   int64_t row_chunk = lmh::kBwdRowChunk;
 };
 
-// Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
-// chunk of o.row_chunk rows, in ascending order:
-//   dl   = recomputed logits -> dlogits (bf16 [rows][Vpad])
-//   dH   = dl * W          (A = dl K-major, B = W MN-major); bf16, or fp32
-//                          into grad_hidden_f32 (a vocab shard's partial)
-//   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
-//   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
 // One fork of the side stream from `main`; the destructor joins a fork that
 // an error left open, so `main` never runs ahead of the side stream's work.
 struct SideBranch {
@@ -559,6 +553,15 @@ int bwd_overlap_mode() {
   return mode;
 }
 
+// Backward of sum_t g[t] * logprob[t] (+ gH[t] * entropy[t]) for every row
+// chunk of o.row_chunk rows, in ascending order:
+//   dl   = recomputed logits -> dlogits (bf16 [rows][Vpad])
+//   dH   = dl * W          (A = dl K-major, B = W MN-major); bf16, or fp32
+//                          into grad_hidden_f32 (a vocab shard's partial)
+//   hT   = hidden^T of the chunk (a transpose kernel, so the next A is K-major)
+//   dW^T (+)= hT * dl      (A = hT K-major, B = dl MN-major; stored transposed)
+// Chunks of up to kBwdOverlapMaxRows rows run dH on the side stream beside hT
+// and dW^T.
 int run_backward(const uint16_t* hidden, const uint16_t* weight, const int32_t* labels,
                  const float* grad_lp, const float* grad_ent, const float* lse, const float* ent,
                  int64_t T, int64_t H, int64_t V, float s, uint16_t* grad_hidden,
