@@ -1,6 +1,8 @@
 """Seeded random shapes through every entry point, against the oracle: ragged
 T, H and V (tails of every tile size), random out-of-vocab labels and
-temperatures, and a sub-batch of each case checked for bit-identity."""
+temperatures, and a sub-batch of each case checked for bit-identity. A second
+set spans 700 to 2600 rows, across the 1024-row chunks up to which the
+backward runs grad_hidden beside grad_weight (and picks other engines)."""
 
 import numpy as np
 import pytest
@@ -13,11 +15,11 @@ from helpers import ATOL_LOGPROB, RTOL_FROB_GRAD, f64, fused_case, max_abs, rel_
 pytestmark = pytest.mark.gpu
 
 
-def _shapes(n=16, seed=77):
+def _shapes(n=16, seed=77, t_lo=1, t_hi=700):
     rng = np.random.default_rng(seed)
     out = []
     for _ in range(n):
-        T = int(rng.integers(1, 700))
+        T = int(rng.integers(t_lo, t_hi))
         H = 8 * int(rng.integers(1, 80))
         V = int(rng.integers(1, 6000))
         s = float(np.float32(rng.uniform(0.5, 2.0)))
@@ -37,7 +39,7 @@ def lmh():
     return m
 
 
-@pytest.mark.parametrize("T,H,V,s", _shapes())
+@pytest.mark.parametrize("T,H,V,s", _shapes() + _shapes(n=8, seed=78, t_lo=700, t_hi=2600))
 def test_random_shape_all_paths(lmh, T, H, V, s):
     import torch
 
