@@ -554,6 +554,24 @@ def bwd_joint_roofline_ms(T, H, V, peaks):
     return max(flop_ms, nbytes / (peaks["hbm_gbs"] * 1e9) * 1e3)
 
 
+def timed_steps(fn, steps, warmup):
+    """Mean ms per call over `steps` calls (total time / steps, as timed()),
+    and each call's own ms: an event on the current stream after every call."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record()
+    for i in range(steps):
+        fn()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    return evs[0].elapsed_time(evs[-1]) / steps, per
+
+
 def timed(fn, steps, warmup):
     import torch
 
@@ -730,13 +748,20 @@ def run_gpu(args):
     torch.cuda.synchronize()
     h2d_gbs = w_host.numel() * 2 / (c0.elapsed_time(c1) * 1e-3) / 1e9
     barrier(ws)
-    e2e_ms = reduce_max(timed(e2e_step, args.steps, 2) * args.steps, ws, dev)
+    e2e_mean, e2e_per = timed_steps(e2e_step, args.steps, 2)
+    e2e_ms = reduce_max(e2e_mean * args.steps, ws, dev)
+    e2e_sorted = sorted(e2e_per)
     h2d = sum(t.numel() * t.element_size() for t in (h_host, w_host, l_host, g_host))
     line["e2e"] = {"value": aggregate_tokens_per_s(T, ws, args.steps, e2e_ms), "unit": "tokens/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 2 * T * 4,
                    "path": "lmhead_logprob_fwd_host (pinned host inputs, copies overlapped with "
                            "the forward) + lmhead_logprob_bwd; logprob and entropy to host",
-                   "h2d_copy_gbs": round(h2d_gbs, 1)}
+                   "h2d_copy_gbs": round(h2d_gbs, 1),
+                   # this rank's steps one by one (events after every step): the host-staged
+                   # copies make single steps vary more than the device-resident ones
+                   "ms_per_step_min_median_max": [round(e2e_sorted[0], 3),
+                                                  round(e2e_sorted[len(e2e_sorted) // 2], 3),
+                                                  round(e2e_sorted[-1], 3)]}
     del h_host, w_host
 
     # ------------------------------------------------- batch invariance (bit mismatches)
